@@ -1,0 +1,162 @@
+/*
+ * mla_dcp.h -- C ABI of the sequence-sharded MLA decode library (sm_103a).
+ *
+ * The operation is the data-parallel core of Decode Context Parallelism
+ * ("Decode Context Parallelism", sections 4 and 4.1): the latent KV cache of
+ * a multi-head latent attention (MLA) model is split along the sequence;
+ * every shard attends the full query over only its slice and emits a partial
+ * output plus a log-sum-exp (LSE); a combine step reweights the partials by
+ * their LSEs, optionally fused with the per-head value up-projection
+ * ("Kimi K3 in vLLM: Specialized CuTe DSL Decode on NVIDIA GB300",
+ * section 1).  On one GPU the N shards are logical partitions of the cache.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must be device memory of the current CUDA
+ *     device, 16-byte aligned.  The caller owns every buffer; the library
+ *     keeps no pointer after a call returns and allocates no device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Argument errors are detected on
+ *     the host and returned before anything is launched.
+ *   - No C++ exception crosses this boundary.
+ *   - Results are deterministic: the same inputs give bitwise-identical
+ *     outputs (fixed reduction order, no atomics on data).
+ *
+ * Layouts (row-major, bf16 = IEEE bfloat16 bit patterns in uint16):
+ *   q            bf16  [B, q_len, H, 576]  absorbed queries: 512 latent + 64 rope
+ *   kv data      bf16  [num_pages, 64, 576]  latent rows [c_kv(512) | k_rope(64)]
+ *                e4m3  [num_pages, 64, 576]  (fp8 caches, OCP e4m3 codes)
+ *   kv scale     fp32  [num_pages, 64]     fp8 only: value = e4m3(code) * scale
+ *   block_table  int32 [B, max_pages_per_req]  page of token t of request b is
+ *                                          block_table[b][t / 64], row t % 64
+ *   seq_lens     int32 [B]                 context length L_b (>= 1), device
+ *   out_partial  fp32  [n_out, B, q_len, H, 512]  normalised partial outputs
+ *   lse_partial  fp32  [n_out, B, q_len, H]       natural-log LSE, -inf if empty
+ *   w_uv         bf16  [H, 512, 128]       per-head value up-projection
+ *   out          bf16  [B, q_len, H, 512]  (or [B, q_len, H, 128] with w_uv)
+ *   lse_out      fp32  [B, q_len, H]
+ */
+#ifndef MLA_DCP_H_
+#define MLA_DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID = -1,       /* bad argument; nothing was launched */
+  MLA_ERR_UNSUPPORTED = -2,   /* well-formed but outside what this build supports */
+  MLA_ERR_CUDA = -3,          /* a CUDA runtime or driver call failed */
+  MLA_ERR_TIMEOUT = -4,       /* a device-side wait gave up (from mla_get_device_error) */
+  MLA_ERR_DEVICE_BOUNDS = -5, /* a block-table entry was outside [0, num_pages) */
+  MLA_ERR_WORKSPACE = -6      /* workspace missing or smaller than mla_workspace_size() */
+} mla_status;
+
+/* Which token positions of a request belong to shard s of N
+ * ("Decode Context Parallelism", section 4):
+ *   INTERLEAVED  t mod N == s                  (N must divide 64)
+ *   CONTIGUOUS   s*c <= t < min((s+1)*c, L),   c = ceil(L / N)
+ * The section's worked example (a 200K-token request on 4 GPUs holding
+ * 0-50K, 50K-100K, 100K-150K, 150K-200K) is the CONTIGUOUS layout. */
+typedef enum mla_layout { MLA_LAYOUT_INTERLEAVED = 0, MLA_LAYOUT_CONTIGUOUS = 1 } mla_layout;
+
+typedef enum mla_kv_dtype { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+
+/* Decode-step shape.  num_heads must be a multiple of 16.  With causal != 0
+ * (a speculative verify step of q_len = 1 + drafts tokens whose KV is the
+ * last q_len entries of the cache), query i sees tokens t <= L - q_len + i. */
+typedef struct mla_shape {
+  int batch;            /* B >= 1 */
+  int q_len;            /* query tokens per request >= 1 */
+  int num_heads;        /* H: multiple of 16 */
+  int causal;           /* 0 or 1 */
+  float softmax_scale;  /* logits = softmax_scale * q . k  (1/sqrt(192) for the workloads here) */
+} mla_shape;
+
+/* The paged latent cache (device memory, not modified). */
+typedef struct mla_kv_pages {
+  const void* data;     /* [num_pages, page_size, 576] bf16 or e4m3 */
+  const float* scale;   /* fp8 only: [num_pages, page_size]; must be NULL for bf16 */
+  mla_kv_dtype dtype;
+  int num_pages;        /* >= 1 */
+  int page_size;        /* must be 64 */
+} mla_kv_pages;
+
+/* shard_id value that computes every shard 0..N-1 in one call (n_out = N). */
+#define MLA_ALL_SHARDS (-1)
+
+/*
+ * Bytes of device workspace mla_decode_partial needs for this shape on the
+ * current device (work list, split-piece partials and an error word).
+ * Returns 0 for invalid arguments.
+ */
+size_t mla_workspace_size(const mla_shape* shape, int num_shards, int shard_id);
+
+/*
+ * Per-shard partial attention ("Decode Context Parallelism", section 4.1,
+ * the "Compute" step; section 5.3: each rank attends over its latent slice).
+ * For every request b, query row (i, h) and computed shard s, over the tokens
+ * T_s of request b that shard s owns (see mla_layout) and the query may see:
+ *     s_t = softmax_scale * q[b,i,h,:] . K_t            (K_t = cache row, 576 wide)
+ *     lse_partial = ln sum_{t in T_s} exp(s_t)           (-inf if T_s is empty)
+ *     out_partial = sum_{t in T_s} exp(s_t - lse) * K_t[0:512]   (0 if empty)
+ * shard_id = MLA_ALL_SHARDS computes all N shards (out_partial holds N
+ * slices, shard-major); shard_id in [0, N) computes that shard only
+ * (n_out = 1), which is the per-GPU call of a multi-GPU deployment.
+ *
+ * Arguments: q, block_table, seq_lens, out_partial, lse_partial, workspace:
+ * device pointers, layouts above.  max_pages_per_req: row stride of
+ * block_table; it must cover ceil(L_b / 64) entries of every request (only
+ * those entries are read).  num_shards: 1..8.  workspace_bytes must be at
+ * least mla_workspace_size(shape, num_shards, shard_id).
+ *
+ * Errors: MLA_ERR_INVALID / MLA_ERR_UNSUPPORTED / MLA_ERR_WORKSPACE before
+ * any launch; MLA_ERR_CUDA if a launch fails.  Device-side problems (a
+ * block-table entry out of range, which then reads as zeros; a wait that
+ * timed out) are recorded in the workspace and read with
+ * mla_get_device_error.
+ */
+mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                              int max_pages_per_req, const int32_t* seq_lens,
+                              const mla_shape* shape, int shard_id, int num_shards,
+                              mla_layout layout, float* out_partial, float* lse_partial,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * LSE combine of N shard partials ("Decode Context Parallelism", section 4.1:
+ * partial outputs reweighted by their LSE and summed into the true output):
+ *     M = max_s lse_s,  w_s = exp(lse_s - M),  lse_out = M + ln sum_s w_s
+ *     o = sum_s w_s out_s / sum_s w_s                  (fp32)
+ *     out = bf16(o)                                    if w_uv == NULL
+ *     out = bf16(o . w_uv[h])  ([B,q_len,H,128])       otherwise (the fused
+ *           v-projection of "Kimi K3 in vLLM ...", section 1)
+ * partials / lses: as written by mla_decode_partial with MLA_ALL_SHARDS (or
+ * the N per-shard slices stacked shard-major).  lse_out may be NULL.
+ * A row whose shards are all empty gives out = 0 and lse_out = -inf.
+ */
+mla_status mla_shard_combine(const float* partials, const float* lses, int num_shards,
+                             const mla_shape* shape, const void* w_uv, void* out, float* lse_out,
+                             void* stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device error word kept in
+ * `workspace` by the last mla_decode_partial on it.  Returns MLA_OK,
+ * MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT (timeout wins if both) or
+ * MLA_ERR_CUDA.
+ */
+mla_status mla_get_device_error(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DCP_H_ */

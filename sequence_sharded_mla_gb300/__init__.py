@@ -1,0 +1,199 @@
+"""Sequence-sharded MLA decode for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/mla_dcp.h``: it checks tensor
+dtypes/devices, allocates outputs and workspace with PyTorch and passes raw
+pointers and the current CUDA stream to ``libmla_dcp.so``.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.
+If the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+D_QK, D_V, D_UV, PAGE = 576, 512, 128, 64
+ALL_SHARDS = -1
+DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
+LAYOUTS = {"interleaved": 0, "contiguous": 1}
+KV_BF16, KV_FP8 = 0, 1
+
+STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_CUDA",
+          -4: "MLA_ERR_TIMEOUT", -5: "MLA_ERR_DEVICE_BOUNDS", -6: "MLA_ERR_WORKSPACE"}
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class mla_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("num_heads", ctypes.c_int),
+                ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+class mla_kv_pages(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("dtype", ctypes.c_int),
+                ("num_pages", ctypes.c_int), ("page_size", ctypes.c_int)]
+
+
+_LIB = None
+EXPORTS = ("mla_decode_partial", "mla_shard_combine", "mla_workspace_size",
+           "mla_get_device_error", "mla_status_string", "mla_version")
+
+
+def lib():
+    """Load (building first if the sources are newer) ``libmla_dcp.so``."""
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.mla_decode_partial.argtypes = [vp, ctypes.POINTER(mla_kv_pages), vp, i32, vp,
+                                         ctypes.POINTER(mla_shape), i32, i32, i32, vp, vp, vp,
+                                         sz, vp]
+        L.mla_decode_partial.restype = i32
+        L.mla_shard_combine.argtypes = [vp, vp, i32, ctypes.POINTER(mla_shape), vp, vp, vp, vp]
+        L.mla_shard_combine.restype = i32
+        L.mla_workspace_size.argtypes = [ctypes.POINTER(mla_shape), i32, i32]
+        L.mla_workspace_size.restype = sz
+        L.mla_get_device_error.argtypes = [vp, vp]
+        L.mla_get_device_error.restype = i32
+        L.mla_status_string.argtypes = [i32]
+        L.mla_status_string.restype = ctypes.c_char_p
+        L.mla_version.argtypes = []
+        L.mla_version.restype = i32
+        _LIB = L
+    return _LIB
+
+
+def _shape(batch, q_len, num_heads, causal, softmax_scale):
+    return mla_shape(int(batch), int(q_len), int(num_heads), int(bool(causal)),
+                     float(softmax_scale))
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtypes, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def mla_workspace_size(batch, q_len, num_heads, num_shards, shard_id=ALL_SHARDS, causal=False,
+                       softmax_scale=DEFAULT_SCALE) -> int:
+    sh = _shape(batch, q_len, num_heads, causal, softmax_scale)
+    return int(lib().mla_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
+
+
+def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
+                       shard_id=ALL_SHARDS, kv_scale=None, causal=False,
+                       softmax_scale=DEFAULT_SCALE, out_partial=None, lse_partial=None,
+                       workspace=None, stream=None):
+    """Per-shard partial attention; returns (out_partial, lse_partial, workspace).
+
+    q: bf16 [B, q_len, H, 576]; kv: bf16 [P, 64, 576] or e4m3 codes
+    (uint8 / float8_e4m3fn) [P, 64, 576] with kv_scale fp32 [P, 64];
+    block_table: int32 [B, max_pages]; seq_lens: int32 [B] (device).
+    out_partial: fp32 [n_out, B, q_len, H, 512]; lse_partial: fp32 [n_out, B, q_len, H].
+    """
+    _check(q, "q", (torch.bfloat16,), 4)
+    dev = q.device
+    B, q_len, H, d = q.shape
+    if d != D_QK:
+        raise ValueError("q must be [B, q_len, H, 576]")
+    if kv.dtype == torch.bfloat16:
+        kv_dtype = KV_BF16
+        if kv_scale is not None:
+            raise ValueError("kv_scale is only for fp8 caches")
+    elif kv.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        kv_dtype = KV_FP8
+        if kv_scale is None:
+            raise ValueError("fp8 caches need kv_scale")
+        _check(kv_scale, "kv_scale", (torch.float32,), 2, dev)
+    else:
+        raise TypeError(f"kv dtype {kv.dtype} unsupported")
+    _check(kv, "kv", (kv.dtype,), 3, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
+    n_out = num_shards if shard_id == ALL_SHARDS else 1
+    if out_partial is None:
+        out_partial = torch.empty((n_out, B, q_len, H, D_V), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
+    _check(out_partial, "out_partial", (torch.float32,), 5, dev)
+    _check(lse_partial, "lse_partial", (torch.float32,), 4, dev)
+    sh = _shape(B, q_len, H, causal, softmax_scale)
+    need = int(lib().mla_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
+                         kv_dtype, kv.shape[0], kv.shape[1])
+    st = lib().mla_decode_partial(_ptr(q), ctypes.byref(pages), _ptr(block_table),
+                                  block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
+                                  int(shard_id), int(num_shards), LAYOUTS[layout],
+                                  _ptr(out_partial), _ptr(lse_partial), _ptr(workspace),
+                                  workspace.numel(), _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "mla_decode_partial")
+    return out_partial, lse_partial, workspace
+
+
+def mla_shard_combine(partials, lses, w_uv=None, out=None, lse_out=None, stream=None,
+                      causal=False, softmax_scale=DEFAULT_SCALE):
+    """LSE combine (optionally fused with W_UV); returns (out, lse_out).
+
+    partials: fp32 [N, B, q_len, H, 512]; lses: fp32 [N, B, q_len, H];
+    w_uv: bf16 [H, 512, 128] or None.  out: bf16 [B, q_len, H, 512|128].
+    """
+    _check(partials, "partials", (torch.float32,), 5)
+    dev = partials.device
+    N, B, q_len, H, d = partials.shape
+    _check(lses, "lses", (torch.float32,), 4, dev)
+    if w_uv is not None:
+        _check(w_uv, "w_uv", (torch.bfloat16,), 3, dev)
+    width = D_UV if w_uv is not None else D_V
+    if out is None:
+        out = torch.empty((B, q_len, H, width), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    sh = _shape(B, q_len, H, causal, softmax_scale)
+    st = lib().mla_shard_combine(_ptr(partials), _ptr(lses), int(N), ctypes.byref(sh),
+                                 _ptr(w_uv), _ptr(out), _ptr(lse_out), _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "mla_shard_combine")
+    return out, lse_out
+
+
+def mla_get_device_error(workspace, stream=None) -> int:
+    """Sync the stream, read and clear the device error word; returns a status code."""
+    return int(lib().mla_get_device_error(_ptr(workspace), _stream_ptr(stream)))
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(int(status)).decode()
+
+
+def mla_version() -> int:
+    return int(lib().mla_version())

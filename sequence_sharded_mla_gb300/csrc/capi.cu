@@ -1,0 +1,255 @@
+// Host side of the C ABI declared in include/mla_dcp.h: argument checks,
+// workspace layout, TMA descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/mla_dcp.h"
+#include "common.cuh"
+
+namespace mla {
+int partial_smem_bytes();
+cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                const PartialParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
+                        int min_tiles, cudaStream_t stream);
+cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
+                         const float* ws_o, const float* ws_lse, float* out_partial,
+                         float* lse_partial, int num_units, cudaStream_t stream);
+cudaError_t launch_combine(const float* partials, const float* lses, int num_shards, int rows,
+                           uint16_t* out, float* lse_out, cudaStream_t stream);
+cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
+                               int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
+                               float* lse_out, cudaStream_t stream);
+}  // namespace mla
+
+using namespace mla;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // device waits give up after 2 s
+constexpr int kMinTilesPerCta = 4;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+struct WsLayout {
+  size_t hdr, prefix, ws_o, ws_lse, total;
+};
+
+WsLayout ws_layout(int num_units, int grid) {
+  auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  WsLayout w;
+  w.hdr = 0;
+  w.prefix = up(sizeof(WsHeader));
+  w.ws_o = w.prefix + up(sizeof(int) * (size_t)(num_units + 1));
+  w.ws_lse = w.ws_o + up(sizeof(float) * (size_t)grid * 2 * kRows * kDv);
+  w.total = w.ws_lse + up(sizeof(float) * (size_t)grid * 2 * kRows);
+  return w;
+}
+
+bool shape_ok(const mla_shape* s) {
+  return s != nullptr && s->batch >= 1 && s->q_len >= 1 && s->num_heads >= 1 &&
+         (s->causal == 0 || s->causal == 1) && std::isfinite(s->softmax_scale) &&
+         s->softmax_scale > 0.f && (long long)s->batch * s->q_len * s->num_heads < (1LL << 30);
+}
+
+int units_for(const mla_shape* s, int num_shards, int shard_id) {
+  int n_out = shard_id == MLA_ALL_SHARDS ? num_shards : 1;
+  int G = ceil_div(s->q_len * s->num_heads, kRows);
+  return s->batch * n_out * G;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return kVersion; }
+
+const char* mla_status_string(mla_status st) {
+  switch (st) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "device wait timed out";
+    case MLA_ERR_DEVICE_BOUNDS: return "block-table entry out of range";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t mla_workspace_size(const mla_shape* shape, int num_shards, int shard_id) {
+  if (!shape_ok(shape) || num_shards < 1 || num_shards > kMaxShards) return 0;
+  if (shard_id != MLA_ALL_SHARDS && (shard_id < 0 || shard_id >= num_shards)) return 0;
+  int grid = device_sm_count();
+  if (grid <= 0) return 0;
+  return ws_layout(units_for(shape, num_shards, shard_id), grid).total;
+}
+
+mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                              int max_pages_per_req, const int32_t* seq_lens,
+                              const mla_shape* shape, int shard_id, int num_shards,
+                              mla_layout layout, float* out_partial, float* lse_partial,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !kv || !block_table || !seq_lens || !out_partial || !lse_partial) return MLA_ERR_INVALID;
+  if (!shape_ok(shape)) return MLA_ERR_INVALID;
+  if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
+  if (shard_id != MLA_ALL_SHARDS && (shard_id < 0 || shard_id >= num_shards)) return MLA_ERR_INVALID;
+  if (layout != MLA_LAYOUT_INTERLEAVED && layout != MLA_LAYOUT_CONTIGUOUS) return MLA_ERR_INVALID;
+  if (kv->data == nullptr || kv->num_pages < 1 || max_pages_per_req < 1) return MLA_ERR_INVALID;
+  if (kv->page_size != kPage) return MLA_ERR_UNSUPPORTED;
+  if (kv->dtype == MLA_KV_BF16) {
+    if (kv->scale != nullptr) return MLA_ERR_INVALID;
+  } else if (kv->dtype == MLA_KV_FP8_E4M3) {
+    if (kv->scale == nullptr) return MLA_ERR_INVALID;
+    return MLA_ERR_UNSUPPORTED;
+  } else {
+    return MLA_ERR_INVALID;
+  }
+  if (shape->num_heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
+  if (layout == MLA_LAYOUT_INTERLEAVED && kPage % num_shards != 0) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kv->data) || !aligned16(out_partial) ||
+      !aligned16(lse_partial) || !aligned16(block_table) || !aligned16(seq_lens))
+    return MLA_ERR_INVALID;
+  if (workspace == nullptr || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
+  const int grid = device_sm_count();
+  if (grid <= 0) return MLA_ERR_CUDA;
+  const int U = units_for(shape, num_shards, shard_id);
+  const WsLayout wl = ws_layout(U, grid);
+  if (workspace_bytes < wl.total) return MLA_ERR_WORKSPACE;
+  EncodeTiledFn encode = encode_fn();
+  if (encode == nullptr) return MLA_ERR_CUDA;
+
+  ProblemDesc pd;
+  pd.B = shape->batch;
+  pd.q_len = shape->q_len;
+  pd.H = shape->num_heads;
+  pd.R = shape->q_len * shape->num_heads;
+  pd.G = ceil_div(pd.R, kRows);
+  pd.num_shards = num_shards;
+  pd.shard_first = shard_id == MLA_ALL_SHARDS ? 0 : shard_id;
+  pd.n_out = shard_id == MLA_ALL_SHARDS ? num_shards : 1;
+  pd.layout = layout == MLA_LAYOUT_INTERLEAVED ? kInterleaved : kContiguous;
+  pd.causal = shape->causal;
+  pd.num_pages = kv->num_pages;
+  pd.max_pages = max_pages_per_req;
+  pd.scale_log2 = shape->softmax_scale * 1.4426950408889634f;
+  pd.block_table = block_table;
+  pd.seq_lens = seq_lens;
+
+  // query rows: [B*q_len*H, 576] bf16, boxes of 64 dims x 64 rows
+  CUtensorMap tm_q, tm_kv;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)pd.B * pd.R};
+    cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kRows};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  }
+  // cache rows viewed as [page][row / nv][row % nv][576]; a box takes the
+  // 64/nv rows of one page that one shard owns (nv = N interleaved, else 1)
+  {
+    const int nv = pd.layout == kInterleaved ? num_shards : 1;
+    cuuint64_t dims[4] = {(cuuint64_t)kDqk, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
+                          (cuuint64_t)kv->num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kDqk * 2 * nv,
+                             (cuuint64_t)kDqk * 2 * kPage};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)(kPage / nv), 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PartialParams p;
+  p.pd = pd;
+  p.out_partial = out_partial;
+  p.lse_partial = lse_partial;
+  p.hdr = reinterpret_cast<WsHeader*>(ws + wl.hdr);
+  p.prefix = reinterpret_cast<int*>(ws + wl.prefix);
+  p.ws_o = reinterpret_cast<float*>(ws + wl.ws_o);
+  p.ws_lse = reinterpret_cast<float*>(ws + wl.ws_lse);
+  p.kv_scale = kv->scale;
+  p.kv_fp8 = nullptr;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_partial_bf16(tm_q, tm_kv, p, grid, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_merge(pd, p.hdr, p.prefix, p.ws_o, p.ws_lse, out_partial, lse_partial, U, st) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status mla_shard_combine(const float* partials, const float* lses, int num_shards,
+                             const mla_shape* shape, const void* w_uv, void* out, float* lse_out,
+                             void* stream) {
+  if (!partials || !lses || !out || !shape_ok(shape)) return MLA_ERR_INVALID;
+  if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
+  if (!aligned16(partials) || !aligned16(out) || (w_uv && !aligned16(w_uv)))
+    return MLA_ERR_INVALID;
+  const int rows = shape->batch * shape->q_len * shape->num_heads;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (w_uv == nullptr)
+    e = launch_combine(partials, lses, num_shards, rows, static_cast<uint16_t*>(out), lse_out, st);
+  else
+    e = launch_combine_wuv(partials, lses, num_shards, shape->batch * shape->q_len,
+                           shape->num_heads, static_cast<const uint16_t*>(w_uv),
+                           static_cast<uint16_t*>(out), lse_out, st);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status mla_get_device_error(void* workspace, void* stream) {
+  if (workspace == nullptr) return MLA_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned err = 0;
+  if (cudaMemcpyAsync(&err, workspace, sizeof(err), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (err != 0) {
+    unsigned zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  if (err & kErrTimeout) return MLA_ERR_TIMEOUT;
+  if (err & kErrBadPage) return MLA_ERR_DEVICE_BOUNDS;
+  return MLA_OK;
+}
+
+}  // extern "C"

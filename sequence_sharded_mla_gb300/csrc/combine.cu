@@ -1,0 +1,177 @@
+// LSE combine of shard partials ("Decode Context Parallelism", section 4.1:
+// each shard's partial output is reweighted by its log-sum-exp and the
+// weighted partials are summed into the true output), optionally fused with
+// the per-head value up-projection W_UV ("Kimi K3 in vLLM: Specialized CuTe
+// DSL Decode on NVIDIA GB300", section 1: a fused kernel combines the partial
+// results with v-proj).
+//
+//   M = max_s lse_s,  w_s = exp(lse_s - M),  lse = M + ln sum_s w_s
+//   out = sum_s w_s o_s / sum_s w_s                      -> bf16 [rows, 512]
+//   y   = out . W_UV[h]   (fp32 out, bf16 weights)       -> bf16 [rows, 128]
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace mla {
+
+namespace {
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace
+
+// One warp per query row; each lane owns 16 of the 512 latent dims
+// (four float4 at dims 4*lane + 128*k), so every load instruction of the warp
+// reads 512 contiguous bytes.
+__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ partials,
+                                                          const float* __restrict__ lses,
+                                                          int num_shards, int rows,
+                                                          uint16_t* __restrict__ out,
+                                                          float* __restrict__ lse_out) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float l[kMaxShards];
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int s = 0; s < kMaxShards; ++s) {
+    l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
+    M = fmaxf(M, l[s]);
+  }
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (M > -CUDART_INF_F) {
+#pragma unroll
+    for (int s = 0; s < kMaxShards; ++s) {
+      if (s >= num_shards) break;
+      const float w = __expf(l[s] - M);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(partials + ((size_t)s * rows + row) * kDv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 o = __ldg(src + lane + 32 * k);
+        acc[k].x += w * o.x;
+        acc[k].y += w * o.y;
+        acc[k].z += w * o.z;
+        acc[k].w += w * o.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(out + (size_t)row * kDv);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    dst[lane + 32 * k] = make_uint2(pack2(acc[k].x * inv, acc[k].y * inv),
+                                    pack2(acc[k].z * inv, acc[k].w * inv));
+  if (lse_out != nullptr && lane == 0)
+    lse_out[row] = M > -CUDART_INF_F ? M + __logf(wsum) : -CUDART_INF_F;
+}
+
+// Fused combine + W_UV.  Block (h, jb) handles head h and output columns
+// [64*jb, 64*jb + 64) for every (b, i) row of that head, 16 rows at a time:
+// it merges the shard partials of those rows into shared memory (fp32), then
+// 256 threads (64 columns x 4 slices of 128 latent dims) accumulate
+// out . W_UV[h][:, col] and reduce the four slices.
+constexpr int kWuvRowsPerPass = 16;
+
+__global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
+    const float* __restrict__ partials, const float* __restrict__ lses, int num_shards,
+    int rows_per_head_group /* B*q_len */, int H, const uint16_t* __restrict__ w_uv,
+    uint16_t* __restrict__ y, float* __restrict__ lse_out) {
+  __shared__ float so[kWuvRowsPerPass][kDv];
+  __shared__ float red[4][kWuvRowsPerPass][64];
+  const int h = blockIdx.x, jb = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int rows = rows_per_head_group * H;
+  const int col = tid & 63, slice = tid >> 6;
+  const uint16_t* wcol = w_uv + (size_t)h * kDv * kDuv + 64 * jb + col;
+  for (int base = 0; base < rows_per_head_group; base += kWuvRowsPerPass) {
+    const int nr = min(kWuvRowsPerPass, rows_per_head_group - base);
+    // merge: warp w handles rows w, w+8 of this pass
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int rr = warp; rr < nr; rr += 8) {
+      const int row = (base + rr) * H + h;
+      float M = -CUDART_INF_F;
+      float l[kMaxShards];
+#pragma unroll
+      for (int s = 0; s < kMaxShards; ++s) {
+        l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
+        M = fmaxf(M, l[s]);
+      }
+      float4 acc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float wsum = 0.f;
+      if (M > -CUDART_INF_F) {
+        for (int s = 0; s < num_shards; ++s) {
+          const float w = __expf(l[s] - M);
+          wsum += w;
+          const float4* src =
+              reinterpret_cast<const float4*>(partials + ((size_t)s * rows + row) * kDv);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 o = __ldg(src + lane + 32 * k);
+            acc[k].x += w * o.x;
+            acc[k].y += w * o.y;
+            acc[k].z += w * o.z;
+            acc[k].w += w * o.w;
+          }
+        }
+      }
+      const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<float4*>(&so[rr][4 * (lane + 32 * k)]) = v;
+      }
+      if (lse_out != nullptr && jb == 0 && lane == 0)
+        lse_out[row] = M > -CUDART_INF_F ? M + __logf(wsum) : -CUDART_INF_F;
+    }
+    __syncthreads();
+    float acc[kWuvRowsPerPass];
+#pragma unroll
+    for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] = 0.f;
+    const int c0 = slice * 128;
+#pragma unroll 4
+    for (int c = c0; c < c0 + 128; ++c) {
+      const float w = __uint_as_float(((uint32_t)__ldg(wcol + (size_t)c * kDuv)) << 16);
+#pragma unroll
+      for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] += so[r][c] * w;
+    }
+#pragma unroll
+    for (int r = 0; r < kWuvRowsPerPass; ++r) red[slice][r][col] = acc[r];
+    __syncthreads();
+    for (int e = tid; e < nr * 64; e += 256) {
+      const int r = e >> 6, c = e & 63;
+      const float v = red[0][r][c] + red[1][r][c] + red[2][r][c] + red[3][r][c];
+      const int row = (base + r) * H + h;
+      __nv_bfloat16 b = __float2bfloat16_rn(v);
+      y[(size_t)row * kDuv + 64 * jb + c] = *reinterpret_cast<uint16_t*>(&b);
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_combine(const float* partials, const float* lses, int num_shards, int rows,
+                           uint16_t* out, float* lse_out, cudaStream_t stream) {
+  mla_combine_kernel<<<ceil_div(rows, 8), 256, 0, stream>>>(partials, lses, num_shards, rows, out,
+                                                            lse_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
+                               int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
+                               float* lse_out, cudaStream_t stream) {
+  dim3 grid(H, kDuv / 64);
+  mla_combine_wuv_kernel<<<grid, 256, 0, stream>>>(partials, lses, num_shards,
+                                                   rows_per_head_group, H, w_uv, y, lse_out);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

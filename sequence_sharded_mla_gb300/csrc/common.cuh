@@ -1,0 +1,134 @@
+// Shared definitions of the CUDA path: problem constants, the work-unit
+// geometry of a (request, shard, query-row group) and the kernel parameter
+// blocks.  Included by the kernels and by the host-side C ABI.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kDqk = 576;        // absorbed query/key width: 512 latent + 64 rope
+constexpr int kDv = 512;         // value width (the latent c_kv)
+constexpr int kDuv = 128;        // per-head up-projected value width
+constexpr int kPage = 64;        // tokens per cache page
+constexpr int kTile = 64;        // tokens per pipeline tile (MMA N of QK^T)
+constexpr int kRows = 64;        // query rows per work unit (MMA M of QK^T)
+constexpr int kChunks = 9;       // 576 / 64: 128-byte swizzle chunks per row
+constexpr int kChunkBytes = 64 * 128;            // 64 rows x 64 bf16
+constexpr int kTileBytes = kChunks * kChunkBytes;  // 73728
+constexpr int kMaxShards = 8;
+
+// Error bits written to the workspace error word.
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrBadPage = 2u;
+
+enum Layout : int { kInterleaved = 0, kContiguous = 1 };
+
+// Workspace header (first 256 bytes of the caller's workspace).
+struct WsHeader {
+  unsigned err;        // OR of error bits
+  int total_tiles;     // W: tiles over all units
+  int per_cta;         // tiles per persistent CTA
+  int grid;            // persistent CTAs
+  int num_units;       // U
+  int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+struct ProblemDesc {
+  int B, q_len, H;
+  int R;               // q_len * H query rows per request
+  int G;               // ceil(R / 64) row groups per request
+  int num_shards;      // N
+  int shard_first;     // first shard computed by this call
+  int n_out;           // shards computed by this call (N, or 1)
+  int layout;          // Layout
+  int causal;
+  int num_pages;
+  int max_pages;
+  float scale_log2;    // softmax scale * log2(e)
+  const int32_t* block_table;  // [B, max_pages]
+  const int32_t* seq_lens;     // [B]
+};
+
+struct PartialParams {
+  ProblemDesc pd;
+  float* out_partial;  // [n_out, B, q_len, H, 512]
+  float* lse_partial;  // [n_out, B, q_len, H]
+  WsHeader* hdr;
+  int* prefix;         // [U + 1] exclusive tile prefix over units
+  float* ws_o;         // [grid * 2, 64, 512] split pieces
+  float* ws_lse;       // [grid * 2, 64]
+  const float* kv_scale;  // fp8 caches: [num_pages * 64]
+  const uint8_t* kv_fp8;  // fp8 caches: [num_pages, 64, 576] codes
+  unsigned long long timeout_ns;
+};
+
+// Geometry of one work unit u = ((b * n_out) + so) * G + g.
+struct Unit {
+  int b, so, s, g;
+  int L;            // context length of request b
+  int rows;         // valid query rows in this group (<= 64, multiple of 16)
+  int tiles;        // pipeline tiles
+  int tstart, tend; // contiguous layout: global token range of the shard
+  int p0;           // contiguous layout: first page slot
+};
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
+  Unit x;
+  x.g = u % pd.G;
+  int bs = u / pd.G;
+  x.so = bs % pd.n_out;
+  x.b = bs / pd.n_out;
+  x.s = pd.shard_first + x.so;
+  x.L = pd.seq_lens[x.b];
+  int r0 = x.g * kRows;
+  x.rows = min(kRows, pd.R - r0);
+  x.tstart = 0;
+  x.tend = 0;
+  x.p0 = 0;
+  int L = x.L > 0 ? x.L : 0;
+  if (pd.layout == kInterleaved) {
+    int n_local = L > x.s ? (L - 1 - x.s) / pd.num_shards + 1 : 0;
+    x.tiles = ceil_div(n_local, kTile);
+  } else {
+    int c = ceil_div(L, pd.num_shards);
+    x.tstart = x.s * c;
+    x.tend = min(x.tstart + c, L);
+    if (x.tstart < x.tend) {
+      x.p0 = x.tstart / kPage;
+      x.tiles = (x.tend - 1) / kPage - x.p0 + 1;
+    } else {
+      x.tiles = 0;
+    }
+  }
+  return x;
+}
+
+// Global token position of slot a (0..63) of tile j of unit x.
+__device__ __forceinline__ int slot_token(const ProblemDesc& pd, const Unit& x, int j, int a) {
+  if (pd.layout == kInterleaved) return (j * kTile + a) * pd.num_shards + x.s;
+  return (x.p0 + j) * kPage + a;
+}
+
+__device__ __forceinline__ bool slot_valid(const ProblemDesc& pd, const Unit& x, int t) {
+  if (pd.layout == kInterleaved) return t < x.L;
+  return t >= x.tstart && t < x.tend;
+}
+
+// True when every slot of tile j is a valid token visible to every query row
+// of the unit (no masking needed).
+__device__ __forceinline__ bool tile_full(const ProblemDesc& pd, const Unit& x, int j) {
+  int first = slot_token(pd, x, j, 0), last = slot_token(pd, x, j, kTile - 1);
+  bool ok = slot_valid(pd, x, first) && slot_valid(pd, x, last);
+  if (pd.causal) {
+    int i_min = (x.g * kRows) / pd.H;  // smallest query position in the group
+    ok = ok && last <= x.L - pd.q_len + i_min;
+  }
+  return ok;
+}
+
+}  // namespace mla

@@ -1,0 +1,514 @@
+// Sequence-sharded MLA decode: per-shard partial attention on tcgen05.
+//
+// Computes, for every (request b, shard s, group of 64 query rows), the
+// attention of the absorbed queries over the shard's slice of the paged
+// latent cache and emits the normalised partial output o_s and its
+// log-sum-exp lse_s ("Decode Context Parallelism", sections 4.1 and 5.3:
+// each rank attends over its local latent slice; partial outputs and LSEs are
+// merged afterwards).
+//
+// Data flow per persistent CTA (one per SM, 192 threads):
+//   warp 0      producer: block-table lookups, TMA loads of the query group
+//               (64 rows x 576, once per piece) and of 64-token KV tiles
+//               (one TMA box per page and 64-wide chunk, 128-byte swizzle)
+//   warp 1      MMA issuer: S = Q K^T (M=64 rows, N=64 tokens, K=576) into
+//               TMEM, then O^T += V^T P^T (M=128 latent dims x4, N=rows,
+//               K=64 tokens) into a TMEM accumulator of 4 x 64 columns
+//   warps 2..5  softmax: one thread per query row reads its 64 logits from
+//               TMEM, masks, keeps the running max / sum, writes bf16
+//               probabilities to shared memory; rescales O^T in TMEM only
+//               when a running max grows by more than 2^8; epilogue writes
+//               o = O / l and lse = m + ln l.
+//
+// Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
+// [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
+// written straight to out_partial; pieces of a split unit go to workspace
+// slots and are merged by mla_merge_kernel.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kBarSoftmax = 1;   // named barrier id for the softmax warps
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct Misc {
+  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
+  uint64_t q_full, q_empty, p_full, pv_done, o_free;
+  uint32_t tmem_base;
+  int abort;
+  float alpha[kRows];
+  float inv_l[kRows];
+};
+
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = kTileBytes;
+constexpr int kSmemP = 3 * kTileBytes;
+constexpr int kSmemMisc = kSmemP + kRows * 128;
+constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // + misc + alignment slack
+static_assert(sizeof(Misc) <= 1024, "misc block");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// TMEM columns: S double buffer (M=64 layout), then four O^T blocks.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColO = 128;
+
+struct PieceIter {
+  const int* prefix;
+  int U, lo, hi, pos, u;
+  __device__ void init(const int* pfx, int num_units, int lo_, int hi_) {
+    prefix = pfx;
+    U = num_units;
+    lo = lo_;
+    hi = hi_;
+    pos = lo_;
+    // last unit with prefix[u] <= lo
+    int a = 0, b = num_units - 1;
+    while (a < b) {
+      int m = (a + b + 1) >> 1;
+      if (prefix[m] <= lo_) a = m;
+      else b = m - 1;
+    }
+    u = a;
+  }
+  // Next piece: unit, tile range [t0, t1), whether it is the whole unit, slot.
+  __device__ bool next(int& unit, int& t0, int& t1, bool& whole, int& slot) {
+    if (pos >= hi) return false;
+    while (u < U && prefix[u + 1] <= pos) ++u;
+    int us = prefix[u], ue = prefix[u + 1];
+    unit = u;
+    t0 = pos - us;
+    t1 = min(hi, ue) - us;
+    whole = (us >= lo) && (ue <= hi);
+    slot = (pos == lo) ? 0 : 1;
+    pos = min(hi, ue);
+    ++u;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void set_error(PartialParams& p, Misc* misc, unsigned bits) {
+  atomicOr(&p.hdr->err, bits);
+  if (bits & kErrTimeout) *(volatile int*)&misc->abort = 1;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Misc* misc = reinterpret_cast<Misc*>(smem + kSmemMisc);
+  const ProblemDesc& pd = p.pd;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int W = p.hdr->total_tiles, per = p.hdr->per_cta;
+  const int lo = blockIdx.x * per;
+  if (lo >= W) return;
+  const int hi = min(lo + per, W);
+  const int U = p.hdr->num_units;
+
+  const uint32_t sQ = smem_u32(smem + kSmemQ);
+  const uint32_t sKV = smem_u32(smem + kSmemKV);
+  const uint32_t sP = smem_u32(smem + kSmemP);
+  const uint32_t b_kv_full = smem_u32(&misc->kv_full[0]);
+  const uint32_t b_kv_empty = smem_u32(&misc->kv_empty[0]);
+  const uint32_t b_s_full = smem_u32(&misc->s_full[0]);
+  const uint32_t b_s_empty = smem_u32(&misc->s_empty[0]);
+  const uint32_t b_q_full = smem_u32(&misc->q_full), b_q_empty = smem_u32(&misc->q_empty);
+  const uint32_t b_p_full = smem_u32(&misc->p_full), b_pv_done = smem_u32(&misc->pv_done);
+  const uint32_t b_o_free = smem_u32(&misc->o_free);
+  volatile int* abort_flag = &misc->abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_kv_full + 8 * i, 1);
+      mbar_init(b_kv_empty + 8 * i, 1);
+      mbar_init(b_s_full + 8 * i, 1);
+      mbar_init(b_s_empty + 8 * i, kSoftmaxThreads);
+    }
+    mbar_init(b_q_full, 1);
+    mbar_init(b_q_empty, 1);
+    mbar_init(b_p_full, kSoftmaxThreads);
+    mbar_init(b_pv_done, 1);
+    mbar_init(b_o_free, kSoftmaxThreads);
+    misc->abort = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < kRows) misc->alpha[threadIdx.x] = 1.0f;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const uint64_t tmo = p.timeout_ns;
+
+  PieceIter it;
+  it.init(p.prefix, U, lo, hi);
+  int armed_kv[2] = {-1, -1}, armed_q = -1;  // producer: last armed phases
+  int unit, t0, t1, slot;
+  bool whole;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int nv = pd.layout == kInterleaved ? pd.num_shards : 1;  // page boxes per tile
+    const int box_rows = kTile / nv;
+    int gt = 0, pc = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit(pd, unit);
+      const int npages_b = ceil_div(x.L, kPage);
+      const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
+      int win_base = -1, win_val = -1;
+      for (int j = t0; j < t1 && ok; ++j, ++gt) {
+        const int stage = gt & 1;
+        if (gt >= 2) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(b_kv_empty + 8 * stage, ((gt >> 1) - 1) & 1, tmo, abort_flag));
+          if (!ok) break;
+        }
+        // page slots of this tile
+        int first_slot = pd.layout == kInterleaved ? j * nv : x.p0 + j;
+        int page_ids[kMaxShards];
+#pragma unroll
+        for (int k = 0; k < kMaxShards; ++k) {
+          page_ids[k] = pd.num_pages;  // out of range: TMA fills zeros
+          if (k < nv) {
+            int idx = first_slot + k;
+            int wb = idx & ~31;
+            if (idx < npages_b && wb != win_base) {
+              win_base = wb;
+              int e = wb + lane;
+              win_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
+            }
+            int v = __shfl_sync(0xffffffffu, win_val, idx & 31);
+            if (idx < npages_b) {
+              if (v < 0 || v >= pd.num_pages) {
+                if (lane == 0) set_error(p, misc, kErrBadPage);
+                v = pd.num_pages;
+              }
+              page_ids[k] = v;
+            }
+          }
+        }
+        if (lane == 0) {
+          const uint32_t full = b_kv_full + 8 * stage;
+          mbar_arrive_expect_tx(full, kTileBytes);
+          armed_kv[stage] = gt;
+          const uint32_t dst0 = sKV + stage * kTileBytes;
+          for (int k = 0; k < nv; ++k) {
+            const int res = pd.layout == kInterleaved ? x.s : 0;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_4d(dst0 + c * kChunkBytes + k * box_rows * 128, &tm_kv, full, c * 64, res,
+                          0, page_ids[k]);
+          }
+        }
+        __syncwarp();
+        if (j == t0) {
+          // query rows of this unit: reuse of the buffer waits for the last
+          // QK^T of the previous piece
+          if (pc >= 1) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(b_q_full, kTileBytes);
+            armed_q = pc;
+            const int row0 = x.b * pd.R + x.g * kRows;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(sQ + c * kChunkBytes, &tm_q, b_q_full, c * 64, row0);
+          }
+          __syncwarp();
+        }
+      }
+      ++pc;
+    }
+    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
+    int gt = 0, pc = 0;
+    bool ok = true;
+    auto issue_pv = [&](int g, bool first_of_piece, int rows) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(b_p_full, g & 1, tmo, abort_flag))) return false;
+      if (first_of_piece && pc >= 1)
+        if (!__all_sync(0xffffffffu, mbar_wait(b_o_free, (pc - 1) & 1, tmo, abort_flag)))
+          return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t id_pv = idesc_bf16_f32(128, rows, true, false);
+        const uint32_t st = sKV + (g & 1) * kTileBytes;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint64_t a = sw128_desc(st + (2 * blk) * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+            uint64_t b = sw128_desc(sP + 32 * kk, 16, 1024);
+            mma_bf16_ss(tmem + kColO + 64 * blk, a, b, id_pv, (first_of_piece && kk == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit(b_pv_done);
+        mma_commit(b_kv_empty + 8 * (g & 1));
+      }
+      __syncwarp();
+      return true;
+    };
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit(pd, unit);
+      const int rows = x.rows;
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
+      for (int j = t0; j < t1 && ok; ++j, ++gt) {
+        const int stage = gt & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full + 8 * stage, (gt >> 1) & 1, tmo, abort_flag));
+        if (ok && gt >= 2)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(b_s_empty + 8 * stage, ((gt >> 1) - 1) & 1, tmo, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = sKV + stage * kTileBytes;
+          const uint32_t d = tmem + kColS0 + 64 * stage;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint64_t a = sw128_desc(sQ + c * kChunkBytes + 32 * k, 16, 1024);
+              uint64_t b = sw128_desc(st + c * kChunkBytes + 32 * k, 16, 1024);
+              mma_bf16_ss(d, a, b, id_qk, (c | k) ? 1u : 0u);
+            }
+          }
+          mma_commit(b_s_full + 8 * stage);
+          if (j == t1 - 1) mma_commit(b_q_empty);
+        }
+        __syncwarp();
+        if (j > t0) ok = issue_pv(gt - 1, j - 1 == t0, rows);
+      }
+      if (ok) ok = issue_pv(gt - 1, t1 - 1 == t0, rows);
+      ++pc;
+    }
+    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int sw = warp - 2;             // 0..3
+    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    const int tid = threadIdx.x - 64;    // 0..127
+    const int r = 16 * quad + lane;      // query row owned by this thread (lane < 16)
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    (void)sw;
+    int gt = 0, pc = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit(pd, unit);
+      const bool owner = lane < 16 && r < x.rows;
+      const int i_row = (x.g * kRows + r) / pd.H;           // query position of row r
+      const int vis_limit = x.L - pd.q_len + i_row;          // causal: t <= vis_limit
+      float m_run = -CUDART_INF_F, l_run = 0.0f;
+      for (int j = t0; j < t1; ++j, ++gt) {
+        const int sb = gt & 1;
+        const bool ok_s = __all_sync(0xffffffffu,
+                                    ok && mbar_wait(b_s_full + 8 * sb, (gt >> 1) & 1, tmo, abort_flag));
+        bool resc = false;
+        uint32_t pk[32];
+        const bool full = tile_full(pd, x, j);
+        if (ok_s) {
+          tc_fence_after();
+          uint32_t sr[64];
+          {
+            uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+            uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+            tmem_ld32(tmem + lane_off + kColS0 + 64 * sb, lo32);
+            tmem_ld32(tmem + lane_off + kColS0 + 64 * sb + 32, hi32);
+            tmem_wait_ld();
+          }
+          tc_fence_before();
+          mbar_arrive(b_s_empty + 8 * sb);
+          if (owner) {
+            float s[64];
+#pragma unroll
+            for (int a = 0; a < 64; ++a) s[a] = __uint_as_float(sr[a]);
+            if (!full) {
+#pragma unroll
+              for (int a = 0; a < 64; ++a) {
+                int t = slot_token(pd, x, j, a);
+                bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
+                if (!vis) s[a] = -CUDART_INF_F;
+              }
+            }
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int a = 0; a < 64; ++a) mx = fmaxf(mx, s[a]);
+            const float m_new = fmaxf(m_run, mx * pd.scale_log2);
+            float alpha = 1.0f;
+            if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
+              alpha = (m_run == -CUDART_INF_F) ? 0.0f : exp2f(m_run - m_new);
+              l_run *= alpha;
+              m_run = m_new;
+              resc = (j != t0);
+            }
+            misc->alpha[r] = alpha;
+            const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int a = 0; a < 32; ++a) {
+              float p0 = exp2f(fmaf(s[2 * a], pd.scale_log2, -m_use));
+              float p1 = exp2f(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
+              pk[a] = pack_bf16x2(p0, p1);
+              lsum += p0 + p1;
+            }
+            l_run += lsum;
+          }
+        }
+        // every softmax thread reaches both reductions, so a failed wait
+        // anywhere in the group is seen by all of them at the same point
+        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
+        const bool any_resc = named_bar_or(kBarSoftmax, kSoftmaxThreads, resc);
+        // previous PV must be done before P is overwritten or O^T rescaled
+        const bool ok_pv = __all_sync(
+            0xffffffffu, (gt == 0) || mbar_wait(b_pv_done, (gt - 1) & 1, tmo, abort_flag));
+        ok = ok_pv;
+        if (!ok_pv) continue;  // caught by the next reduction (or the epilogue's)
+        if (any_resc) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v[32];
+              const uint32_t ta = tmem + lane_off + kColO + 64 * blk + 32 * h2;
+              tmem_ld32(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[32 * h2 + c]);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+        if (owner) {
+          uint8_t* prow = smem + kSmemP + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v;
+          }
+        }
+        if (!full) {
+          // zero V rows of slots that hold no valid token of this shard so
+          // that garbage (even NaN) past the context end cannot reach O
+          uint8_t* st = smem + kSmemKV + (gt & 1) * kTileBytes;
+          for (int e = tid; e < kTile * 8 * 8; e += kSoftmaxThreads) {
+            int a = e >> 6, plane = (e >> 3) & 7, ch = e & 7;
+            int t = slot_token(pd, x, j, a);
+            if (!slot_valid(pd, x, t))
+              *reinterpret_cast<uint4*>(st + plane * kChunkBytes + a * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_p_full);
+      }
+      // ---------------------------------------------------------- epilogue
+      const bool ok_e = ok && mbar_wait(b_pv_done, (gt - 1) & 1, tmo, abort_flag);
+      if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_e)) { ok = false; break; }
+      tc_fence_after();
+      float* dst_o;
+      float* dst_lse;
+      if (whole) {
+        size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
+        dst_o = p.out_partial + row0 * kDv;
+        dst_lse = p.lse_partial + row0;
+      } else {
+        size_t sl = 2 * (size_t)blockIdx.x + slot;
+        dst_o = p.ws_o + sl * kRows * kDv;
+        dst_lse = p.ws_lse + sl * kRows;
+      }
+      if (owner) {
+        float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f
+                                   : -CUDART_INF_F;
+        misc->inv_l[r] = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+        dst_lse[r] = lse;
+      }
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + kColO + 64 * blk + 32 * h2, v);
+          tmem_wait_ld();
+          const int dim = 128 * blk + 32 * quad + lane;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int row = 32 * h2 + c;
+            if (row < x.rows) dst_o[(size_t)row * kDv + dim] = __uint_as_float(v[c]) * misc->inv_l[row];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(b_o_free);
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // inv_l reused by the next piece
+      ++pc;
+    }
+    if (!ok && tid == 0) set_error(p, misc, kErrTimeout);
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // after a failure, let this CTA's own TMA copies land before it exits
+    int never = 0;
+    for (int st = 0; st < 2; ++st)
+      if (armed_kv[st] >= 0) mbar_wait(b_kv_full + 8 * st, (armed_kv[st] >> 1) & 1, tmo, &never);
+    if (armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, tmo, &never);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int partial_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                const PartialParams& p, int grid, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_bf16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  mla_partial_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

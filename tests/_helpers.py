@@ -1,0 +1,75 @@
+"""Shared test helpers: move a workload to the GPU, run the CUDA path through
+the C ABI binding, compare with the oracle."""
+import numpy as np
+
+import oracle
+
+# Contract tolerances: bf16 outputs of order 1 within 1e-2, LSE within 1e-3.
+TOL_OUT = 1e-2
+TOL_LSE = 1e-3
+# Derived bound: the kernel rounds each probability to bf16 before P.V
+# (relative error <= 2^-9); the output is a probability-weighted mean, so its
+# error stays below 2^-9 times the spread of the values it averages.  Add one
+# bf16 rounding of the result (2^-9 relative) and a factor 4 of margin:
+# max|err| <= 2^-6 * max|ref| over a tensor.
+REL_OUT = 2.0 ** -6
+
+
+def to_device(w, dev):
+    import torch
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    if w.kv_dtype == "bf16":
+        kv = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16).to(dev)
+        sc = None
+    else:
+        kv = torch.from_numpy(w.kv).to(dev)
+        sc = torch.from_numpy(w.kv_scale).to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    wuv = None
+    if w.w_uv is not None:
+        wuv = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16).to(dev)
+    return dict(q=q, kv=kv, kv_scale=sc, block_table=bt, seq_lens=sl, w_uv=wuv)
+
+
+def run_gpu(w, dev, shard_id=-1, num_shards=None, layout=None, with_wuv=True):
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    t = to_device(w, dev)
+    N = w.num_shards if num_shards is None else num_shards
+    lay = w.layout if layout is None else layout
+    part, lse, ws = mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], N,
+                                           lay, shard_id=shard_id, kv_scale=t["kv_scale"],
+                                           causal=w.causal, softmax_scale=w.softmax_scale)
+    res = {"partial": part, "lse_partial": lse, "workspace": ws}
+    if shard_id == -1:
+        out, lse_out = mla.mla_shard_combine(part, lse, causal=w.causal,
+                                             softmax_scale=w.softmax_scale)
+        res["out"], res["lse"] = out, lse_out
+        if with_wuv and t["w_uv"] is not None:
+            y, _ = mla.mla_shard_combine(part, lse, w_uv=t["w_uv"])
+            res["y"] = y
+    torch.cuda.synchronize()
+    res["status"] = mla.mla_get_device_error(ws)
+    return res
+
+
+def check_close(got, ref, tol_abs, what, rel=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), f"{what}: -inf pattern differs"
+    g = np.where(both_inf, 0.0, got)
+    r = np.where(both_inf, 0.0, ref)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(g - r))) if g.size else 0.0
+    assert err <= tol_abs, f"{what}: max abs err {err:.3e} > {tol_abs:.1e}"
+    if rel is not None and g.size:
+        scale = float(np.max(np.abs(r)))
+        assert err <= rel * scale + 1e-6, f"{what}: max abs err {err:.3e} > {rel:.2e} * {scale:.3e}"
+    return err
+
+
+def bf16_to_np(t):
+    return t.float().cpu().numpy()

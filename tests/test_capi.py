@@ -1,0 +1,53 @@
+"""The C ABI library loads and exports every function include/mla_dcp.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla_dcp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("mla_decode_partial", "mla_shard_combine", "mla_workspace_size",
+                 "mla_get_device_error", "mla_status_string", "mla_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert mla.mla_version() == 100
+    assert mla.mla_status_string(-5) == "block-table entry out of range"
+
+
+def test_null_arguments_rejected_on_host():
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    sh = mla.mla_shape(1, 1, 16, 0, 0.07)
+    kv = mla.mla_kv_pages(None, None, 0, 1, 64)
+    st = L.mla_decode_partial(None, ctypes.byref(kv), None, 1, None, ctypes.byref(sh), -1, 2, 0,
+                              None, None, None, 0, None)
+    assert st == -1
+    st = L.mla_shard_combine(None, None, 2, ctypes.byref(sh), None, None, None, None)
+    assert st == -1
+    bad = mla.mla_shape(0, 1, 16, 0, 0.07)
+    assert L.mla_workspace_size(ctypes.byref(bad), 2, -1) == 0
+    assert L.mla_get_device_error(None, None) == -1
+
+
+def test_python_binding_names_match_the_abi():
+    import sequence_sharded_mla_gb300 as mla
+    for name in declared_functions():
+        assert callable(getattr(mla, name)), name

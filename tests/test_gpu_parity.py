@@ -1,0 +1,152 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output element: per-shard partials and LSEs, the
+LSE-combined bf16 output and LSE, and the fused W_UV projection.  They span
+several 64-token tiles with ragged tails, empty shards, both shard layouts,
+N = 1..8, 16..64 heads, q_len 1/2/9 (causal), bf16 and fp8 caches and
+NaN-poisoned unused cache rows.  Full-size configurations are checked on
+sampled query rows in test_gpu_configs.py.
+"""
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+import oracle
+from _helpers import REL_OUT, TOL_LSE, TOL_OUT, bf16_to_np, check_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    return torch.device("cuda:0")
+
+
+def compare_all(w, dev, layout=None, N=None):
+    N = w.num_shards if N is None else N
+    lay = w.layout if layout is None else layout
+    res = run_gpu(w, dev, num_shards=N, layout=lay)
+    assert res["status"] == 0, res["status"]
+    rows = w.batch * w.q_len * w.num_heads
+    part = res["partial"].cpu().numpy().reshape(N, rows, 512)
+    lsep = res["lse_partial"].cpu().numpy().reshape(N, rows)
+    for s in range(N):
+        ro, rl = oracle.attend(w, shard=s, num_shards=N, layout=lay)
+        check_close(part[s], ro, TOL_OUT, f"partial shard {s}", rel=REL_OUT)
+        check_close(lsep[s], rl, TOL_LSE, f"lse_partial shard {s}")
+    ref, ref_lse, ref_y = oracle.reference_step(w)
+    check_close(bf16_to_np(res["out"]).reshape(rows, 512), ref, TOL_OUT, "out", rel=REL_OUT)
+    check_close(res["lse"].cpu().numpy().reshape(rows), ref_lse, TOL_LSE, "lse")
+    if ref_y is not None:
+        check_close(bf16_to_np(res["y"]).reshape(rows, 128), ref_y, TOL_OUT, "y", rel=REL_OUT)
+    return res
+
+
+@pytest.mark.parametrize("H", [16, 32, 64])
+@pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
+def test_ragged_lengths(dev, H, layout):
+    lens = [1, 2, 63, 64, 65, 1000, 333]
+    w = mi.build_workload("ragged", len(lens), 1, H, lens, 2, layout, "bf16", False,
+                          seed=100 + H, poison=True, extra_pages=3)
+    compare_all(w, dev)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
+def test_shard_counts(dev, N, layout):
+    if layout == "interleaved" and 64 % N != 0:
+        pytest.skip("interleaved layout needs N | 64")
+    lens = [5, 700, 2049, 130]
+    w = mi.build_workload("shards", len(lens), 1, 32, lens, N, layout, "bf16", False,
+                          seed=200 + N)
+    compare_all(w, dev)
+
+
+@pytest.mark.parametrize("q_len", [2, 9])
+@pytest.mark.parametrize("H", [16, 64])
+def test_causal_verify(dev, q_len, H):
+    lens = [8000 // 8, 130, 9, 64]
+    w = mi.build_workload("verify", len(lens), q_len, H, lens, 2, "interleaved", "bf16", True,
+                          seed=300 + q_len + H, poison=True)
+    compare_all(w, dev)
+
+
+def test_causal_context_shorter_than_query(dev):
+    """Rows that see no token at all give lse = -inf and a zero output."""
+    w = mi.build_workload("tiny", 2, 9, 16, [5, 1], 2, "contiguous", "bf16", True, seed=310)
+    compare_all(w, dev)
+
+
+def test_empty_shards(dev):
+    w = mi.build_workload("empty", 3, 1, 16, [1, 3, 7], 8, "interleaved", "bf16", False, seed=320)
+    compare_all(w, dev)
+    w = mi.build_workload("empty", 3, 1, 16, [1, 3, 7], 8, "contiguous", "bf16", False, seed=321)
+    compare_all(w, dev)
+
+
+def test_single_shard_call_matches_all_shards(dev):
+    """A per-shard call (the per-GPU call of a multi-GPU deployment) gives the
+    same partials as the all-shards call.  The two calls split the work list
+    at different points, so fp32 summation order differs: equal to within
+    fp32 reassociation, not bitwise."""
+    w = mi.build_workload("one", 3, 1, 32, [100, 1000, 64], 4, "interleaved", "bf16", False,
+                          seed=330)
+    full = run_gpu(w, dev)
+    for s in range(4):
+        one = run_gpu(w, dev, shard_id=s)
+        assert one["status"] == 0
+        a = one["partial"].cpu().numpy()[0]
+        b = full["partial"].cpu().numpy()[s]
+        assert np.max(np.abs(a - b)) <= 1e-5 * np.max(np.abs(b))
+        la = one["lse_partial"].cpu().numpy()[0]
+        lb = full["lse_partial"].cpu().numpy()[s]
+        assert np.max(np.abs(la - lb)) <= 1e-5
+
+
+def test_deterministic(dev):
+    w = mi.build_workload("det", 4, 1, 64, [5000, 70, 20000, 1], 4, "interleaved", "bf16", False,
+                          seed=340)
+    a = run_gpu(w, dev)
+    b = run_gpu(w, dev)
+    assert np.array_equal(a["partial"].cpu().numpy(), b["partial"].cpu().numpy())
+    assert np.array_equal(a["out"].cpu().numpy(), b["out"].cpu().numpy())
+
+
+def test_fused_wuv_small(dev):
+    w = mi.build_workload("wuv", 3, 1, 32, [100, 3000, 17], 4, "interleaved", "bf16", False,
+                          seed=350, with_w_uv=True)
+    compare_all(w, dev)
+
+
+def test_bad_block_table_entry_reports_bounds_error(dev):
+    import sequence_sharded_mla_gb300 as mla
+    w = mi.build_workload("bad", 2, 1, 16, [200, 64], 2, "interleaved", "bf16", False, seed=360)
+    w.block_table[0, 2] = w.num_pages + 100
+    res = run_gpu(w, dev)
+    assert res["status"] == -5          # MLA_ERR_DEVICE_BOUNDS
+    assert mla.mla_get_device_error(res["workspace"]) == 0   # read clears it
+    assert np.all(np.isfinite(res["partial"].cpu().numpy()))
+
+
+def test_invalid_arguments_rejected_before_launch(dev):
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    w = mi.build_workload("inv", 1, 1, 16, [64], 2, "interleaved", "bf16", False, seed=370)
+    from _helpers import to_device
+    t = to_device(w, dev)
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 9)
+    assert e.value.status == -1
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 3, "interleaved")
+    assert e.value.status == -2          # interleaved needs N | 64
+    q20 = torch.zeros((1, 1, 20, 576), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_partial(q20, t["kv"], t["block_table"], t["seq_lens"], 2)
+    assert e.value.status == -2          # heads must be a multiple of 16
+    small_ws = torch.empty((64,), dtype=torch.uint8, device=dev)
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 2,
+                               workspace=small_ws)
+    assert e.value.status == -6
