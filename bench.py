@@ -1,0 +1,358 @@
+"""Benchmark: one sharded MLA decode step (all shards' partial attention, then
+the LSE combine) on the bimodal agentic batch, on N GPUs of one node.
+
+Workload (seeded, synthetic; stands in for the agentic long-context trace of
+"Decode Context Parallelism", section 2.1): 32 requests, 64 query heads,
+q_len 1, bf16 paged latent cache (576 = 512 c_kv + 64 k_rope, page size 64,
+pages scattered by a random block table), context lengths from a stratified
+log-uniform mix (~47% below 64k, ~18% below 8k, median ~67k, tail to ~1M,
+total <= 4M tokens), 4 logical shards interleaved, merged by LSE combine.
+
+metric: KV HBM GB/s = algorithmic KV bytes (every token < L_b once, 1152 B)
+        / device time of one whole step.  Inputs (3.4 GB) exceed L2.
+Also printed: decode steps/s per layer, the partial kernel's roofline
+fraction against the measured copy bandwidth, the oracle timed on host
+cores (cpu_baseline), and the same metric end to end through host buffers
+(e2e: pinned host -> device copies of the step's inputs and device -> host
+read of its outputs inside the timed region).
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA sharded decode: KV HBM GB/s (% of ~8 TB/s peak), decode steps/s per layer"
+CONFIG_ID = 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_for(kernel_src):
+    """ncu DRAM bytes per launch recorded for this exact kernel source, or None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    ent = rec.get(sha)
+    return None if ent is None else ent
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def cpu_sample(w, budget_s, oracle):
+    """Oracle on whole requests (all heads, unsharded, W_UV if present) until
+    about ``budget_s`` of CPU time; returns (KV bytes covered, seconds, desc)."""
+    import numpy as np
+    order = np.argsort(w.seq_lens)            # short to long, one of each band first
+    picked, t_used, kv_bytes = [], 0.0, 0
+    per = 1152 if w.kv_dtype == "bf16" else 580
+    H, q_len = w.num_heads, w.q_len
+    for b in order[::max(1, len(order) // 8)]:
+        rows = np.arange(b * q_len * H, (b + 1) * q_len * H, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.reference_step(w, rows=rows)
+        dt = time.perf_counter() - t0
+        picked.append(int(b))
+        t_used += dt
+        kv_bytes += int(w.seq_lens[b]) * per
+        if t_used >= budget_s:
+            break
+    desc = (f"requests {picked} of the workload (all {H} heads each, unsharded "
+            f"attention{', W_UV' if w.w_uv is not None else ''}), "
+            f"{int(sum(int(w.seq_lens[b]) for b in picked))} tokens")
+    return kv_bytes, t_used, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import mla_inputs as mi
+    import oracle
+    w = mi.config_workload(CONFIG_ID)
+    threads = oracle.num_threads()
+    per = 1152
+    # one step = the oracle over a bounded sample of the workload
+    import numpy as np
+    order = np.argsort(w.seq_lens)
+    budget = args.ref_step_seconds
+    results = []
+    for step in range(args.warmup + args.steps):
+        kv_bytes, dt, desc = cpu_sample(w, budget, oracle)
+        if step >= args.warmup:
+            results.append((kv_bytes, dt))
+    tot_b = sum(r[0] for r in results)
+    tot_t = sum(r[1] for r in results)
+    value = tot_b / tot_t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / len(results) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": mi.CONFIG_NAMES[CONFIG_ID], "batch": w.batch,
+                       "heads": w.num_heads, "q_len": w.q_len, "num_shards": w.num_shards,
+                       "layout": w.layout, "kv_dtype": w.kv_dtype,
+                       "total_tokens": w.total_tokens},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, world, rank, local, dist):
+    import numpy as np
+    import torch
+
+    import mla_inputs as mi
+    import sequence_sharded_mla_gb300 as mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.lib()
+    # each rank decodes its own batch of the same shape (independent requests)
+    w = mi.config_workload(CONFIG_ID, pinned=True)
+    if args.requests:
+        # a reduced copy of the workload (first K requests) for profiling runs
+        w = mi.build_workload(w.name + f"-first{args.requests}", args.requests, 1, 64,
+                              w.seq_lens[:args.requests], 4, "interleaved", "bf16", False,
+                              seed=2, pinned=True)
+    if rank > 0:
+        lens = mi.agentic_lengths(2 + 1000 * rank, 32)
+        w = mi.build_workload(w.name, 32, 1, 64, lens, 4, "interleaved", "bf16", False,
+                              seed=2 + 1000 * rank, pinned=True)
+    B, H, q_len, N = w.batch, w.num_heads, w.q_len, w.num_shards
+    kv_bytes = w.kv_bytes()
+
+    h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
+    h_kv = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16)
+    h_bt = torch.from_numpy(w.block_table).pin_memory()
+    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
+    d_q = h_q.to(dev)
+    d_kv = h_kv.to(dev)
+    d_bt = h_bt.to(dev)
+    d_sl = h_sl.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    part = torch.empty((N, B, q_len, H, 512), dtype=torch.float32, device=dev)
+    lsep = torch.empty((N, B, q_len, H), dtype=torch.float32, device=dev)
+    out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    ws = torch.empty((mla.mla_workspace_size(B, q_len, H, N),), dtype=torch.uint8, device=dev)
+    h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    h_lse = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+
+    ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+
+    def step(i=None):
+        if i is not None:
+            ev_p[2 * i].record(stream)
+        mla.mla_decode_partial(d_q, d_kv, d_bt, d_sl, N, w.layout, out_partial=part,
+                               lse_partial=lsep, workspace=ws, stream=stream)
+        if i is not None:
+            ev_p[2 * i + 1].record(stream)
+        mla.mla_shard_combine(part, lsep, out=out, lse_out=lse, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    assert mla.mla_get_device_error(ws, stream) == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    partial_ms = [ev_p[2 * i].elapsed_time(ev_p[2 * i + 1]) for i in range(args.steps)]
+    status = mla.mla_get_device_error(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"device error status {status}")
+
+    # end to end through host buffers: copy the step's inputs in, read results out
+    h2d = h_q.numel() * 2 + h_kv.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_kv.copy_(h_kv, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+
+    t = torch.tensor([elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms)],
+                     dtype=torch.float64, device=dev)
+    kvt = torch.tensor([float(kv_bytes)], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(kvt, op=dist.ReduceOp.SUM)
+    elapsed, e2e_per_step, partial_avg_ms = t.tolist()
+    total_kv = kvt.item()
+    if rank != 0:
+        return
+    peak, peak_kind = load_peaks()
+    value = total_kv * args.steps / elapsed / 1e9
+    ms_per_step = elapsed / args.steps * 1e3
+    achieved = kv_bytes / (partial_avg_ms / 1e3) / 1e9
+    traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc", "partial.cu"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": mi.CONFIG_NAMES[CONFIG_ID], "batch": B, "heads": H, "q_len": q_len,
+                   "num_shards": N, "layout": w.layout, "kv_dtype": "bf16",
+                   "total_tokens_per_gpu": w.total_tokens, "kv_bytes_per_gpu": kv_bytes,
+                   "l2": "inputs larger than L2 (KV cache 3.4 GB per GPU vs 129 MB L2)",
+                   "parallelism": f"{world} GPU(s), independent batches; {N} logical shards each"},
+        "steps_per_s": args.steps / elapsed,
+        "pct_of_peak_hbm": value / world / peak,
+        "roofline": {"kernel": "mla_partial_bf16_kernel (+plan, merge)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": traffic},
+        "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        kvb, dt, desc = cpu_sample(w, args.cpu_seconds, oracle)
+        line["cpu_baseline"] = {"value": kvb / dt / 1e9, "unit": "GB/s",
+                                "cores": oracle.num_threads(), "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="profiling only: keep the first K requests of the workload")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local, dist = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gpu(args, world, rank, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

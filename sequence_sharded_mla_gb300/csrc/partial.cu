@@ -173,58 +173,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane k < nv issues the nine 64-wide chunk boxes of page k of the tile;
+    // lane 0 arms the stage barrier with the whole tile's byte count first.
     const int nv = pd.layout == kInterleaved ? pd.num_shards : 1;  // page boxes per tile
-    const int box_rows = kTile / nv;
+    const int box_bytes = (kTile / nv) * 128;
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit(pd, unit);
       const int npages_b = ceil_div(x.L, kPage);
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
+      const int res = pd.layout == kInterleaved ? x.s : 0;
       int win_base = -1, win_val = -1;
       for (int j = t0; j < t1 && ok; ++j, ++gt) {
         const int stage = gt & 1;
+        // page slot of this lane's box; nv divides 32, so a tile never
+        // straddles two 32-entry windows of the block table
+        const int first_slot = pd.layout == kInterleaved ? j * nv : x.p0 + j;
+        const int wb = first_slot & ~31;
+        if (wb != win_base && first_slot < npages_b) {
+          win_base = wb;
+          const int e = wb + lane;
+          win_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
+        }
+        const int idx = first_slot + lane;
+        int page = __shfl_sync(0xffffffffu, win_val, idx & 31);
+        if (lane < nv && idx < npages_b && (page < 0 || page >= pd.num_pages)) {
+          set_error(p, misc, kErrBadPage);
+          page = pd.num_pages;
+        }
+        if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
         if (gt >= 2) {
           ok = __all_sync(0xffffffffu,
                           mbar_wait(b_kv_empty + 8 * stage, ((gt >> 1) - 1) & 1, tmo, abort_flag));
           if (!ok) break;
         }
-        // page slots of this tile
-        int first_slot = pd.layout == kInterleaved ? j * nv : x.p0 + j;
-        int page_ids[kMaxShards];
-#pragma unroll
-        for (int k = 0; k < kMaxShards; ++k) {
-          page_ids[k] = pd.num_pages;  // out of range: TMA fills zeros
-          if (k < nv) {
-            int idx = first_slot + k;
-            int wb = idx & ~31;
-            if (idx < npages_b && wb != win_base) {
-              win_base = wb;
-              int e = wb + lane;
-              win_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
-            }
-            int v = __shfl_sync(0xffffffffu, win_val, idx & 31);
-            if (idx < npages_b) {
-              if (v < 0 || v >= pd.num_pages) {
-                if (lane == 0) set_error(p, misc, kErrBadPage);
-                v = pd.num_pages;
-              }
-              page_ids[k] = v;
-            }
-          }
-        }
+        const uint32_t full = b_kv_full + 8 * stage;
         if (lane == 0) {
-          const uint32_t full = b_kv_full + 8 * stage;
           mbar_arrive_expect_tx(full, kTileBytes);
           armed_kv[stage] = gt;
-          const uint32_t dst0 = sKV + stage * kTileBytes;
-          for (int k = 0; k < nv; ++k) {
-            const int res = pd.layout == kInterleaved ? x.s : 0;
+        }
+        __syncwarp();
+        if (lane < nv) {
+          const uint32_t dst0 = sKV + stage * kTileBytes + lane * box_bytes;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-              tma_load_4d(dst0 + c * kChunkBytes + k * box_rows * 128, &tm_kv, full, c * 64, res,
-                          0, page_ids[k]);
-          }
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_4d(dst0 + c * kChunkBytes, &tm_kv, full, c * 64, res, 0, page);
         }
         __syncwarp();
         if (j == t0) {
@@ -250,64 +244,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
+    // Issues QK^T of tile j and P.V of tile j-1 in whichever order their
+    // inputs become ready (P.V first when both are): P.V is what releases a
+    // KV stage, so issuing it early lets the next tile's load start early.
     const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
-    int gt = 0, pc = 0;
+    // descriptor bases; adding (byte offset >> 4) moves the start address
+    const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
+    const uint64_t dkv0 = sw128_desc(sKV, 16, 1024);
+    const uint64_t dv0 = sw128_desc(sKV, kChunkBytes, 1024);
+    const uint64_t dp0 = sw128_desc(sP, 16, 1024);
+    int gbase = 0, pc = 0;
     bool ok = true;
-    auto issue_pv = [&](int g, bool first_of_piece, int rows) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(b_p_full, g & 1, tmo, abort_flag))) return false;
-      if (first_of_piece && pc >= 1)
-        if (!__all_sync(0xffffffffu, mbar_wait(b_o_free, (pc - 1) & 1, tmo, abort_flag)))
-          return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t id_pv = idesc_bf16_f32(128, rows, true, false);
-        const uint32_t st = sKV + (g & 1) * kTileBytes;
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            uint64_t a = sw128_desc(st + (2 * blk) * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-            uint64_t b = sw128_desc(sP + 32 * kk, 16, 1024);
-            mma_bf16_ss(tmem + kColO + 64 * blk, a, b, id_pv, (first_of_piece && kk == 0) ? 0u : 1u);
-          }
-        }
-        mma_commit(b_pv_done);
-        mma_commit(b_kv_empty + 8 * (g & 1));
-      }
-      __syncwarp();
-      return true;
-    };
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit(pd, unit);
-      const int rows = x.rows;
+      const int n = t1 - t0;
+      const uint32_t id_pv = idesc_bf16_f32(128, x.rows, true, false);
       ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
-      for (int j = t0; j < t1 && ok; ++j, ++gt) {
-        const int stage = gt & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full + 8 * stage, (gt >> 1) & 1, tmo, abort_flag));
-        if (ok && gt >= 2)
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(b_s_empty + 8 * stage, ((gt >> 1) - 1) & 1, tmo, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t st = sKV + stage * kTileBytes;
-          const uint32_t d = tmem + kColS0 + 64 * stage;
+      int nq = 0, np = 0;
+      uint64_t t_idle = 0;
+      while (ok && np < n) {
+        bool did = false;
+        if (np < nq) {
+          const int g = gbase + np;
+          bool ready = mbar_test(b_p_full, g & 1);
+          if (ready && np == 0 && pc >= 1) ready = mbar_test(b_o_free, (pc - 1) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t st_off = (uint32_t)((g & 1) * kTileBytes) >> 4;
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
+              for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint64_t a = sw128_desc(sQ + c * kChunkBytes + 32 * k, 16, 1024);
-              uint64_t b = sw128_desc(st + c * kChunkBytes + 32 * k, 16, 1024);
-              mma_bf16_ss(d, a, b, id_qk, (c | k) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t a = dv0 + st_off + (uint32_t)((2 * blk * kChunkBytes + kk * 2048) >> 4);
+                  const uint64_t bdesc = dp0 + (uint32_t)((32 * kk) >> 4);
+                  mma_bf16_ss(tmem + kColO + 64 * blk, a, bdesc, id_pv,
+                              (np == 0 && kk == 0) ? 0u : 1u);
+                }
+              }
+              mma_commit(b_pv_done);
+              mma_commit(b_kv_empty + 8 * (g & 1));
             }
+            __syncwarp();
+            ++np;
+            did = true;
           }
-          mma_commit(b_s_full + 8 * stage);
-          if (j == t1 - 1) mma_commit(b_q_empty);
         }
-        __syncwarp();
-        if (j > t0) ok = issue_pv(gt - 1, j - 1 == t0, rows);
+        if (!did && nq < n) {
+          const int g = gbase + nq;
+          const int stage = g & 1;
+          bool ready = mbar_test(b_kv_full + 8 * stage, (g >> 1) & 1);
+          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * stage, ((g >> 1) - 1) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t st_off = (uint32_t)(stage * kTileBytes) >> 4;
+              const uint32_t d = tmem + kColS0 + 64 * stage;
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint32_t off = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
+                  mma_bf16_ss(d, dq0 + off, dkv0 + st_off + off, id_qk, (c | k) ? 1u : 0u);
+                }
+              }
+              mma_commit(b_s_full + 8 * stage);
+              if (nq == n - 1) mma_commit(b_q_empty);
+            }
+            __syncwarp();
+            ++nq;
+            did = true;
+          }
+        }
+        if (did) {
+          t_idle = 0;
+        } else {
+          // nothing ready: park on the event expected next, then re-check
+          if (np < nq) mbar_try_wait_hint(b_p_full, (gbase + np) & 1, 200);
+          else mbar_try_wait_hint(b_kv_full + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 200);
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (now - t_idle > tmo || *abort_flag) ok = false;
+          ok = __all_sync(0xffffffffu, ok);
+        }
       }
-      if (ok) ok = issue_pv(gt - 1, t1 - 1 == t0, rows);
+      gbase += n;
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);

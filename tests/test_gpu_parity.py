@@ -88,8 +88,9 @@ def test_empty_shards(dev):
 def test_single_shard_call_matches_all_shards(dev):
     """A per-shard call (the per-GPU call of a multi-GPU deployment) gives the
     same partials as the all-shards call.  The two calls split the work list
-    at different points, so fp32 summation order differs: equal to within
-    fp32 reassociation, not bitwise."""
+    at different points, and each split piece rounds its probabilities to
+    bf16 against its own running maximum, so the two agree to the bf16
+    probability rounding bound (REL_OUT), not bitwise."""
     w = mi.build_workload("one", 3, 1, 32, [100, 1000, 64], 4, "interleaved", "bf16", False,
                           seed=330)
     full = run_gpu(w, dev)
@@ -98,10 +99,10 @@ def test_single_shard_call_matches_all_shards(dev):
         assert one["status"] == 0
         a = one["partial"].cpu().numpy()[0]
         b = full["partial"].cpu().numpy()[s]
-        assert np.max(np.abs(a - b)) <= 1e-5 * np.max(np.abs(b))
+        check_close(a, b, TOL_OUT, f"shard {s}", rel=REL_OUT)
         la = one["lse_partial"].cpu().numpy()[0]
         lb = full["lse_partial"].cpu().numpy()[s]
-        assert np.max(np.abs(la - lb)) <= 1e-5
+        check_close(la, lb, TOL_LSE, f"lse shard {s}")
 
 
 def test_deterministic(dev):
@@ -110,7 +111,8 @@ def test_deterministic(dev):
     a = run_gpu(w, dev)
     b = run_gpu(w, dev)
     assert np.array_equal(a["partial"].cpu().numpy(), b["partial"].cpu().numpy())
-    assert np.array_equal(a["out"].cpu().numpy(), b["out"].cpu().numpy())
+    import torch
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
 
 
 def test_fused_wuv_small(dev):
