@@ -25,9 +25,12 @@ def nvcc():
     return exe if os.path.exists(exe) else (shutil.which("nvcc") or "nvcc")
 
 
+INCLUDE = os.path.join(os.path.dirname(HERE), "include")
+
+
 def flags(extra=()):
     return ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-                   "--expt-relaxed-constexpr", *extra]
+                   "--expt-relaxed-constexpr", "-I" + INCLUDE, *extra]
 
 
 def _inputs():

@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/mla_dcp.h"
+#include "mla_dcp.h"
 #include "common.cuh"
 
 namespace mla {
@@ -203,6 +203,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.prefix = reinterpret_cast<int*>(ws + wl.prefix);
   p.ws_o = reinterpret_cast<float*>(ws + wl.ws_o);
   p.ws_lse = reinterpret_cast<float*>(ws + wl.ws_lse);
+  p.kv_bytes = static_cast<const uint8_t*>(kv->data);
   p.kv_scale = kv->scale;
   p.kv_fp8 = nullptr;
   p.timeout_ns = kTimeoutNs;

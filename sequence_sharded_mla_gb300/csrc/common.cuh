@@ -60,6 +60,7 @@ struct PartialParams {
   int* prefix;         // [U + 1] exclusive tile prefix over units
   float* ws_o;         // [grid * 2, 64, 512] split pieces
   float* ws_lse;       // [grid * 2, 64]
+  const uint8_t* kv_bytes;  // the cache itself (for L2 prefetch)
   const float* kv_scale;  // fp8 caches: [num_pages * 64]
   const uint8_t* kv_fp8;  // fp8 caches: [num_pages, 64, 576] codes
   unsigned long long timeout_ns;

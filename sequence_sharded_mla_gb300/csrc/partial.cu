@@ -8,17 +8,24 @@
 // merged afterwards).
 //
 // Data flow per persistent CTA (one per SM, 192 threads):
-//   warp 0      producer: block-table lookups, TMA loads of the query group
+//   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
 //               (one TMA box per page and 64-wide chunk, 128-byte swizzle)
+//               into two stages; a stage is refilled as soon as its P.V is
+//               done.
 //   warp 1      MMA issuer: S = Q K^T (M=64 rows, N=64 tokens, K=576) into
-//               TMEM, then O^T += V^T P^T (M=128 latent dims x4, N=rows,
-//               K=64 tokens) into a TMEM accumulator of 4 x 64 columns
-//   warps 2..5  softmax: one thread per query row reads its 64 logits from
-//               TMEM, masks, keeps the running max / sum, writes bf16
-//               probabilities to shared memory; rescales O^T in TMEM only
-//               when a running max grows by more than 2^8; epilogue writes
-//               o = O / l and lse = m + ln l.
+//               TMEM, group by group as the data lands, and
+//               O^T += V^T P^T (M=128 latent dims x 4 blocks, N=rows,
+//               K=64 tokens) into a TMEM accumulator of 4 x 64 columns.  P.V
+//               of a tile is issued the moment its probabilities are ready;
+//               QK^T of the next tile is issued whole once its data is in, so
+//               it never queues in the tensor pipe ahead of a ready P.V.
+//   warps 2..5  softmax: two threads per query row (32 logits each) read S
+//               from TMEM, mask, keep the running max / sum and write bf16
+//               probabilities into the tile's own rope-chunk slot (free once
+//               QK^T has read it), so P is double-buffered with the stages;
+//               O^T is rescaled in TMEM only when a running max grows by more
+//               than 2^8; the epilogue writes o = O / l and lse = m + ln l.
 //
 // Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
 // [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
@@ -36,22 +43,27 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
-constexpr uint32_t kBarSoftmax = 1;   // named barrier id for the softmax warps
+constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSoftmaxWarps = 4;
 
 struct Misc {
-  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
-  uint64_t q_full, q_empty, p_full, pv_done, o_free;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
+  // single barrier could complete two phases between tests and alias parities
+  uint64_t p_full[2], pv_done[2];
+  uint64_t q_full, q_empty, o_free;
   uint32_t tmem_base;
   int abort;
-  float alpha[kRows];
+  float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
   float inv_l[kRows];
 };
 
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTileBytes;
-constexpr int kSmemP = 3 * kTileBytes;
-constexpr int kSmemMisc = kSmemP + kRows * 128;
+constexpr int kSmemRope = 8 * kChunkBytes;          // rope chunk offset inside a stage (P after QK^T)
+constexpr int kSmemMisc = 3 * kTileBytes;
 constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // + misc + alignment slack
 static_assert(sizeof(Misc) <= 1024, "misc block");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -104,7 +116,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -125,32 +136,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sQ = smem_u32(smem + kSmemQ);
   const uint32_t sKV = smem_u32(smem + kSmemKV);
-  const uint32_t sP = smem_u32(smem + kSmemP);
+  // barrier addresses: the two stages' barriers are 8 bytes apart
   const uint32_t b_kv_full = smem_u32(&misc->kv_full[0]);
   const uint32_t b_kv_empty = smem_u32(&misc->kv_empty[0]);
   const uint32_t b_s_full = smem_u32(&misc->s_full[0]);
   const uint32_t b_s_empty = smem_u32(&misc->s_empty[0]);
   const uint32_t b_q_full = smem_u32(&misc->q_full), b_q_empty = smem_u32(&misc->q_empty);
-  const uint32_t b_p_full = smem_u32(&misc->p_full), b_pv_done = smem_u32(&misc->pv_done);
+  const uint32_t b_p_full = smem_u32(&misc->p_full[0]), b_pv_done = smem_u32(&misc->pv_done[0]);
   const uint32_t b_o_free = smem_u32(&misc->o_free);
   volatile int* abort_flag = &misc->abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(b_kv_full + 8 * i, 1);
-      mbar_init(b_kv_empty + 8 * i, 1);
-      mbar_init(b_s_full + 8 * i, 1);
-      mbar_init(b_s_empty + 8 * i, kSoftmaxThreads);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(b_kv_full + 8 * st, 1);
+      mbar_init(b_kv_empty + 8 * st, 1);
+      mbar_init(b_s_full + 8 * st, 1);
+      mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
+      mbar_init(b_p_full + 8 * st, kSoftmaxWarps);
+      mbar_init(b_pv_done + 8 * st, 1);
     }
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, 1);
-    mbar_init(b_p_full, kSoftmaxThreads);
-    mbar_init(b_pv_done, 1);
-    mbar_init(b_o_free, kSoftmaxThreads);
+    mbar_init(b_o_free, kSoftmaxWarps);
     misc->abort = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < kRows) misc->alpha[threadIdx.x] = 1.0f;
+  if (threadIdx.x < kRows) misc->alpha[0][threadIdx.x] = misc->alpha[1][threadIdx.x] = 1.0f;
   if (warp == 1) {
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -167,14 +178,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   PieceIter it;
   it.init(p.prefix, U, lo, hi);
-  int armed_kv[2] = {-1, -1}, armed_q = -1;  // producer: last armed phases
+  int armed_kv[2] = {-1, -1}, armed_q = -1;  // producer: last armed phase per barrier
   int unit, t0, t1, slot;
   bool whole;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane k < nv issues the nine 64-wide chunk boxes of page k of the tile;
-    // lane 0 arms the stage barrier with the whole tile's byte count first.
+    // Lane k < nv issues the boxes of page k of the tile; lane 0 arms each
+    // group barrier with the group's whole byte count first.
     const int nv = pd.layout == kInterleaved ? pd.num_shards : 1;  // page boxes per tile
     const int box_bytes = (kTile / nv) * 128;
     int gt = 0, pc = 0;
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int res = pd.layout == kInterleaved ? x.s : 0;
       int win_base = -1, win_val = -1;
       for (int j = t0; j < t1 && ok; ++j, ++gt) {
-        const int stage = gt & 1;
+        const int st = gt & 1;
         // page slot of this lane's box; nv divides 32, so a tile never
         // straddles two 32-entry windows of the block table
         const int first_slot = pd.layout == kInterleaved ? j * nv : x.p0 + j;
@@ -205,23 +216,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
         if (gt >= 2) {
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(b_kv_empty + 8 * stage, ((gt >> 1) - 1) & 1, tmo, abort_flag));
+                          mbar_wait(b_kv_empty + 8 * st, ((gt >> 1) - 1) & 1, tmo, abort_flag));
           if (!ok) break;
         }
-        const uint32_t full = b_kv_full + 8 * stage;
+        const uint32_t full = b_kv_full + 8 * st;
         if (lane == 0) {
           mbar_arrive_expect_tx(full, kTileBytes);
-          armed_kv[stage] = gt;
+          armed_kv[st] = gt;
         }
         __syncwarp();
         if (lane < nv) {
-          const uint32_t dst0 = sKV + stage * kTileBytes + lane * box_bytes;
+          const uint32_t dst = sKV + st * kTileBytes + lane * box_bytes;
 #pragma unroll
           for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(dst0 + c * kChunkBytes, &tm_kv, full, c * 64, res, 0, page);
+            tma_load_4d(dst + c * kChunkBytes, &tm_kv, full, c * 64, res, 0, page);
         }
         __syncwarp();
-        if (j == t0) {
+        if (ok && j == t0) {
           // query rows of this unit: reuse of the buffer waits for the last
           // QK^T of the previous piece
           if (pc >= 1) {
@@ -244,15 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    // Issues QK^T of tile j and P.V of tile j-1 in whichever order their
-    // inputs become ready (P.V first when both are): P.V is what releases a
-    // KV stage, so issuing it early lets the next tile's load start early.
     const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
     // descriptor bases; adding (byte offset >> 4) moves the start address
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
     const uint64_t dkv0 = sw128_desc(sKV, 16, 1024);
     const uint64_t dv0 = sw128_desc(sKV, kChunkBytes, 1024);
-    const uint64_t dp0 = sw128_desc(sP, 16, 1024);
+    const uint64_t dp0 = sw128_desc(sKV + kSmemRope, 16, 1024);  // P of stage 0
     int gbase = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -264,42 +272,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t t_idle = 0;
       while (ok && np < n) {
         bool did = false;
+        // P.V of the oldest tile whose probabilities are ready
         if (np < nq) {
           const int g = gbase + np;
-          bool ready = mbar_test(b_p_full, g & 1);
+          bool ready = mbar_test(b_p_full + 8 * (g & 1), (g >> 1) & 1);
           if (ready && np == 0 && pc >= 1) ready = mbar_test(b_o_free, (pc - 1) & 1);
           if (__all_sync(0xffffffffu, ready)) {
             tc_fence_after();
             if (lane == 0) {
-              const uint32_t st_off = (uint32_t)((g & 1) * kTileBytes) >> 4;
+              const int st = g & 1;
+              const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
 #pragma unroll
               for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t a = dv0 + st_off + (uint32_t)((2 * blk * kChunkBytes + kk * 2048) >> 4);
-                  const uint64_t bdesc = dp0 + (uint32_t)((32 * kk) >> 4);
-                  mma_bf16_ss(tmem + kColO + 64 * blk, a, bdesc, id_pv,
+                  const uint64_t a =
+                      dv0 + st_off + (uint32_t)((2 * blk * kChunkBytes + kk * 2048) >> 4);
+                  const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
+                  mma_bf16_ss(tmem + kColO + 64 * blk, a, bd, id_pv,
                               (np == 0 && kk == 0) ? 0u : 1u);
                 }
               }
-              mma_commit(b_pv_done);
-              mma_commit(b_kv_empty + 8 * (g & 1));
+              mma_commit(b_kv_empty + 8 * st);
+              mma_commit(b_pv_done + 8 * st);
             }
             __syncwarp();
             ++np;
             did = true;
           }
         }
+        // QK^T of the next tile, issued whole once all its chunk groups have
+        // landed: issued piecemeal, its MMAs would queue in the tensor pipe
+        // ahead of a P.V that becomes ready meanwhile, and P.V is what frees
+        // a stage for the next load
         if (!did && nq < n) {
           const int g = gbase + nq;
-          const int stage = g & 1;
-          bool ready = mbar_test(b_kv_full + 8 * stage, (g >> 1) & 1);
-          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * stage, ((g >> 1) - 1) & 1);
+          const int st = g & 1;
+          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 1) & 1);
+          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * st, ((g >> 1) - 1) & 1);
           if (__all_sync(0xffffffffu, ready)) {
             tc_fence_after();
             if (lane == 0) {
-              const uint32_t st_off = (uint32_t)(stage * kTileBytes) >> 4;
-              const uint32_t d = tmem + kColS0 + 64 * stage;
+              const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
+              const uint32_t d = tmem + kColS0 + 64 * st;
 #pragma unroll
               for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -308,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mma_bf16_ss(d, dq0 + off, dkv0 + st_off + off, id_qk, (c | k) ? 1u : 0u);
                 }
               }
-              mma_commit(b_s_full + 8 * stage);
+              mma_commit(b_s_full + 8 * st);
               if (nq == n - 1) mma_commit(b_q_empty);
             }
             __syncwarp();
@@ -319,9 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (did) {
           t_idle = 0;
         } else {
-          // nothing ready: park on the event expected next, then re-check
-          if (np < nq) mbar_try_wait_hint(b_p_full, (gbase + np) & 1, 200);
-          else mbar_try_wait_hint(b_kv_full + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 200);
+          // nothing ready: park briefly on the event expected next
+          if (np < nq) mbar_try_wait_hint(b_p_full + 8 * ((gbase + np) & 1), ((gbase + np) >> 1) & 1, 100);
+          else if (nq < n)
+            mbar_try_wait_hint(b_kv_full + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 100);
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) t_idle = now;
           if (now - t_idle > tmo || *abort_flag) ok = false;
@@ -334,85 +350,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
   } else {
     // ------------------------------------------------------------ softmax
-    const int sw = warp - 2;             // 0..3
+    // Thread (quadrant, lane) owns query row r = 16*quad + lane%16 and the
+    // 32 logits of half h = lane/16 of each tile (16x32bx2 TMEM loads).
     const int quad = warp & 3;           // TMEM lane quadrant this warp may access
     const int tid = threadIdx.x - 64;    // 0..127
-    const int r = 16 * quad + lane;      // query row owned by this thread (lane < 16)
+    const int half = lane >> 4;
+    const int r = 16 * quad + (lane & 15);
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-    (void)sw;
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit(pd, unit);
-      const bool owner = lane < 16 && r < x.rows;
+      const bool owner = r < x.rows;
       const int i_row = (x.g * kRows + r) / pd.H;           // query position of row r
       const int vis_limit = x.L - pd.q_len + i_row;          // causal: t <= vis_limit
-      float m_run = -CUDART_INF_F, l_run = 0.0f;
+      float m_run = -CUDART_INF_F, l_run = 0.0f;             // l_run: this half's sum
       for (int j = t0; j < t1; ++j, ++gt) {
         const int sb = gt & 1;
-        const bool ok_s = __all_sync(0xffffffffu,
-                                    ok && mbar_wait(b_s_full + 8 * sb, (gt >> 1) & 1, tmo, abort_flag));
+        const bool ok_s = __all_sync(
+            0xffffffffu, ok && mbar_wait(b_s_full + 8 * sb, (gt >> 1) & 1, tmo, abort_flag));
         bool resc = false;
-        uint32_t pk[32];
+        uint32_t pk[16];
         const bool full = tile_full(pd, x, j);
         if (ok_s) {
           tc_fence_after();
-          uint32_t sr[64];
-          {
-            uint32_t (&lo32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-            uint32_t (&hi32)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-            tmem_ld32(tmem + lane_off + kColS0 + 64 * sb, lo32);
-            tmem_ld32(tmem + lane_off + kColS0 + 64 * sb + 32, hi32);
-            tmem_wait_ld();
-          }
+          uint32_t sr[32];
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 64 * sb, sr);
+          tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(b_s_empty + 8 * sb);
-          if (owner) {
-            float s[64];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
+          float s[32];
 #pragma unroll
-            for (int a = 0; a < 64; ++a) s[a] = __uint_as_float(sr[a]);
-            if (!full) {
-#pragma unroll
-              for (int a = 0; a < 64; ++a) {
-                int t = slot_token(pd, x, j, a);
-                bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
-                if (!vis) s[a] = -CUDART_INF_F;
-              }
-            }
-            float mx = -CUDART_INF_F;
-#pragma unroll
-            for (int a = 0; a < 64; ++a) mx = fmaxf(mx, s[a]);
-            const float m_new = fmaxf(m_run, mx * pd.scale_log2);
-            float alpha = 1.0f;
-            if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
-              alpha = (m_run == -CUDART_INF_F) ? 0.0f : exp2f(m_run - m_new);
-              l_run *= alpha;
-              m_run = m_new;
-              resc = (j != t0);
-            }
-            misc->alpha[r] = alpha;
-            const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-            float lsum = 0.0f;
+          for (int a = 0; a < 32; ++a) s[a] = __uint_as_float(sr[a]);
+          if (!full) {
 #pragma unroll
             for (int a = 0; a < 32; ++a) {
-              float p0 = exp2f(fmaf(s[2 * a], pd.scale_log2, -m_use));
-              float p1 = exp2f(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
-              pk[a] = pack_bf16x2(p0, p1);
-              lsum += p0 + p1;
+              int t = slot_token(pd, x, j, 32 * half + a);
+              bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
+              if (!vis) s[a] = -CUDART_INF_F;
             }
-            l_run += lsum;
           }
+          float mx = -CUDART_INF_F;
+#pragma unroll
+          for (int a = 0; a < 32; ++a) mx = fmaxf(mx, s[a]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run, mx * pd.scale_log2);
+          float alpha = 1.0f;
+          if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
+            alpha = (m_run == -CUDART_INF_F) ? 0.0f : exp2f(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            resc = owner && (j != t0);
+          }
+          if (owner && half == 0) misc->alpha[gt & 1][r] = alpha;
+          const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+          float lsum = 0.0f;
+#pragma unroll
+          for (int a = 0; a < 16; ++a) {
+            const float p0 = exp2f(fmaf(s[2 * a], pd.scale_log2, -m_use));
+            const float p1 = exp2f(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
+            pk[a] = pack_bf16x2(p0, p1);
+            lsum += p0 + p1;
+          }
+          l_run += lsum;
         }
-        // every softmax thread reaches both reductions, so a failed wait
-        // anywhere in the group is seen by all of them at the same point
-        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
-        const bool any_resc = named_bar_or(kBarSoftmax, kSoftmaxThreads, resc);
-        // previous PV must be done before P is overwritten or O^T rescaled
-        const bool ok_pv = __all_sync(
-            0xffffffffu, (gt == 0) || mbar_wait(b_pv_done, (gt - 1) & 1, tmo, abort_flag));
-        ok = ok_pv;
-        if (!ok_pv) continue;  // caught by the next reduction (or the epilogue's)
-        if (any_resc) {
+        // every softmax thread reaches the reduction, so a failed wait
+        // anywhere in the group is seen by all of them at the same point;
+        // the common case (no failure, no rescale) costs one barrier
+        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, resc || !ok_s)) {
+          if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
+          // some row's running max grew: rescale O^T, which needs the
+          // previous P.V to have landed
+          const bool ok_pv = __all_sync(
+              0xffffffffu, (gt == 0) || mbar_wait(b_pv_done + 8 * ((gt - 1) & 1),
+                                                  ((gt - 1) >> 1) & 1, tmo, abort_flag));
+          ok = ok_pv;
+          if (!ok_pv) continue;  // caught by the next reduction (or the epilogue's)
           tc_fence_after();
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
@@ -424,18 +438,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < 32; ++c)
-                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[32 * h2 + c]);
+                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[gt & 1][32 * h2 + c]);
               tmem_st32(ta, v);
             }
           }
           tmem_wait_st();
         }
         if (owner) {
-          uint8_t* prow = smem + kSmemP + r * 128;
+          uint8_t* prow = smem + kSmemKV + (gt & 1) * kTileBytes + kSmemRope + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
+            const int ch = 4 * half + c;   // 16-byte chunk of the 128-byte row
             uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = v;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = v;
           }
         }
         if (!full) {
@@ -452,10 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(b_p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p_full + 8 * (gt & 1));
       }
       // ---------------------------------------------------------- epilogue
-      const bool ok_e = ok && mbar_wait(b_pv_done, (gt - 1) & 1, tmo, abort_flag);
+      const bool ok_e = __all_sync(
+          0xffffffffu, ok && mbar_wait(b_pv_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, tmo,
+                                       abort_flag));
       if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_e)) { ok = false; break; }
       tc_fence_after();
       float* dst_o;
@@ -469,10 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         dst_o = p.ws_o + sl * kRows * kDv;
         dst_lse = p.ws_lse + sl * kRows;
       }
-      if (owner) {
-        float lse = (l_run > 0.0f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f
+      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+      if (owner && half == 0) {
+        float lse = (l_tot > 0.0f) ? (m_run + __log2f(l_tot)) * 0.69314718055994530942f
                                    : -CUDART_INF_F;
-        misc->inv_l[r] = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+        misc->inv_l[r] = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
         dst_lse[r] = lse;
       }
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
@@ -492,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(b_o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_o_free);
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // inv_l reused by the next piece
       ++pc;
     }
