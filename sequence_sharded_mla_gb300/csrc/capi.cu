@@ -166,32 +166,59 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   pd.block_table = block_table;
   pd.seq_lens = seq_lens;
 
-  // query rows: [B*q_len*H, 576] bf16, boxes of 64 dims x 64 rows
+  // query rows: [B*q_len*H, 576] bf16.  Preferred view [rows][9 chunks][64]
+  // read as (64 dims, rows, chunk) so one box lands a 64-row group in the
+  // [chunk][row][64] shared-memory layout; fallback: one box per chunk.
   CUtensorMap tm_q, tm_kv;
+  int q_one_box = 1, kv_page_box = 0;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)pd.B * pd.R};
-    cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kRows};
-    cuuint32_t es[2] = {1, 1};
-    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides,
+    cuuint64_t dims[3] = {64, (cuuint64_t)pd.B * pd.R, (cuuint64_t)kChunks};
+    cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kChunks};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MLA_ERR_CUDA;
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      q_one_box = 0;
+      cuuint64_t d2[2] = {(cuuint64_t)kDqk, (cuuint64_t)pd.B * pd.R};
+      cuuint64_t s2[1] = {(cuuint64_t)kDqk * 2};
+      cuuint32_t b2[2] = {64, (cuuint32_t)kRows};
+      if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), d2, s2, b2, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_CUDA;
+    }
   }
-  // cache rows viewed as [page][row / nv][row % nv][576]; a box takes the
-  // 64/nv rows of one page that one shard owns (nv = N interleaved, else 1)
+  // cache rows.  When every row of a page belongs to the tile (contiguous
+  // shards, or one interleaved shard) the view [page][row][9 chunks][64] read
+  // as (64 dims, row, chunk, page) lands a whole page in one box.  Otherwise
+  // [page][row / nv][row % nv][576]: a box takes the 64/nv rows of one page
+  // that one shard owns, one 64-wide chunk at a time (nv = N interleaved).
+  const int nv = pd.layout == kInterleaved ? num_shards : 1;
   {
-    const int nv = pd.layout == kInterleaved ? num_shards : 1;
-    cuuint64_t dims[4] = {(cuuint64_t)kDqk, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
-                          (cuuint64_t)kv->num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kDqk * 2 * nv,
-                             (cuuint64_t)kDqk * 2 * kPage};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)(kPage / nv), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MLA_ERR_CUDA;
+    bool done = false;
+    if (nv == 1) {
+      cuuint64_t dims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)kChunks, (cuuint64_t)kv->num_pages};
+      cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, 128, (cuuint64_t)kDqk * 2 * kPage};
+      cuuint32_t box[4] = {64, (cuuint32_t)kPage, (cuuint32_t)kChunks, 1};
+      done = encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
+                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      kv_page_box = done ? 1 : 0;
+    }
+    if (!done) {
+      cuuint64_t dims[4] = {(cuuint64_t)kDqk, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
+                            (cuuint64_t)kv->num_pages};
+      cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kDqk * 2 * nv,
+                               (cuuint64_t)kDqk * 2 * kPage};
+      cuuint32_t box[4] = {64, 1, (cuuint32_t)(kPage / nv), 1};
+      if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
+                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_CUDA;
+    }
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -203,8 +230,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.prefix = reinterpret_cast<int*>(ws + wl.prefix);
   p.ws_o = reinterpret_cast<float*>(ws + wl.ws_o);
   p.ws_lse = reinterpret_cast<float*>(ws + wl.ws_lse);
-  p.kv_bytes = static_cast<const uint8_t*>(kv->data);
   p.kv_scale = kv->scale;
+  p.kv_page_box = kv_page_box;
+  p.q_one_box = q_one_box;
   p.kv_fp8 = nullptr;
   p.timeout_ns = kTimeoutNs;
 

@@ -13,8 +13,11 @@
 //               (one TMA box per page and 64-wide chunk, 128-byte swizzle)
 //               into two stages; a stage is refilled as soon as its P.V is
 //               done.
-//   warp 1      MMA issuer: S = Q K^T (M=64 rows, N=64 tokens, K=576) into
-//               TMEM, group by group as the data lands, and
+//   warps 1, 6  MMA issuers (two, on different SM sub-partitions: one issuing
+//               thread cannot keep the tensor pipe full with MMAs this small).
+//               Each issues half of S = Q K^T (M=64 rows, N=64 tokens; even /
+//               odd 64-wide chunks of K=576 into two TMEM accumulators that
+//               the softmax adds) and two of the four latent blocks of
 //               O^T += V^T P^T (M=128 latent dims x 4 blocks, N=rows,
 //               K=64 tokens) into a TMEM accumulator of 4 x 64 columns.  P.V
 //               of a tile is issued the moment its probabilities are ready;
@@ -41,7 +44,8 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kIssuers = 2;                // MMA-issuing warps (1 and 6)
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -68,9 +72,10 @@ constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // + misc + alignment slack
 static_assert(sizeof(Misc) <= 1024, "misc block");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// TMEM columns: S double buffer (M=64 layout), then four O^T blocks.
+// TMEM columns: per stage two partial S accumulators (M=64 layout, 64
+// columns each: stage st, issuer i at 128*st + 64*i), then four O^T blocks.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColO = 128;
+constexpr uint32_t kColS0 = 0, kColO = 256;
 
 struct PieceIter {
   const int* prefix;
@@ -149,14 +154,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
       mbar_init(b_kv_full + 8 * st, 1);
-      mbar_init(b_kv_empty + 8 * st, 1);
-      mbar_init(b_s_full + 8 * st, 1);
+      mbar_init(b_kv_empty + 8 * st, kIssuers);
+      mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
       mbar_init(b_p_full + 8 * st, kSoftmaxWarps);
-      mbar_init(b_pv_done + 8 * st, 1);
+      mbar_init(b_pv_done + 8 * st, kIssuers);
     }
     mbar_init(b_q_full, 1);
-    mbar_init(b_q_empty, 1);
+    mbar_init(b_q_empty, kIssuers);
     mbar_init(b_o_free, kSoftmaxWarps);
     misc->abort = 0;
     fence_mbar_init();
@@ -225,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed_kv[st] = gt;
         }
         __syncwarp();
-        if (lane < nv) {
+        if (p.kv_page_box) {
+          if (lane == 0) tma_load_4d(sKV + st * kTileBytes, &tm_kv, full, 0, 0, 0, page);
+        } else if (lane < nv) {
           const uint32_t dst = sKV + st * kTileBytes + lane * box_bytes;
 #pragma unroll
           for (int c = 0; c < kChunks; ++c)
@@ -243,9 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(b_q_full, kTileBytes);
             armed_q = pc;
             const int row0 = x.b * pd.R + x.g * kRows;
+            if (p.q_one_box) {
+              tma_load_3d(sQ, &tm_q, b_q_full, 0, row0, 0);
+            } else {
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-              tma_load_2d(sQ + c * kChunkBytes, &tm_q, b_q_full, c * 64, row0);
+              for (int c = 0; c < kChunks; ++c)
+                tma_load_2d(sQ + c * kChunkBytes, &tm_q, b_q_full, c * 64, row0);
+            }
           }
           __syncwarp();
         }
@@ -253,8 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issue
+    const int mi = warp == 6 ? 1 : 0;    // issuer index: chunk parity / latent half
     const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
     // descriptor bases; adding (byte offset >> 4) moves the start address
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
@@ -283,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int st = g & 1;
               const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
 #pragma unroll
-              for (int blk = 0; blk < 4; ++blk) {
+              for (int blk = 2 * mi; blk < 2 * mi + 2; ++blk) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   const uint64_t a =
@@ -314,13 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (lane == 0) {
               const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
-              const uint32_t d = tmem + kColS0 + 64 * st;
+              const uint32_t d = tmem + kColS0 + 128 * st + 64 * mi;
 #pragma unroll
-              for (int c = 0; c < kChunks; ++c) {
+              for (int c = mi; c < kChunks; c += kIssuers) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   const uint32_t off = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
-                  mma_bf16_ss(d, dq0 + off, dkv0 + st_off + off, id_qk, (c | k) ? 1u : 0u);
+                  mma_bf16_ss(d, dq0 + off, dkv0 + st_off + off, id_qk,
+                              (c != mi || k != 0) ? 1u : 0u);
                 }
               }
               mma_commit(b_s_full + 8 * st);
@@ -374,15 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = tile_full(pd, x, j);
         if (ok_s) {
           tc_fence_after();
-          uint32_t sr[32];
-          tmem_ld16x2_32(tmem + lane_off + kColS0 + 64 * sb, sr);
+          uint32_t sr[32], sr2[32];
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb, sr);
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb + 64, sr2);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
           float s[32];
 #pragma unroll
-          for (int a = 0; a < 32; ++a) s[a] = __uint_as_float(sr[a]);
+          for (int a = 0; a < 32; ++a) s[a] = __uint_as_float(sr[a]) + __uint_as_float(sr2[a]);
           if (!full) {
 #pragma unroll
             for (int a = 0; a < 32; ++a) {
