@@ -13,7 +13,9 @@
  * Conventions for every entry point:
  *   - Pointers named "device" must be device memory of the current CUDA
  *     device, 16-byte aligned.  The caller owns every buffer; the library
- *     keeps no pointer after a call returns and allocates no device memory.
+ *     keeps no pointer after a call returns and allocates no device memory
+ *     at run time (its one static buffer, the scratch of
+ *     mla_decode_partial_noalloc, exists from library load to process exit).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream).  Argument errors are detected on
  *     the host and returned before anything is launched.
@@ -124,6 +126,37 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
                               const mla_shape* shape, int shard_id, int num_shards,
                               mla_layout layout, float* out_partial, float* lse_partial,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_partial without a workspace argument, for callers that cannot
+ * allocate device memory (for example code running while a serving engine's
+ * pool already owns the whole GPU, allocator or out-of-memory callbacks, or
+ * loops where an allocation is not allowed).  The pages this library follows
+ * have no counterpart of this call; it exists only for such callers.
+ *
+ * The work list and split partial results live in a fixed scratch buffer
+ * that the library keeps in device memory: about 40 MiB on every GPU that
+ * loads the library, held until the process exits.  Shapes whose workspace
+ * (mla_workspace_size) would exceed it, i.e. more than 8192 work units
+ * (batch x computed shards x ceil(q_len * num_heads / 64)) or a GPU with
+ * more than 160 SMs, return MLA_ERR_UNSUPPORTED before any launch.
+ * Arguments, layouts, results and host-side errors are those of
+ * mla_decode_partial.
+ *
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on a device share the one scratch buffer, so calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race:
+ * order them on one stream.  Nothing needs clearing between calls; each call
+ * rebuilds what it reads.  Device-side error words (see
+ * mla_get_device_error) are kept in the scratch and are not reported by this
+ * call.
+ */
+mla_status mla_decode_partial_noalloc(const void* q, const mla_kv_pages* kv,
+                                      const int32_t* block_table, int max_pages_per_req,
+                                      const int32_t* seq_lens, const mla_shape* shape,
+                                      int shard_id, int num_shards, mla_layout layout,
+                                      float* out_partial, float* lse_partial, void* stream);
 
 /*
  * LSE combine of N shard partials ("Decode Context Parallelism", section 4.1:

@@ -43,8 +43,8 @@ class mla_kv_pages(ctypes.Structure):
 
 
 _LIB = None
-EXPORTS = ("mla_decode_partial", "mla_shard_combine", "mla_workspace_size",
-           "mla_get_device_error", "mla_status_string", "mla_version")
+EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
+           "mla_workspace_size", "mla_get_device_error", "mla_status_string", "mla_version")
 
 
 def lib():
@@ -58,6 +58,10 @@ def lib():
                                          ctypes.POINTER(mla_shape), i32, i32, i32, vp, vp, vp,
                                          sz, vp]
         L.mla_decode_partial.restype = i32
+        L.mla_decode_partial_noalloc.argtypes = [vp, ctypes.POINTER(mla_kv_pages), vp, i32, vp,
+                                                 ctypes.POINTER(mla_shape), i32, i32, i32, vp,
+                                                 vp, vp]
+        L.mla_decode_partial_noalloc.restype = i32
         L.mla_shard_combine.argtypes = [vp, vp, i32, ctypes.POINTER(mla_shape), vp, vp, vp, vp]
         L.mla_shard_combine.restype = i32
         L.mla_workspace_size.argtypes = [ctypes.POINTER(mla_shape), i32, i32]
@@ -158,6 +162,39 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
     if st != 0:
         raise MLAError(st, "mla_decode_partial")
     return out_partial, lse_partial, workspace
+
+
+def mla_decode_partial_noalloc(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
+                               shard_id=ALL_SHARDS, kv_scale=None, causal=False,
+                               softmax_scale=DEFAULT_SCALE, out_partial=None, lse_partial=None,
+                               stream=None):
+    """mla_decode_partial on the library's fixed scratch buffer (no workspace).
+
+    For callers that may not allocate device memory; the output tensors are
+    still supplied by (or allocated here for) the caller.  All calls on a
+    device share one scratch buffer: keep calls on one stream.
+    Returns (out_partial, lse_partial).
+    """
+    _check(q, "q", (torch.bfloat16,), 4)
+    dev = q.device
+    B, q_len, H, _ = q.shape
+    kv_dtype = KV_BF16 if kv.dtype == torch.bfloat16 else KV_FP8
+    n_out = num_shards if shard_id == ALL_SHARDS else 1
+    if out_partial is None:
+        out_partial = torch.empty((n_out, B, q_len, H, D_V), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
+    sh = _shape(B, q_len, H, causal, softmax_scale)
+    pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
+                         kv_dtype, kv.shape[0], kv.shape[1])
+    st = lib().mla_decode_partial_noalloc(_ptr(q), ctypes.byref(pages), _ptr(block_table),
+                                          block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
+                                          int(shard_id), int(num_shards), LAYOUTS[layout],
+                                          _ptr(out_partial), _ptr(lse_partial),
+                                          _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "mla_decode_partial_noalloc")
+    return out_partial, lse_partial
 
 
 def mla_shard_combine(partials, lses, w_uv=None, out=None, lse_out=None, stream=None,

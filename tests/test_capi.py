@@ -51,3 +51,18 @@ def test_python_binding_names_match_the_abi():
     import sequence_sharded_mla_gb300 as mla
     for name in declared_functions():
         assert callable(getattr(mla, name)), name
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch_before_any_cuda_call():
+    """The no-allocation entry point checks its stated limits (at most 8192
+    work units) with host arithmetic first, so the refusal needs no GPU and
+    no buffers are ever touched."""
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    sh = mla.mla_shape(4096, 1, 64, 0, 0.07)        # 4096 requests x 8 shards = 32768 units
+    kv = mla.mla_kv_pages(None, None, 0, 1, 64)
+    st = L.mla_decode_partial_noalloc(None, ctypes.byref(kv), None, 1, None, ctypes.byref(sh),
+                                      -1, 8, 0, None, None, None)
+    assert st == -2
+    assert L.mla_decode_partial_noalloc(None, ctypes.byref(kv), None, 1, None, None, -1, 8, 0,
+                                        None, None, None) == -1
