@@ -14,6 +14,8 @@ namespace mla {
 int partial_smem_bytes();
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const PartialParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                               const PartialParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
                         int min_tiles, cudaStream_t stream);
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
@@ -130,8 +132,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (kv->dtype == MLA_KV_BF16) {
     if (kv->scale != nullptr) return MLA_ERR_INVALID;
   } else if (kv->dtype == MLA_KV_FP8_E4M3) {
-    if (kv->scale == nullptr) return MLA_ERR_INVALID;
-    return MLA_ERR_UNSUPPORTED;
+    if (kv->scale == nullptr || !aligned16(kv->scale)) return MLA_ERR_INVALID;
   } else {
     return MLA_ERR_INVALID;
   }
@@ -195,7 +196,22 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // [page][row / nv][row % nv][576]: a box takes the 64/nv rows of one page
   // that one shard owns, one 64-wide chunk at a time (nv = N interleaved).
   const int nv = pd.layout == kInterleaved ? num_shards : 1;
-  {
+  const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
+  if (fp8) {
+    // e4m3 codes: view [page][row / nv][row % nv][3][192] read as
+    // (192 codes, third, residue, row / nv, page); a box lands the 64/nv rows
+    // of one page that one shard owns, each row's 576 codes contiguous
+    cuuint64_t dims[5] = {192, 3, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
+                          (cuuint64_t)kv->num_pages};
+    cuuint64_t strides[4] = {192, (cuuint64_t)kDqk, (cuuint64_t)kDqk * nv,
+                             (cuuint64_t)kDqk * kPage};
+    cuuint32_t box[5] = {192, 3, 1, (cuuint32_t)(kPage / nv), 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  } else {
     cuuint32_t es[4] = {1, 1, 1, 1};
     bool done = false;
     if (nv == 1) {
@@ -238,7 +254,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, st) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_partial_bf16(tm_q, tm_kv, p, grid, st) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t le = fp8 ? launch_partial_fp8(tm_q, tm_kv, p, grid, st)
+                             : launch_partial_bf16(tm_q, tm_kv, p, grid, st);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_merge(pd, p.hdr, p.prefix, p.ws_o, p.ws_lse, out_partial, lse_partial, U, st) !=
       cudaSuccess)
     return MLA_ERR_CUDA;

@@ -30,6 +30,14 @@
 //               O^T is rescaled in TMEM only when a running max grows by more
 //               than 2^8; the epilogue writes o = O / l and lse = m + ln l.
 //
+// fp8 caches (OCP e4m3 codes + one fp32 scale per token): the producer lands
+// a tile's codes (36 KB) in the upper half of the tile's 72 KB stage, one TMA
+// box per page, and the token scales next to it (4-byte cp.async counted on
+// the same barrier); warps 7..10 expand the codes to bf16 in place (e4m3 ->
+// bf16 is exact) in the swizzled layout the MMAs read.  The scales are folded
+// into the logits and into P before its bf16 rounding, so both MMAs see the
+// exact dequantised values.
+//
 // Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
 // [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
 // written straight to out_partial; pieces of a split unit go to workspace
@@ -45,6 +53,11 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 224;
+constexpr int kThreadsFp8 = 352;           // + four converter warps (7..10)
+constexpr int kConvThreads = 128;
+constexpr uint32_t kBarConv = 2;           // named barrier id for the converter warps
+constexpr int kFp8TileBytes = kTile * kDqk;  // 36864: codes of one tile
+constexpr int kFp8Staging = kTileBytes - kFp8TileBytes;  // codes land in the stage's upper half
 constexpr int kIssuers = 2;                // MMA-issuing warps (1 and 6)
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
@@ -57,19 +70,21 @@ struct Misc {
   // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
   // single barrier could complete two phases between tests and alias parities
   uint64_t p_full[2], pv_done[2];
+  uint64_t kv_conv[2];  // fp8: stage expanded to bf16
   uint64_t q_full, q_empty, o_free;
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
   float inv_l[kRows];
+  float scale[2][kTile];  // fp8: per-token scales of the tile in each stage
 };
 
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTileBytes;
 constexpr int kSmemRope = 8 * kChunkBytes;          // rope chunk offset inside a stage (P after QK^T)
 constexpr int kSmemMisc = 3 * kTileBytes;
-constexpr int kSmemBytes = kSmemMisc + 1024 + 1024;  // + misc + alignment slack
-static_assert(sizeof(Misc) <= 1024, "misc block");
+constexpr int kSmemBytes = kSmemMisc + 2048 + 1024;  // + misc + alignment slack
+static_assert(sizeof(Misc) <= 2048, "misc block");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM columns: per stage two partial S accumulators (M=64 layout, 64
@@ -123,9 +138,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_partial_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
-                            const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+    mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -149,11 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_q_full = smem_u32(&misc->q_full), b_q_empty = smem_u32(&misc->q_empty);
   const uint32_t b_p_full = smem_u32(&misc->p_full[0]), b_pv_done = smem_u32(&misc->pv_done[0]);
   const uint32_t b_o_free = smem_u32(&misc->o_free);
+  const uint32_t b_kv_conv = smem_u32(&misc->kv_conv[0]);
+  // the MMAs wait for the stage in bf16: straight from TMA, or after expansion
+  const uint32_t b_kv_ready = kFp8 ? b_kv_conv : b_kv_full;
   volatile int* abort_flag = &misc->abort;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
-      mbar_init(b_kv_full + 8 * st, 1);
+      mbar_init(b_kv_full + 8 * st, kFp8 ? 1 + 32 : 1);  // fp8: + one cp.async arrival per lane
+      mbar_init(b_kv_conv + 8 * st, kConvThreads / 32);
       mbar_init(b_kv_empty + 8 * st, kIssuers);
       mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
@@ -226,11 +246,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t full = b_kv_full + 8 * st;
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, kTileBytes);
+          mbar_arrive_expect_tx(full, kFp8 ? kFp8TileBytes : kTileBytes);
           armed_kv[st] = gt;
         }
         __syncwarp();
-        if (p.kv_page_box) {
+        if constexpr (kFp8) {
+          // codes: one box per page, rows of 576 codes (row-major) in the
+          // stage's upper half; scales: one 4-byte copy per token slot
+          if (lane < nv)
+            tma_load_5d(sKV + st * kTileBytes + kFp8Staging + lane * (kTile / nv) * kDqk, &tm_kv,
+                        full, 0, 0, res, 0, page);
+          const int rows_per = kTile / nv;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int a = lane + 32 * h;             // token slot
+            const int k = a / rows_per;              // page box of the slot
+            const int pg = __shfl_sync(0xffffffffu, page, k);
+            const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
+            const float* src = p.kv_scale + (okpg ? (size_t)pg * kPage + (a % rows_per) * nv + res : 0);
+            cp_async_4(smem_u32(&misc->scale[st][a]), src);
+          }
+          cp_async_mbar_arrive_noinc(full);
+        } else if (p.kv_page_box) {
           if (lane == 0) tma_load_4d(sKV + st * kTileBytes, &tm_kv, full, 0, 0, 0, page);
         } else if (lane < nv) {
           const uint32_t dst = sKV + st * kTileBytes + lane * box_bytes;
@@ -320,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!did && nq < n) {
           const int g = gbase + nq;
           const int st = g & 1;
-          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 1) & 1);
+          bool ready = mbar_test(b_kv_ready + 8 * st, (g >> 1) & 1);
           if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * st, ((g >> 1) - 1) & 1);
           if (__all_sync(0xffffffffu, ready)) {
             tc_fence_after();
@@ -350,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // nothing ready: park briefly on the event expected next
           if (np < nq) mbar_try_wait_hint(b_p_full + 8 * ((gbase + np) & 1), ((gbase + np) >> 1) & 1, 100);
           else if (nq < n)
-            mbar_try_wait_hint(b_kv_full + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 100);
+            mbar_try_wait_hint(b_kv_ready + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 100);
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) t_idle = now;
           if (now - t_idle > tmo || *abort_flag) ok = false;
@@ -361,6 +398,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else if (kFp8 && warp >= 7) {
+    // ------------------------------------------------------------ fp8 -> bf16
+    // Thread t expands, for every 64-wide chunk c, 32 codes of tile row t/2
+    // (half t%2 of the chunk) into the swizzled bf16 plane c.  Planes 0..3
+    // lie below the codes; planes 4..8 overlap them, so their codes are read
+    // into registers first and written after a barrier over the converter
+    // warps.
+    const int ct = threadIdx.x - 7 * 32;   // 0..127
+    const int row = ct >> 1, hh = ct & 1;
+    int gt = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      for (int j = t0; j < t1; ++j, ++gt) {
+        const int st = gt & 1;
+        ok = __all_sync(0xffffffffu,
+                        ok && mbar_wait(b_kv_full + 8 * st, (gt >> 1) & 1, tmo, abort_flag));
+        // every converter thread reaches the barrier, failure or not
+        const bool any_fail = named_bar_or(kBarConv, kConvThreads, !ok);
+        if (any_fail) { ok = false; break; }
+        uint8_t* stage = smem + kSmemKV + st * kTileBytes;
+        const uint8_t* src = stage + kFp8Staging + row * kDqk + 32 * hh;
+        uint4 hi[5][2];
+#pragma unroll
+        for (int c = 4; c < kChunks; ++c) {
+          hi[c - 4][0] = *reinterpret_cast<const uint4*>(src + 64 * c);
+          hi[c - 4][1] = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
+        }
+        auto put = [&](int c, uint4 a, uint4 b) {
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          uint8_t* dst = stage + c * kChunkBytes + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {     // 16-byte output chunk 4*hh + q
+            const uint2 lo2 = e4m3x4_to_bf16x4(w[2 * q]);
+            const uint2 hi2 = e4m3x4_to_bf16x4(w[2 * q + 1]);
+            const int ch = 4 * hh + q;
+            *reinterpret_cast<uint4*>(dst + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
+          }
+        };
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 a = *reinterpret_cast<const uint4*>(src + 64 * c);
+          const uint4 b = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
+          put(c, a, b);
+        }
+        named_bar_sync(kBarConv, kConvThreads);   // all codes of planes 4..8 are in registers
+#pragma unroll
+        for (int c = 4; c < kChunks; ++c) put(c, hi[c - 4][0], hi[c - 4][1]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_kv_conv + 8 * st);
+      }
+    }
+    if (!ok && ct == 0) set_error(p, misc, kErrTimeout);
   } else {
     // ------------------------------------------------------------ softmax
     // Thread (quadrant, lane) owns query row r = 16*quad + lane%16 and the
@@ -394,15 +485,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
-          float s[32];
+          float s[32], sc[32];
 #pragma unroll
           for (int a = 0; a < 32; ++a) s[a] = __uint_as_float(sr[a]) + __uint_as_float(sr2[a]);
+          if constexpr (kFp8) {
+            // the scales were copied with the codes; acquire them from the
+            // stage barrier (long complete: QK^T already consumed the stage)
+            int never = 0;
+            mbar_wait(b_kv_full + 8 * sb, (gt >> 1) & 1, tmo, &never);
+            const float4* scp = reinterpret_cast<const float4*>(&misc->scale[sb][32 * half]);
+#pragma unroll
+            for (int a4 = 0; a4 < 8; ++a4) {
+              const float4 v = scp[a4];
+              sc[4 * a4] = v.x;
+              sc[4 * a4 + 1] = v.y;
+              sc[4 * a4 + 2] = v.z;
+              sc[4 * a4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int a = 0; a < 32; ++a) s[a] *= sc[a];   // logits of the dequantised keys
+          }
           if (!full) {
 #pragma unroll
             for (int a = 0; a < 32; ++a) {
               int t = slot_token(pd, x, j, 32 * half + a);
               bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
-              if (!vis) s[a] = -CUDART_INF_F;
+              if (!vis) {
+                s[a] = -CUDART_INF_F;
+                sc[a] = 0.0f;   // a masked slot's scale may be garbage (even NaN)
+              }
             }
           }
           float mx = -CUDART_INF_F;
@@ -424,7 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < 16; ++a) {
             const float p0 = exp2f(fmaf(s[2 * a], pd.scale_log2, -m_use));
             const float p1 = exp2f(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
-            pk[a] = pack_bf16x2(p0, p1);
+            if constexpr (kFp8) {
+              // P.V multiplies the codes; the token scale rides on P
+              pk[a] = pack_bf16x2(p0 * sc[2 * a], p1 * sc[2 * a + 1]);
+            } else {
+              pk[a] = pack_bf16x2(p0, p1);
+            }
             lsum += p0 + p1;
           }
           l_run += lsum;
@@ -551,19 +667,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                const PartialParams& p, int grid, cudaStream_t stream) {
+template <bool kFp8>
+static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                  const PartialParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_bf16_kernel,
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  mla_partial_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  mla_partial_kernel<kFp8><<<grid, kFp8 ? kThreadsFp8 : kThreads, kSmemBytes, stream>>>(tm_q, tm_kv,
+                                                                                       p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                const PartialParams& p, int grid, cudaStream_t stream) {
+  return launch_partial<false>(tm_q, tm_kv, p, grid, stream);
+}
+
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                               const PartialParams& p, int grid, cudaStream_t stream) {
+  return launch_partial<true>(tm_q, tm_kv, p, grid, stream);
 }
 
 }  // namespace mla

@@ -138,6 +138,42 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w, int v) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+      : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (LDGSTS).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies are done
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Four OCP e4m3 codes -> four bf16 values (exact), as two bf16x2 words.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t codes) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(codes & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(codes >> 16)));
+  float f0, f1, f2, f3;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h01 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h01 >> 16)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f2) : "h"((unsigned short)(h23 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f3) : "h"((unsigned short)(h23 >> 16)));
+  uint32_t b01, b23;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b01) : "f"(f1), "f"(f0));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b23) : "f"(f3), "f"(f2));
+  return make_uint2(b01, b23);
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z, int w) {
   asm volatile(

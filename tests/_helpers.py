@@ -5,6 +5,9 @@ import numpy as np
 import oracle
 
 # Contract tolerances: bf16 outputs of order 1 within 1e-2, LSE within 1e-3.
+# For outputs whose magnitude exceeds 1 (single-token contexts of N(0,1)
+# caches reach ~5) the 1e-2 applies relative to that magnitude: a bf16 output
+# cannot be closer than 2^-9 of its own value, whatever the kernel does.
 TOL_OUT = 1e-2
 TOL_LSE = 1e-3
 # Derived bound: the kernel rounds each probability to bf16 before P.V
@@ -64,6 +67,8 @@ def check_close(got, ref, tol_abs, what, rel=None):
     r = np.where(both_inf, 0.0, ref)
     assert np.all(np.isfinite(g)), f"{what}: non-finite values"
     err = float(np.max(np.abs(g - r))) if g.size else 0.0
+    if rel is not None and g.size:
+        tol_abs = tol_abs * max(1.0, float(np.max(np.abs(r))))
     assert err <= tol_abs, f"{what}: max abs err {err:.3e} > {tol_abs:.1e}"
     if rel is not None and g.size:
         scale = float(np.max(np.abs(r)))

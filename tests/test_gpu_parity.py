@@ -152,3 +152,20 @@ def test_invalid_arguments_rejected_before_launch(dev):
         mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 2,
                                workspace=small_ws)
     assert e.value.status == -6
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
+@pytest.mark.parametrize("N", [1, 2, 8])
+def test_fp8_cache(dev, layout, N):
+    """fp8 e4m3 cache with one fp32 scale per token; unused rows and pages
+    carry NaN codes and NaN scales."""
+    lens = [1, 63, 65, 1000, 4097]
+    w = mi.build_workload("fp8", len(lens), 1, 64, lens, N, layout, "fp8", False, seed=400 + N,
+                          kv_sigma=1.0, poison=True, extra_pages=2)
+    compare_all(w, dev)
+
+
+def test_fp8_causal_verify_with_wuv(dev):
+    w = mi.build_workload("fp8v", 3, 9, 32, [300, 9, 2000], 2, "interleaved", "fp8", True,
+                          seed=410, kv_sigma=1.0, poison=True, with_w_uv=True)
+    compare_all(w, dev)
