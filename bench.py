@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA sharded decode: KV HBM GB/s (% of ~8 TB/s peak), decode steps/s per layer"
-CONFIG_ID = 2
+DEFAULT_CONFIG = 2     # the bimodal agentic batch the metric is quoted on
 
 
 def load_peaks():
@@ -151,7 +151,7 @@ def run_reference(args, world, rank):
         return
     import mla_inputs as mi
     import oracle
-    w = mi.config_workload(CONFIG_ID)
+    w = mi.config_workload(args.config)
     threads = oracle.num_threads()
     per = 1152
     # one step = the oracle over a bounded sample of the workload
@@ -170,7 +170,7 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / len(results) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": mi.CONFIG_NAMES[CONFIG_ID], "batch": w.batch,
+            "config": {"workload": mi.CONFIG_NAMES[args.config], "batch": w.batch,
                        "heads": w.num_heads, "q_len": w.q_len, "num_shards": w.num_shards,
                        "layout": w.layout, "kv_dtype": w.kv_dtype,
                        "total_tokens": w.total_tokens},
@@ -192,31 +192,47 @@ def run_gpu(args, world, rank, local, dist):
     dev = torch.device("cuda", local)
     mla.lib()
     # each rank decodes its own batch of the same shape (independent requests)
-    w = mi.config_workload(CONFIG_ID, pinned=True)
+    w = mi.config_workload(args.config, pinned=True)
     if args.requests:
         # a reduced copy of the workload (first K requests) for profiling runs
-        w = mi.build_workload(w.name + f"-first{args.requests}", args.requests, 1, 64,
-                              w.seq_lens[:args.requests], 4, "interleaved", "bf16", False,
-                              seed=2, pinned=True)
+        w = mi.build_workload(w.name + f"-first{args.requests}", args.requests, w.q_len,
+                              w.num_heads, w.seq_lens[:args.requests], w.num_shards, w.layout,
+                              w.kv_dtype, w.causal, seed=w.seed, pinned=True,
+                              kv_sigma=1.0 if w.kv_dtype == "fp8" else 0.5,
+                              with_w_uv=w.w_uv is not None)
     if rank > 0:
-        lens = mi.agentic_lengths(2 + 1000 * rank, 32)
-        w = mi.build_workload(w.name, 32, 1, 64, lens, 4, "interleaved", "bf16", False,
-                              seed=2 + 1000 * rank, pinned=True)
+        # every rank decodes its own, independently seeded batch of the same shape
+        w2 = mi.config_workload(args.config, pinned=False)
+        seed = w2.seed + 1000 * rank
+        lens = mi.agentic_lengths(seed, w2.batch) if args.config == 2 else w2.seq_lens
+        w = mi.build_workload(w.name, w.batch, w.q_len, w.num_heads, lens, w.num_shards,
+                              w.layout, w.kv_dtype, w.causal, seed=seed, pinned=True,
+                              kv_sigma=1.0 if w.kv_dtype == "fp8" else 0.5,
+                              with_w_uv=w.w_uv is not None)
     B, H, q_len, N = w.batch, w.num_heads, w.q_len, w.num_shards
     kv_bytes = w.kv_bytes()
 
     h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
-    h_kv = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16)
+    if w.kv_dtype == "bf16":
+        h_kv = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16)
+        h_sc = None
+    else:
+        h_kv = torch.from_numpy(w.kv)
+        h_sc = torch.from_numpy(w.kv_scale)
+    h_wuv = None if w.w_uv is None else torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16)
     h_bt = torch.from_numpy(w.block_table).pin_memory()
     h_sl = torch.from_numpy(w.seq_lens).pin_memory()
     d_q = h_q.to(dev)
     d_kv = h_kv.to(dev)
+    d_sc = None if h_sc is None else h_sc.to(dev)
+    d_wuv = None if h_wuv is None else h_wuv.to(dev)
     d_bt = h_bt.to(dev)
     d_sl = h_sl.to(dev)
     stream = torch.cuda.current_stream(dev)
     part = torch.empty((N, B, q_len, H, 512), dtype=torch.float32, device=dev)
     lsep = torch.empty((N, B, q_len, H), dtype=torch.float32, device=dev)
-    out = torch.empty((B, q_len, H, 512), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((B, q_len, H, 512 if d_wuv is None else 128), dtype=torch.bfloat16,
+                      device=dev)
     lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
     ws = torch.empty((mla.mla_workspace_size(B, q_len, H, N),), dtype=torch.uint8, device=dev)
     h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
@@ -227,11 +243,11 @@ def run_gpu(args, world, rank, local, dist):
     def step(i=None):
         if i is not None:
             ev_p[2 * i].record(stream)
-        mla.mla_decode_partial(d_q, d_kv, d_bt, d_sl, N, w.layout, out_partial=part,
-                               lse_partial=lsep, workspace=ws, stream=stream)
+        mla.mla_decode_partial(d_q, d_kv, d_bt, d_sl, N, w.layout, kv_scale=d_sc, causal=w.causal,
+                               out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
         if i is not None:
             ev_p[2 * i + 1].record(stream)
-        mla.mla_shard_combine(part, lsep, out=out, lse_out=lse, stream=stream)
+        mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
 
     def barrier():
         if dist is not None:
@@ -260,13 +276,16 @@ def run_gpu(args, world, rank, local, dist):
         raise RuntimeError(f"device error status {status}")
 
     # end to end through host buffers: copy the step's inputs in, read results out
-    h2d = h_q.numel() * 2 + h_kv.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
+    h2d = (h_q.numel() * 2 + h_kv.numel() * h_kv.element_size() + h_bt.numel() * 4 +
+           h_sl.numel() * 4 + (0 if h_sc is None else h_sc.numel() * 4))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_step():
         d_q.copy_(h_q, non_blocking=True)
         d_kv.copy_(h_kv, non_blocking=True)
+        if h_sc is not None:
+            d_sc.copy_(h_sc, non_blocking=True)
         d_bt.copy_(h_bt, non_blocking=True)
         d_sl.copy_(h_sl, non_blocking=True)
         step()
@@ -303,10 +322,11 @@ def run_gpu(args, world, rank, local, dist):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": mi.CONFIG_NAMES[CONFIG_ID], "batch": B, "heads": H, "q_len": q_len,
-                   "num_shards": N, "layout": w.layout, "kv_dtype": "bf16",
+        "config": {"workload": mi.CONFIG_NAMES[args.config], "batch": B, "heads": H,
+                   "q_len": q_len, "num_shards": N, "layout": w.layout, "kv_dtype": w.kv_dtype,
+                   "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
                    "total_tokens_per_gpu": w.total_tokens, "kv_bytes_per_gpu": kv_bytes,
-                   "l2": "inputs larger than L2 (KV cache 3.4 GB per GPU vs 129 MB L2)",
+                   "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per GPU vs 129 MB)",
                    "parallelism": f"{world} GPU(s), independent batches; {N} logical shards each"},
         "steps_per_s": args.steps / elapsed,
         "pct_of_peak_hbm": value / world / peak,
@@ -314,6 +334,7 @@ def run_gpu(args, world, rank, local, dist):
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": traffic},
+        "partial_ms": partial_avg_ms,
         "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
@@ -338,6 +359,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5],
+                    help="workload: one of the five benchmark configurations (default 2)")
     ap.add_argument("--requests", type=int, default=0,
                     help="profiling only: keep the first K requests of the workload")
     args = ap.parse_args()

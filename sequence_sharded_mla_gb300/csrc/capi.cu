@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -112,7 +113,7 @@ const char* mla_status_string(mla_status st) {
 size_t mla_workspace_size(const mla_shape* shape, int num_shards, int shard_id) {
   if (!shape_ok(shape) || num_shards < 1 || num_shards > kMaxShards) return 0;
   if (shard_id != MLA_ALL_SHARDS && (shard_id < 0 || shard_id >= num_shards)) return 0;
-  int grid = device_sm_count();
+  int grid = std::min(device_sm_count(), 512);
   if (grid <= 0) return 0;
   return ws_layout(units_for(shape, num_shards, shard_id), grid).total;
 }
@@ -142,7 +143,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
       !aligned16(lse_partial) || !aligned16(block_table) || !aligned16(seq_lens))
     return MLA_ERR_INVALID;
   if (workspace == nullptr || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
-  const int grid = device_sm_count();
+  // one persistent CTA per SM (at most 512: the merge keeps per-piece
+  // weights of a unit in shared memory)
+  const int grid = std::min(device_sm_count(), 512);
   if (grid <= 0) return MLA_ERR_CUDA;
   const int U = units_for(shape, num_shards, shard_id);
   const WsLayout wl = ws_layout(U, grid);

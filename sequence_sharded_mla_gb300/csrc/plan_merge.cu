@@ -48,55 +48,69 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
   }
 }
 
-__global__ void __launch_bounds__(256) mla_merge_kernel(ProblemDesc pd, const WsHeader* hdr,
-                                                        const int* prefix, const float* ws_o,
-                                                        const float* ws_lse, float* out_partial,
-                                                        float* lse_partial) {
+// Block (u, y) handles query rows [4y, 4y + 4) of unit u, one warp per row:
+// the warp forms the row's piece weights once (in shared memory), then each
+// lane accumulates 16 of the 512 latent dims over the pieces.
+constexpr int kMergeRowsPerBlock = 4;
+constexpr int kMaxPieces = 512;    // pieces of one unit <= persistent CTAs
+
+__global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
+    ProblemDesc pd, const WsHeader* hdr, const int* prefix, const float* ws_o,
+    const float* ws_lse, float* out_partial, float* lse_partial) {
+  __shared__ float wts[kMergeRowsPerBlock][kMaxPieces];
   const int u = blockIdx.x;
   const Unit x = make_unit(pd, u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * kMergeRowsPerBlock + warp;
+  if (r >= x.rows) return;
   const int us = prefix[u], ue = prefix[u + 1];
   const size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
-  float* dst_o = out_partial + row0 * kDv;
-  float* dst_lse = lse_partial + row0;
-  const int nvec = x.rows * (kDv / 4);
+  float4* dst = reinterpret_cast<float4*>(out_partial + (row0 + r) * kDv);
   if (us == ue) {  // the shard holds no token of this request
-    for (int e = threadIdx.x; e < nvec; e += blockDim.x)
-      reinterpret_cast<float4*>(dst_o)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = threadIdx.x; r < x.rows; r += blockDim.x) dst_lse[r] = -CUDART_INF_F;
+    for (int v = lane; v < kDv / 4; v += 32) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) lse_partial[row0 + r] = -CUDART_INF_F;
     return;
   }
   const int per = hdr->per_cta;
   const int c0 = us / per, c1 = (ue - 1) / per;
   if (c0 == c1) return;  // written directly by the partial kernel
+  const int np = c1 - c0 + 1;
   auto slot_of = [&](int c) -> size_t {
     return (c == c0 && us > c0 * per) ? 2 * (size_t)c + 1 : 2 * (size_t)c;
   };
-  for (int e = threadIdx.x; e < nvec; e += blockDim.x) {
-    const int r = e / (kDv / 4), v = e % (kDv / 4);
-    float M = -CUDART_INF_F;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, ws_lse[slot_of(c) * kRows + r]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M > -CUDART_INF_F) {
-      for (int c = c0; c <= c1; ++c) {
-        const size_t sl = slot_of(c);
-        const float w = __expf(ws_lse[sl * kRows + r] - M);
-        const float4 o = reinterpret_cast<const float4*>(ws_o + (sl * kRows + r) * kDv)[v];
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
-        wsum += w;
-      }
-      const float inv = 1.0f / wsum;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-    }
-    reinterpret_cast<float4*>(dst_o + (size_t)r * kDv)[v] = acc;
-    if (v == 0) dst_lse[r] = (M > -CUDART_INF_F) ? M + __logf(wsum) : -CUDART_INF_F;
+  float M = -CUDART_INF_F;
+  for (int k = lane; k < np; k += 32) M = fmaxf(M, ws_lse[slot_of(c0 + k) * kRows + r]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float wsum = 0.f;
+  for (int k = lane; k < np; k += 32) {
+    const float w = M > -CUDART_INF_F ? __expf(ws_lse[slot_of(c0 + k) * kRows + r] - M) : 0.f;
+    wts[warp][k] = w;
+    wsum += w;
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+  __syncwarp();
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < np; ++k) {
+    const float w = wts[warp][k];
+    const float4* src = reinterpret_cast<const float4*>(ws_o + (slot_of(c0 + k) * kRows + r) * kDv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 o = src[lane + 32 * i];
+      acc[i].x += w * o.x;
+      acc[i].y += w * o.y;
+      acc[i].z += w * o.z;
+      acc[i].w += w * o.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    dst[lane + 32 * i] = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+  if (lane == 0) lse_partial[row0 + r] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
 }
 
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
@@ -108,8 +122,9 @@ cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int g
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
                          const float* ws_o, const float* ws_lse, float* out_partial,
                          float* lse_partial, int num_units, cudaStream_t stream) {
-  mla_merge_kernel<<<num_units, 256, 0, stream>>>(pd, hdr, prefix, ws_o, ws_lse, out_partial,
-                                                  lse_partial);
+  dim3 grid(num_units, kRows / kMergeRowsPerBlock);
+  mla_merge_kernel<<<grid, 32 * kMergeRowsPerBlock, 0, stream>>>(pd, hdr, prefix, ws_o, ws_lse,
+                                                                 out_partial, lse_partial);
   return cudaGetLastError();
 }
 
