@@ -174,7 +174,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // read as (64 dims, rows, chunk) so one box lands a 64-row group in the
   // [chunk][row][64] shared-memory layout; fallback: one box per chunk.
   CUtensorMap tm_q, tm_kv;
-  int q_one_box = 1, kv_page_box = 0;
+  int q_one_box = 1;
   {
     cuuint64_t dims[3] = {64, (cuuint64_t)pd.B * pd.R, (cuuint64_t)kChunks};
     cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, 128};
@@ -193,11 +193,12 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
         return MLA_ERR_CUDA;
     }
   }
-  // cache rows.  When every row of a page belongs to the tile (contiguous
-  // shards, or one interleaved shard) the view [page][row][9 chunks][64] read
-  // as (64 dims, row, chunk, page) lands a whole page in one box.  Otherwise
-  // [page][row / nv][row % nv][576]: a box takes the 64/nv rows of one page
-  // that one shard owns, one 64-wide chunk at a time (nv = N interleaved).
+  // cache rows, nv = N for interleaved shards (else 1): a tile's 64 slots
+  // are nv pages x 64/nv rows, slot a in 8-slot group a/8.  The bf16 view
+  // (64 dims, row in group, chunk, group, cache row) with strides
+  // (-, 1152 nv, 128, 9216 nv, 1152) starts at cache row page*64 + residue
+  // and lands the residue's 64/nv rows of a page, all 9 chunks, in one box in
+  // the group-major shared-memory layout.
   const int nv = pd.layout == kInterleaved ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   if (fp8) {
@@ -215,29 +216,16 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   } else {
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    bool done = false;
-    if (nv == 1) {
-      cuuint64_t dims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)kChunks, (cuuint64_t)kv->num_pages};
-      cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, 128, (cuuint64_t)kDqk * 2 * kPage};
-      cuuint32_t box[4] = {64, (cuuint32_t)kPage, (cuuint32_t)kChunks, 1};
-      done = encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
-                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-      kv_page_box = done ? 1 : 0;
-    }
-    if (!done) {
-      cuuint64_t dims[4] = {(cuuint64_t)kDqk, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
-                            (cuuint64_t)kv->num_pages};
-      cuuint64_t strides[3] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kDqk * 2 * nv,
-                               (cuuint64_t)kDqk * 2 * kPage};
-      cuuint32_t box[4] = {64, 1, (cuuint32_t)(kPage / nv), 1};
-      if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data), dims,
-                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return MLA_ERR_CUDA;
-    }
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
+                          (cuuint64_t)kv->num_pages * kPage};
+    cuuint64_t strides[4] = {(cuuint64_t)kDqk * 2 * nv, 128, (cuuint64_t)kDqk * 2 * 8 * nv,
+                             (cuuint64_t)kDqk * 2};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kPage / 8 / nv), 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -250,7 +238,6 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.ws_o = reinterpret_cast<float*>(ws + wl.ws_o);
   p.ws_lse = reinterpret_cast<float*>(ws + wl.ws_lse);
   p.kv_scale = kv->scale;
-  p.kv_page_box = kv_page_box;
   p.q_one_box = q_one_box;
   p.kv_fp8 = nullptr;
   p.timeout_ns = kTimeoutNs;

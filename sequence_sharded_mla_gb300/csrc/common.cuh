@@ -61,7 +61,6 @@ struct PartialParams {
   float* ws_o;         // [grid * 2, 64, 512] split pieces
   float* ws_lse;       // [grid * 2, 64]
   const float* kv_scale;  // fp8 caches: [num_pages * 64]
-  int kv_page_box;      // 1: tm_kv loads a whole page (all 9 chunks) per box
   int q_one_box;        // 1: tm_q loads all 9 chunks of a 64-row group per box
   const uint8_t* kv_fp8;  // fp8 caches: [num_pages, 64, 576] codes
   unsigned long long timeout_ns;

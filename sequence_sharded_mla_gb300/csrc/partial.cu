@@ -10,9 +10,16 @@
 // Data flow per persistent CTA (one per SM, 192 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
-//               (one TMA box per page and 64-wide chunk, 128-byte swizzle)
-//               into two stages; a stage is refilled as soon as its P.V is
-//               done.
+//               (one TMA box per page, 128-byte swizzle) into two stages; a
+//               stage is refilled as soon as its P.V is done.
+//
+// Stage layout ("group-major"): token slot a of a tile lies in 8-slot group
+// a/8 at byte (a/8)*9216 + c*1024 + (a%8)*128 for 64-wide chunk c, i.e. each
+// 8-row x 128-byte swizzle atom of a group's nine chunks is contiguous.  The
+// MMAs only need a uniform stride between 8-row groups (9216 bytes), and a
+// page's slots of one interleaved shard are whole groups, so one TMA box
+// brings every chunk of a page's slots: N boxes per tile for N interleaved
+// shards instead of 9N with a chunk-major layout.
 //   warps 1, 6  MMA issuers (two, on different SM sub-partitions: one issuing
 //               thread cannot keep the tensor pipe full with MMAs this small).
 //               Each issues half of S = Q K^T (M=64 rows, N=64 tokens; even /
@@ -81,7 +88,9 @@ struct Misc {
 
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTileBytes;
-constexpr int kSmemRope = 8 * kChunkBytes;          // rope chunk offset inside a stage (P after QK^T)
+constexpr int kGroupBytes = kChunks * 1024;          // 9216: one 8-slot group, all chunks
+constexpr int kGroupRope = 8 * 1024;                 // rope atom inside a group (P after QK^T)
+static_assert(kTileBytes == 8 * kGroupBytes, "tile = 8 groups");
 constexpr int kSmemMisc = 3 * kTileBytes;
 constexpr int kSmemBytes = kSmemMisc + 2048 + 1024;  // + misc + alignment slack
 static_assert(sizeof(Misc) <= 2048, "misc block");
@@ -212,7 +221,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // Lane k < nv issues the boxes of page k of the tile; lane 0 arms each
     // group barrier with the group's whole byte count first.
     const int nv = pd.layout == kInterleaved ? pd.num_shards : 1;  // page boxes per tile
-    const int box_bytes = (kTile / nv) * 128;
+    const int box_bytes = kTileBytes / nv;   // bf16: the whole groups of one page
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -267,13 +276,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             cp_async_4(smem_u32(&misc->scale[st][a]), src);
           }
           cp_async_mbar_arrive_noinc(full);
-        } else if (p.kv_page_box) {
-          if (lane == 0) tma_load_4d(sKV + st * kTileBytes, &tm_kv, full, 0, 0, 0, page);
         } else if (lane < nv) {
-          const uint32_t dst = sKV + st * kTileBytes + lane * box_bytes;
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_4d(dst + c * kChunkBytes, &tm_kv, full, c * 64, res, 0, page);
+          // cache row page*64 + res of the (row-in-group, chunk, group, row)
+          // view; a page of num_pages is out of range and fills zeros
+          tma_load_5d(sKV + st * kTileBytes + lane * box_bytes, &tm_kv, full, 0, 0, 0, 0,
+                      page * kPage + res);
         }
         __syncwarp();
         if (ok && j == t0) {
@@ -307,9 +314,12 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
     // descriptor bases; adding (byte offset >> 4) moves the start address
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
-    const uint64_t dkv0 = sw128_desc(sKV, 16, 1024);
-    const uint64_t dv0 = sw128_desc(sKV, kChunkBytes, 1024);
-    const uint64_t dp0 = sw128_desc(sKV + kSmemRope, 16, 1024);  // P of stage 0
+    // K (B of QK^T, K-major): 8-slot groups 9216 bytes apart; V^T (A of P.V,
+    // MN-major): 64-dim blocks 1024 bytes apart, 8-token groups 9216 apart;
+    // P (B of P.V, K-major): query-row groups in the groups' rope atoms
+    const uint64_t dkv0 = sw128_desc(sKV, 16, kGroupBytes);
+    const uint64_t dv0 = sw128_desc(sKV, 1024, kGroupBytes);
+    const uint64_t dp0 = sw128_desc(sKV + kGroupRope, 16, kGroupBytes);  // P of stage 0
     int gbase = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   const uint64_t a =
-                      dv0 + st_off + (uint32_t)((2 * blk * kChunkBytes + kk * 2048) >> 4);
+                      dv0 + st_off + (uint32_t)((2 * blk * 1024 + kk * 2 * kGroupBytes) >> 4);
                   const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
                   mma_bf16_ss(tmem + kColO + 64 * blk, a, bd, id_pv,
                               (np == 0 && kk == 0) ? 0u : 1u);
@@ -368,8 +378,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
               for (int c = mi; c < kChunks; c += kIssuers) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const uint32_t off = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
-                  mma_bf16_ss(d, dq0 + off, dkv0 + st_off + off, id_qk,
+                  const uint32_t offq = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
+                  const uint32_t offk = (uint32_t)((c * 1024 + 32 * k) >> 4);
+                  mma_bf16_ss(d, dq0 + offq, dkv0 + st_off + offk, id_qk,
                               (c != mi || k != 0) ? 1u : 0u);
                 }
               }
@@ -401,10 +412,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   } else if (kFp8 && warp >= 7) {
     // ------------------------------------------------------------ fp8 -> bf16
     // Thread t expands, for every 64-wide chunk c, 32 codes of tile row t/2
-    // (half t%2 of the chunk) into the swizzled bf16 plane c.  Planes 0..3
-    // lie below the codes; planes 4..8 overlap them, so their codes are read
-    // into registers first and written after a barrier over the converter
-    // warps.
+    // (half t%2 of the chunk) into the row's swizzled bf16 atom of chunk c.
+    // Rows 0..31 (groups 0..3) land below the codes and are expanded at once;
+    // rows 32..63 land on top of the codes of every row, so their threads
+    // hold all their codes in registers until the barrier over the converter
+    // warps says every code has been read.
     const int ct = threadIdx.x - 7 * 32;   // 0..127
     const int row = ct >> 1, hh = ct & 1;
     int gt = 0;
@@ -419,15 +431,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         if (any_fail) { ok = false; break; }
         uint8_t* stage = smem + kSmemKV + st * kTileBytes;
         const uint8_t* src = stage + kFp8Staging + row * kDqk + 32 * hh;
-        uint4 hi[5][2];
-#pragma unroll
-        for (int c = 4; c < kChunks; ++c) {
-          hi[c - 4][0] = *reinterpret_cast<const uint4*>(src + 64 * c);
-          hi[c - 4][1] = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
-        }
         auto put = [&](int c, uint4 a, uint4 b) {
           const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-          uint8_t* dst = stage + c * kChunkBytes + row * 128;
+          uint8_t* dst = stage + (row >> 3) * kGroupBytes + c * 1024 + (row & 7) * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {     // 16-byte output chunk 4*hh + q
             const uint2 lo2 = e4m3x4_to_bf16x4(w[2 * q]);
@@ -437,15 +443,25 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                 make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
           }
         };
+        if (row < kTile / 2) {   // warp-uniform: warps 7, 8
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 a = *reinterpret_cast<const uint4*>(src + 64 * c);
-          const uint4 b = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
-          put(c, a, b);
+          for (int c = 0; c < kChunks; ++c) {
+            const uint4 a = *reinterpret_cast<const uint4*>(src + 64 * c);
+            const uint4 b = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
+            put(c, a, b);
+          }
+          named_bar_sync(kBarConv, kConvThreads);
+        } else {                 // warps 9, 10
+          uint4 hi[kChunks][2];
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            hi[c][0] = *reinterpret_cast<const uint4*>(src + 64 * c);
+            hi[c][1] = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
+          }
+          named_bar_sync(kBarConv, kConvThreads);   // every row's codes have been read
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) put(c, hi[c][0], hi[c][1]);
         }
-        named_bar_sync(kBarConv, kConvThreads);   // all codes of planes 4..8 are in registers
-#pragma unroll
-        for (int c = 4; c < kChunks; ++c) put(c, hi[c - 4][0], hi[c - 4][1]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_kv_conv + 8 * st);
@@ -516,34 +532,41 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
               }
             }
           }
-          float mx = -CUDART_INF_F;
+          // tree reduction: independent partial maxima keep the chain short
+          float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-          for (int a = 0; a < 32; ++a) mx = fmaxf(mx, s[a]);
+          for (int a = 4; a < 32; a += 4) {
+            m4[0] = fmaxf(m4[0], s[a]);
+            m4[1] = fmaxf(m4[1], s[a + 1]);
+            m4[2] = fmaxf(m4[2], s[a + 2]);
+            m4[3] = fmaxf(m4[3], s[a + 3]);
+          }
+          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const float m_new = fmaxf(m_run, mx * pd.scale_log2);
           float alpha = 1.0f;
           if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
-            alpha = (m_run == -CUDART_INF_F) ? 0.0f : exp2f(m_run - m_new);
+            alpha = (m_run == -CUDART_INF_F) ? 0.0f : ex2_approx(m_run - m_new);
             l_run *= alpha;
             m_run = m_new;
             resc = owner && (j != t0);
           }
           if (owner && half == 0) misc->alpha[gt & 1][r] = alpha;
           const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-          float lsum = 0.0f;
+          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int a = 0; a < 16; ++a) {
-            const float p0 = exp2f(fmaf(s[2 * a], pd.scale_log2, -m_use));
-            const float p1 = exp2f(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
+            const float p0 = ex2_approx(fmaf(s[2 * a], pd.scale_log2, -m_use));
+            const float p1 = ex2_approx(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
             if constexpr (kFp8) {
               // P.V multiplies the codes; the token scale rides on P
               pk[a] = pack_bf16x2(p0 * sc[2 * a], p1 * sc[2 * a + 1]);
             } else {
               pk[a] = pack_bf16x2(p0, p1);
             }
-            lsum += p0 + p1;
+            ls4[a & 3] += p0 + p1;
           }
-          l_run += lsum;
+          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
         }
         // every softmax thread reaches the reduction, so a failed wait
         // anywhere in the group is seen by all of them at the same point;
@@ -575,7 +598,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           tmem_wait_st();
         }
         if (owner) {
-          uint8_t* prow = smem + kSmemKV + (gt & 1) * kTileBytes + kSmemRope + r * 128;
+          uint8_t* prow = smem + kSmemKV + (gt & 1) * kTileBytes + (r >> 3) * kGroupBytes +
+                          kGroupRope + (r & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int ch = 4 * half + c;   // 16-byte chunk of the 128-byte row
@@ -591,7 +615,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             int a = e >> 6, plane = (e >> 3) & 7, ch = e & 7;
             int t = slot_token(pd, x, j, a);
             if (!slot_valid(pd, x, t))
-              *reinterpret_cast<uint4*>(st + plane * kChunkBytes + a * 128 + ch * 16) =
+              *reinterpret_cast<uint4*>(st + (a >> 3) * kGroupBytes + plane * 1024 +
+                                        (a & 7) * 128 + ch * 16) =
                   make_uint4(0, 0, 0, 0);
           }
         }

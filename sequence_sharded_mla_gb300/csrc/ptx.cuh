@@ -158,6 +158,14 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22; inputs
+// below -126 flush to 0, which is what masked logits need).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Four OCP e4m3 codes -> four bf16 values (exact), as two bf16x2 words.
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t codes) {
   uint32_t h01, h23;
