@@ -45,17 +45,22 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def traffic_for(kernel_src):
-    """ncu DRAM bytes per launch recorded for this exact kernel source, or None."""
+def kernel_sha(kernel_src):
+    return hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_src, workload):
+    """ncu DRAM bytes (read + write) per launch of the partial kernel on this
+    workload, as recorded in profiles/traffic.json for this exact kernel
+    source; None when no record matches (the kernel changed since)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
+        ent = rec[kernel_sha(kernel_src)][workload]
+        return float(ent["dram_bytes_per_launch"])
     except Exception:
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    ent = rec.get(sha)
-    return None if ent is None else ent
 
 
 class ClockSampler:
@@ -238,14 +243,22 @@ def run_gpu(args, world, rank, local, dist):
     h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
     h_lse = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
 
+    # per timed step: events around the whole partial call (plan, partial
+    # kernel, merge) and, recorded by the library itself, around the partial
+    # kernel alone
     ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    ev_k = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for ev in ev_p + ev_k:
+        ev.record(stream)
 
     def step(i=None):
         if i is not None:
             ev_p[2 * i].record(stream)
+            mla.mla_set_profile_events(ev_k[2 * i], ev_k[2 * i + 1])
         mla.mla_decode_partial(d_q, d_kv, d_bt, d_sl, N, w.layout, kv_scale=d_sc, causal=w.causal,
                                out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
         if i is not None:
+            mla.mla_set_profile_events(None, None)
             ev_p[2 * i + 1].record(stream)
         mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
 
@@ -271,6 +284,7 @@ def run_gpu(args, world, rank, local, dist):
     clk = clocks.stop()
     elapsed = t_start.elapsed_time(t_end) / 1e3
     partial_ms = [ev_p[2 * i].elapsed_time(ev_p[2 * i + 1]) for i in range(args.steps)]
+    kernel_ms = [ev_k[2 * i].elapsed_time(ev_k[2 * i + 1]) for i in range(args.steps)]
     status = mla.mla_get_device_error(ws, stream)
     if status != 0:
         raise RuntimeError(f"device error status {status}")
@@ -303,21 +317,22 @@ def run_gpu(args, world, rank, local, dist):
     barrier()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
 
-    t = torch.tensor([elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms)],
-                     dtype=torch.float64, device=dev)
+    t = torch.tensor([elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
+                      statistics.mean(kernel_ms)], dtype=torch.float64, device=dev)
     kvt = torch.tensor([float(kv_bytes)], dtype=torch.float64, device=dev)
     if dist is not None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.all_reduce(kvt, op=dist.ReduceOp.SUM)
-    elapsed, e2e_per_step, partial_avg_ms = t.tolist()
+    elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms = t.tolist()
     total_kv = kvt.item()
     if rank != 0:
         return
     peak, peak_kind = load_peaks()
     value = total_kv * args.steps / elapsed / 1e9
     ms_per_step = elapsed / args.steps * 1e3
-    achieved = kv_bytes / (partial_avg_ms / 1e3) / 1e9
-    traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc", "partial.cu"))
+    achieved = kv_bytes / (kernel_avg_ms / 1e3) / 1e9
+    traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc", "partial.cu"),
+                          mi.CONFIG_NAMES[args.config])
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -330,11 +345,13 @@ def run_gpu(args, world, rank, local, dist):
                    "parallelism": f"{world} GPU(s), independent batches; {N} logical shards each"},
         "steps_per_s": args.steps / elapsed,
         "pct_of_peak_hbm": value / world / peak,
-        "roofline": {"kernel": "mla_partial_bf16_kernel (+plan, merge)", "bound": "hbm",
+        "roofline": {"kernel": "mla_partial_kernel<%s>" % ("true" if w.kv_dtype == "fp8" else "false"),
+                     "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": traffic},
-        "partial_ms": partial_avg_ms,
+        "partial_kernel_ms": kernel_avg_ms,
+        "partial_call_ms": partial_avg_ms,
         "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},

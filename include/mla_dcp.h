@@ -182,6 +182,18 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
  */
 mla_status mla_get_device_error(void* workspace, void* stream);
 
+/*
+ * Profiling aid (not part of the method): while set, every later
+ * mla_decode_partial call (both entry points, any thread) records
+ * `before_partial` and `after_partial` -- two cudaEvent_t handles passed as
+ * void*, owned by the caller -- on its stream immediately before and after
+ * the launch of its partial-attention kernel, so that kernel's device time
+ * can be read without the planning and merge kernels around it.  Pass two
+ * NULLs to stop.  Exactly one NULL is MLA_ERR_INVALID.  The caller keeps the
+ * events alive while they are set; the setting is process-wide.
+ */
+mla_status mla_set_profile_events(void* before_partial, void* after_partial);
+
 /* Static description of a status code. */
 const char* mla_status_string(mla_status status);
 

@@ -44,7 +44,8 @@ class mla_kv_pages(ctypes.Structure):
 
 _LIB = None
 EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
-           "mla_workspace_size", "mla_get_device_error", "mla_status_string", "mla_version")
+           "mla_workspace_size", "mla_get_device_error", "mla_set_profile_events",
+           "mla_status_string", "mla_version")
 
 
 def lib():
@@ -68,6 +69,8 @@ def lib():
         L.mla_workspace_size.restype = sz
         L.mla_get_device_error.argtypes = [vp, vp]
         L.mla_get_device_error.restype = i32
+        L.mla_set_profile_events.argtypes = [vp, vp]
+        L.mla_set_profile_events.restype = i32
         L.mla_status_string.argtypes = [i32]
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_version.argtypes = []
@@ -226,6 +229,24 @@ def mla_shard_combine(partials, lses, w_uv=None, out=None, lse_out=None, stream=
 def mla_get_device_error(workspace, stream=None) -> int:
     """Sync the stream, read and clear the device error word; returns a status code."""
     return int(lib().mla_get_device_error(_ptr(workspace), _stream_ptr(stream)))
+
+
+def mla_set_profile_events(before=None, after=None) -> None:
+    """Record two torch.cuda.Events around the partial-attention kernel of
+    every later mla_decode_partial call (None, None stops).  The events are
+    recorded once here on the current stream so that their CUDA handles exist."""
+    if (before is None) != (after is None):
+        raise ValueError("give both events or neither")
+    if before is None:
+        st = lib().mla_set_profile_events(None, None)
+    else:
+        for ev in (before, after):
+            if ev.cuda_event == 0:
+                ev.record()
+        st = lib().mla_set_profile_events(ctypes.c_void_p(before.cuda_event),
+                                          ctypes.c_void_p(after.cuda_event))
+    if st != 0:
+        raise MLAError(st, "mla_set_profile_events")
 
 
 def mla_status_string(status: int) -> str:

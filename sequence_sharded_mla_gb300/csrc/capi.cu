@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -90,6 +91,10 @@ int units_for(const mla_shape* s, int num_shards, int shard_id) {
   int G = ceil_div(s->q_len * s->num_heads, kRows);
   return s->batch * n_out * G;
 }
+
+// Profiling events (cudaEvent_t) recorded around the partial-attention
+// kernel of every mla_decode_partial call while set.
+std::atomic<void*> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 }  // namespace
 
@@ -244,8 +249,14 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, st) != cudaSuccess) return MLA_ERR_CUDA;
+  void* ev0 = g_ev_before.load();
+  void* ev1 = g_ev_after.load();
+  if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
+    return MLA_ERR_CUDA;
   const cudaError_t le = fp8 ? launch_partial_fp8(tm_q, tm_kv, p, grid, st)
                              : launch_partial_bf16(tm_q, tm_kv, p, grid, st);
+  if (ev1 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev1), st) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_merge(pd, p.hdr, p.prefix, p.ws_o, p.ws_lse, out_partial, lse_partial, U, st) !=
       cudaSuccess)
@@ -270,6 +281,13 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
                            shape->num_heads, static_cast<const uint16_t*>(w_uv),
                            static_cast<uint16_t*>(out), lse_out, st);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status mla_set_profile_events(void* before_partial, void* after_partial) {
+  if ((before_partial == nullptr) != (after_partial == nullptr)) return MLA_ERR_INVALID;
+  g_ev_before.store(before_partial);
+  g_ev_after.store(after_partial);
+  return MLA_OK;
 }
 
 mla_status mla_get_device_error(void* workspace, void* stream) {

@@ -66,3 +66,11 @@ def test_noalloc_refuses_shapes_beyond_its_scratch_before_any_cuda_call():
     assert st == -2
     assert L.mla_decode_partial_noalloc(None, ctypes.byref(kv), None, 1, None, None, -1, 8, 0,
                                         None, None, None) == -1
+
+
+def test_profile_events_take_both_or_neither():
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    assert L.mla_set_profile_events(None, ctypes.c_void_p(64)) == -1
+    assert L.mla_set_profile_events(ctypes.c_void_p(64), None) == -1
+    assert L.mla_set_profile_events(None, None) == 0
