@@ -94,37 +94,83 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sms, maxes, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sms.append(float(parts[1]))
-                maxes.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+        with open(self.path) as f:
+            res = parse_clock_samples(f)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sms) if sms else None,
-                "sm_max_mhz": max(maxes) if maxes else None,
-                "reasons": sorted(reasons), "samples": len(sms)}
+        return res
 
 
-def dist_setup(args):
+def parse_clock_samples(lines):
+    """Summarise nvidia-smi rows of ClockSampler.FIELDS (csv, no header, no
+    units): median SM clock, max SM clock, and every throttle reason seen
+    active in any sample."""
+    sms, maxes, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sms.append(float(parts[1]))
+            maxes.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sms) if sms else None,
+            "sm_max_mhz": max(maxes) if maxes else None,
+            "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_setup(args, backend="nccl"):
+    """World, rank and local rank from the launcher's environment; joins the
+    process group when there is more than one rank.  The reference arm runs
+    on rank 0 alone and joins nothing."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     pg = None
-    if world > 1:
+    if world > 1 and args.impl != "reference":
         import torch.distributed as dist
-        backend = "gloo" if args.impl == "reference" else "nccl"
         dist.init_process_group(backend=backend)
         pg = dist
     return world, rank, local, pg
+
+
+def rank_workload_params(config, rank, requests=0):
+    """Arguments of the batch rank ``rank`` decodes: rank 0 the configuration
+    itself, every other rank an independently seeded batch of the same shape
+    (weak scaling: ranks share nothing on the data path).  ``requests`` > 0
+    keeps the first K requests (profiling runs only)."""
+    import mla_inputs as mi
+    p = mi.config_params(config)
+    if rank > 0:
+        p["seed"] += 1000 * rank
+        if config == 2:
+            p["seq_lens"] = mi.agentic_lengths(p["seed"], p["batch"])
+    if requests:
+        p["name"] += f"-first{requests}"
+        p["batch"] = requests
+        p["seq_lens"] = list(p["seq_lens"])[:requests]
+    return p
+
+
+def rank_workload(config, rank, requests=0, pinned=True):
+    import mla_inputs as mi
+    return mi.build_workload(pinned=pinned, **rank_workload_params(config, rank, requests))
+
+
+def reduce_over_ranks(dist, times, kv_bytes, device):
+    """Max of the per-rank times (the slowest rank ends the job) and sum of
+    the per-rank KV bytes (the whole job's work)."""
+    import torch
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    b = torch.tensor([float(kv_bytes)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return t.tolist(), b.item()
 
 
 def cpu_sample(w, budget_s, oracle):
@@ -158,10 +204,7 @@ def run_reference(args, world, rank):
     import oracle
     w = mi.config_workload(args.config)
     threads = oracle.num_threads()
-    per = 1152
     # one step = the oracle over a bounded sample of the workload
-    import numpy as np
-    order = np.argsort(w.seq_lens)
     budget = args.ref_step_seconds
     results = []
     for step in range(args.warmup + args.steps):
@@ -197,23 +240,7 @@ def run_gpu(args, world, rank, local, dist):
     dev = torch.device("cuda", local)
     mla.lib()
     # each rank decodes its own batch of the same shape (independent requests)
-    w = mi.config_workload(args.config, pinned=True)
-    if args.requests:
-        # a reduced copy of the workload (first K requests) for profiling runs
-        w = mi.build_workload(w.name + f"-first{args.requests}", args.requests, w.q_len,
-                              w.num_heads, w.seq_lens[:args.requests], w.num_shards, w.layout,
-                              w.kv_dtype, w.causal, seed=w.seed, pinned=True,
-                              kv_sigma=1.0 if w.kv_dtype == "fp8" else 0.5,
-                              with_w_uv=w.w_uv is not None)
-    if rank > 0:
-        # every rank decodes its own, independently seeded batch of the same shape
-        w2 = mi.config_workload(args.config, pinned=False)
-        seed = w2.seed + 1000 * rank
-        lens = mi.agentic_lengths(seed, w2.batch) if args.config == 2 else w2.seq_lens
-        w = mi.build_workload(w.name, w.batch, w.q_len, w.num_heads, lens, w.num_shards,
-                              w.layout, w.kv_dtype, w.causal, seed=seed, pinned=True,
-                              kv_sigma=1.0 if w.kv_dtype == "fp8" else 0.5,
-                              with_w_uv=w.w_uv is not None)
+    w = rank_workload(args.config, rank, args.requests)
     B, H, q_len, N = w.batch, w.num_heads, w.q_len, w.num_shards
     kv_bytes = w.kv_bytes()
 
@@ -317,14 +344,9 @@ def run_gpu(args, world, rank, local, dist):
     barrier()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
 
-    t = torch.tensor([elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
-                      statistics.mean(kernel_ms)], dtype=torch.float64, device=dev)
-    kvt = torch.tensor([float(kv_bytes)], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(kvt, op=dist.ReduceOp.SUM)
-    elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms = t.tolist()
-    total_kv = kvt.item()
+    (elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms), total_kv = reduce_over_ranks(
+        dist, [elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
+               statistics.mean(kernel_ms)], kv_bytes, dev)
     if rank != 0:
         return
     peak, peak_kind = load_peaks()

@@ -294,30 +294,37 @@ CONFIG_NAMES = {
 }
 
 
+def config_params(cfg: int):
+    """Arguments of build_workload for the five benchmark configurations."""
+    if cfg == 1:
+        return dict(name=CONFIG_NAMES[1], batch=1, q_len=1, num_heads=16, seq_lens=[1024],
+                    num_shards=2, layout="interleaved", kv_dtype="bf16", causal=False, seed=1,
+                    q_sigma=0.5, kv_sigma=0.5)
+    if cfg == 2:
+        return dict(name=CONFIG_NAMES[2], batch=32, q_len=1, num_heads=64,
+                    seq_lens=agentic_lengths(2, 32), num_shards=4, layout="interleaved",
+                    kv_dtype="bf16", causal=False, seed=2)
+    if cfg == 3:
+        return dict(name=CONFIG_NAMES[3], batch=64, q_len=1, num_heads=64,
+                    seq_lens=uniform_lengths(3, 64, 16384, 98304), num_shards=1,
+                    layout="interleaved", kv_dtype="bf16", causal=False, seed=3)
+    if cfg == 4:
+        return dict(name=CONFIG_NAMES[4], batch=16, q_len=9, num_heads=64, seq_lens=[8000] * 16,
+                    num_shards=2, layout="interleaved", kv_dtype="bf16", causal=True, seed=4)
+    if cfg == 5:
+        return dict(name=CONFIG_NAMES[5], batch=4, q_len=1, num_heads=64,
+                    seq_lens=[1048576, 262144, 131072, 65536], num_shards=8,
+                    layout="interleaved", kv_dtype="fp8", causal=False, seed=5,
+                    q_sigma=0.5, kv_sigma=1.0, with_w_uv=True, w_sigma=0.02)
+    raise ValueError(cfg)
+
+
 def config_workload(cfg: int, num_shards=None, layout=None, pinned=False, **kw):
     """The five benchmark configurations, generated from their seeds."""
-    if cfg == 1:
-        return build_workload(CONFIG_NAMES[1], 1, 1, 16, [1024], num_shards or 2,
-                              layout or "interleaved", "bf16", False, seed=1,
-                              q_sigma=0.5, kv_sigma=0.5, pinned=pinned, **kw)
-    if cfg == 2:
-        lens = agentic_lengths(2, 32)
-        return build_workload(CONFIG_NAMES[2], 32, 1, 64, lens, num_shards or 4,
-                              layout or "interleaved", "bf16", False, seed=2,
-                              pinned=pinned, **kw)
-    if cfg == 3:
-        lens = uniform_lengths(3, 64, 16384, 98304)
-        return build_workload(CONFIG_NAMES[3], 64, 1, 64, lens, num_shards or 1,
-                              layout or "interleaved", "bf16", False, seed=3,
-                              pinned=pinned, **kw)
-    if cfg == 4:
-        return build_workload(CONFIG_NAMES[4], 16, 9, 64, [8000] * 16, num_shards or 2,
-                              layout or "interleaved", "bf16", True, seed=4,
-                              pinned=pinned, **kw)
-    if cfg == 5:
-        return build_workload(CONFIG_NAMES[5], 4, 1, 64,
-                              [1048576, 262144, 131072, 65536], num_shards or 8,
-                              layout or "interleaved", "fp8", False, seed=5,
-                              q_sigma=0.5, kv_sigma=1.0, with_w_uv=True, w_sigma=0.02,
-                              pinned=pinned, **kw)
-    raise ValueError(cfg)
+    p = config_params(cfg)
+    if num_shards:
+        p["num_shards"] = num_shards
+    if layout:
+        p["layout"] = layout
+    p.update(kw)
+    return build_workload(pinned=pinned, **p)
