@@ -19,7 +19,7 @@ cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k
 cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                const PartialParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
-                        int min_tiles, cudaStream_t stream);
+                        int min_tiles, int unit_cost, cudaStream_t stream);
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
                          const float* ws_o, const float* ws_lse, float* out_partial,
                          float* lse_partial, int num_units, cudaStream_t stream);
@@ -37,6 +37,9 @@ namespace {
 constexpr int kVersion = 100;  // 0.1.0
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // device waits give up after 2 s
 constexpr int kMinTilesPerCta = 4;
+// Work positions charged to a unit for its fixed costs (query load, pipeline
+// refill, the epilogue's 128 KB of output): about two tiles' time.
+constexpr int kUnitCost = 2;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -248,7 +251,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.timeout_ns = kTimeoutNs;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, kUnitCost, st) != cudaSuccess) return MLA_ERR_CUDA;
   void* ev0 = g_ev_before.load();
   void* ev1 = g_ev_after.load();
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)

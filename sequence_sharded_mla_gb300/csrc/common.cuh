@@ -28,12 +28,20 @@ enum Layout : int { kInterleaved = 0, kContiguous = 1 };
 // Workspace header (first 256 bytes of the caller's workspace).
 struct WsHeader {
   unsigned err;        // OR of error bits
-  int total_tiles;     // W: tiles over all units
-  int per_cta;         // tiles per persistent CTA
+  int total_cost;      // C: work positions over all units
+  int per_cta;         // work positions per persistent CTA
   int grid;            // persistent CTAs
   int num_units;       // U
-  int pad[59];
+  int unit_cost;       // overhead positions charged to every unit that has tiles
+  int pad[58];
 };
+
+// Work positions: unit u owns [prefix[u], prefix[u+1]) -- unit_cost positions
+// standing for its fixed costs (query load, epilogue), then one per tile --
+// or nothing when it has no tile.  First position of unit u's tiles:
+__host__ __device__ inline int unit_tile_start(const int* prefix, int u, int unit_cost) {
+  return prefix[u + 1] > prefix[u] ? prefix[u] + unit_cost : prefix[u];
+}
 static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct ProblemDesc {

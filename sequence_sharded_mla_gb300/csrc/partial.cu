@@ -94,6 +94,7 @@ static_assert(kTileBytes == 8 * kGroupBytes, "tile = 8 groups");
 constexpr int kSmemMisc = 3 * kTileBytes;
 constexpr int kSmemBytes = kSmemMisc + 2048 + 1024;  // + misc + alignment slack
 static_assert(sizeof(Misc) <= 2048, "misc block");
+static_assert(offsetof(Misc, inv_l) % 16 == 0, "inv_l is read as float4");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM columns: per stage two partial S accumulators (M=64 layout, 64
@@ -103,13 +104,16 @@ constexpr uint32_t kColS0 = 0, kColO = 256;
 
 struct PieceIter {
   const int* prefix;
-  int U, lo, hi, pos, u;
-  __device__ void init(const int* pfx, int num_units, int lo_, int hi_) {
+  int U, lo, hi, pos, u, uc;
+  bool first;
+  __device__ void init(const int* pfx, int num_units, int lo_, int hi_, int unit_cost) {
     prefix = pfx;
     U = num_units;
     lo = lo_;
     hi = hi_;
     pos = lo_;
+    uc = unit_cost;
+    first = true;
     // last unit with prefix[u] <= lo
     int a = 0, b = num_units - 1;
     while (a < b) {
@@ -119,19 +123,29 @@ struct PieceIter {
     }
     u = a;
   }
-  // Next piece: unit, tile range [t0, t1), whether it is the whole unit, slot.
+  // Next piece: unit, tile range [t0, t1), whether it is the whole unit, and
+  // the workspace slot of a partial piece (0: the CTA's first piece, 1: its
+  // last).  Positions of a unit's fixed-cost part hold no tile.
   __device__ bool next(int& unit, int& t0, int& t1, bool& whole, int& slot) {
-    if (pos >= hi) return false;
-    while (u < U && prefix[u + 1] <= pos) ++u;
-    int us = prefix[u], ue = prefix[u + 1];
-    unit = u;
-    t0 = pos - us;
-    t1 = min(hi, ue) - us;
-    whole = (us >= lo) && (ue <= hi);
-    slot = (pos == lo) ? 0 : 1;
-    pos = min(hi, ue);
-    ++u;
-    return true;
+    while (pos < hi) {
+      while (u < U && prefix[u + 1] <= pos) ++u;
+      if (u >= U) return false;
+      const int ue = prefix[u + 1];
+      const int ts = unit_tile_start(prefix, u, uc);
+      const int a = max(pos, ts), b = min(hi, ue);
+      const int cur = u;
+      pos = b;
+      ++u;
+      if (a >= b) continue;
+      unit = cur;
+      t0 = a - ts;
+      t1 = b - ts;
+      whole = (a == ts) && (b == ue);
+      slot = first ? 0 : 1;
+      first = false;
+      return true;
+    }
+    return false;
   }
 };
 
@@ -152,13 +166,15 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, formed by pointer arithmetic on the shared array
+  // (not through an integer) so that the compiler keeps every access through
+  // it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc* misc = reinterpret_cast<Misc*>(smem + kSmemMisc);
   const ProblemDesc& pd = p.pd;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int W = p.hdr->total_tiles, per = p.hdr->per_cta;
+  const int W = p.hdr->total_cost, per = p.hdr->per_cta;
   const int lo = blockIdx.x * per;
   if (lo >= W) return;
   const int hi = min(lo + per, W);
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   const uint64_t tmo = p.timeout_ns;
 
   PieceIter it;
-  it.init(p.prefix, U, lo, hi);
+  it.init(p.prefix, U, lo, hi, p.hdr->unit_cost);
   int armed_kv[2] = {-1, -1}, armed_q = -1;  // producer: last armed phase per barrier
   int unit, t0, t1, slot;
   bool whole;
@@ -650,19 +666,37 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         dst_lse[r] = lse;
       }
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-#pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kColO + 64 * blk + 32 * h2, v);
-          tmem_wait_ld();
-          const int dim = 128 * blk + 32 * quad + lane;
+      // O^T block k/2, rows 32*(k%2).. of this thread's latent dim, two TMEM
+      // loads in flight: the stores of one overlap the load of the next
+      {
+        const uint32_t o_base = tmem + lane_off + kColO;
+        auto store32 = [&](int k, const uint32_t (&v)[32]) {
+          const int dim = 128 * (k >> 1) + 32 * quad + lane;
+          float il[32];
+          const float4* il4 = reinterpret_cast<const float4*>(misc->inv_l + 32 * (k & 1));
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = il4[c4];
+            il[4 * c4] = t.x;
+            il[4 * c4 + 1] = t.y;
+            il[4 * c4 + 2] = t.z;
+            il[4 * c4 + 3] = t.w;
+          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int row = 32 * h2 + c;
-            if (row < x.rows) dst_o[(size_t)row * kDv + dim] = __uint_as_float(v[c]) * misc->inv_l[row];
+            const int row = 32 * (k & 1) + c;
+            if (row < x.rows) dst_o[(size_t)row * kDv + dim] = __uint_as_float(v[c]) * il[c];
           }
+        };
+        uint32_t va[32], vb[32];
+        tmem_ld32(o_base, va);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          tmem_ld32(o_base + 32 * (k + 1), vb);
+          tmem_wait_ld();
+          store32(k, va);
+          if (k + 2 < 8) tmem_ld32(o_base + 32 * (k + 2), va);
+          store32(k + 1, vb);
         }
       }
       tc_fence_before();

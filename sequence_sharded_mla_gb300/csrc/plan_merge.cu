@@ -1,8 +1,11 @@
 // Work planning and split merging for the partial kernel.
 //
 // mla_plan_kernel      counts the 64-token tiles of every work unit
-//                      (request, shard, 64-row query group), forms their
-//                      exclusive prefix and picks the tiles per persistent CTA.
+//                      (request, shard, 64-row query group), charges every
+//                      unit with tiles unit_cost extra positions for its fixed
+//                      costs, forms the exclusive prefix of these work
+//                      positions and splits them evenly over the persistent
+//                      CTAs (a CTA with many short units gets fewer tiles).
 // mla_merge_kernel     writes every unit the partial kernel did not write
 //                      itself: units with no tokens (o = 0, lse = -inf) and
 //                      units split across CTAs, whose pieces it merges by
@@ -15,14 +18,19 @@
 namespace mla {
 
 __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader* hdr, int* prefix,
-                                                        int grid, int min_tiles) {
+                                                        int grid, int min_tiles,
+                                                        int unit_cost) {
   __shared__ int part[1024];
   const int U = pd.B * pd.n_out * pd.G;
   const int tid = threadIdx.x;
   const int per_thread = ceil_div(U, 1024);
   const int u0 = tid * per_thread, u1 = min(U, u0 + per_thread);
   int sum = 0;
-  for (int u = u0; u < u1; ++u) sum += make_unit(pd, u).tiles;
+  auto cost = [&](int u) {
+    const int t = make_unit(pd, u).tiles;
+    return t > 0 ? t + unit_cost : 0;
+  };
+  for (int u = u0; u < u1; ++u) sum += cost(u);
   part[tid] = sum;
   __syncthreads();
   // inclusive Hillis-Steele scan of the 1024 partial sums
@@ -35,16 +43,17 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
   int run = part[tid] - sum;  // exclusive
   for (int u = u0; u < u1; ++u) {
     prefix[u] = run;
-    run += make_unit(pd, u).tiles;
+    run += cost(u);
   }
   if (tid == 1023) {
     const int W = part[1023];
     prefix[U] = W;
     hdr->err = 0;
-    hdr->total_tiles = W;
+    hdr->total_cost = W;
     hdr->per_cta = max(min_tiles, ceil_div(W, grid));
     hdr->grid = grid;
     hdr->num_units = U;
+    hdr->unit_cost = unit_cost;
   }
 }
 
@@ -63,7 +72,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kMergeRowsPerBlock + warp;
   if (r >= x.rows) return;
-  const int us = prefix[u], ue = prefix[u + 1];
+  const int ps = prefix[u], ue = prefix[u + 1];
+  const int us = unit_tile_start(prefix, u, hdr->unit_cost);
   const size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
   float4* dst = reinterpret_cast<float4*>(out_partial + (row0 + r) * kDv);
   if (us == ue) {  // the shard holds no token of this request
@@ -75,8 +85,11 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   const int c0 = us / per, c1 = (ue - 1) / per;
   if (c0 == c1) return;  // written directly by the partial kernel
   const int np = c1 - c0 + 1;
+  // a CTA writes its first piece to slot 0 and its last to slot 1; the first
+  // CTA of the unit had an earlier piece iff its range starts before the
+  // unit's positions (the position before them is another unit's tile)
   auto slot_of = [&](int c) -> size_t {
-    return (c == c0 && us > c0 * per) ? 2 * (size_t)c + 1 : 2 * (size_t)c;
+    return (c == c0 && c0 * per < ps) ? 2 * (size_t)c + 1 : 2 * (size_t)c;
   };
   float M = -CUDART_INF_F;
   for (int k = lane; k < np; k += 32) M = fmaxf(M, ws_lse[slot_of(c0 + k) * kRows + r]);
@@ -114,8 +127,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
 }
 
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
-                        int min_tiles, cudaStream_t stream) {
-  mla_plan_kernel<<<1, 1024, 0, stream>>>(pd, hdr, prefix, grid, min_tiles);
+                        int min_tiles, int unit_cost, cudaStream_t stream) {
+  mla_plan_kernel<<<1, 1024, 0, stream>>>(pd, hdr, prefix, grid, min_tiles, unit_cost);
   return cudaGetLastError();
 }
 
