@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
       int nq = 0, np = 0;
       uint64_t t_idle = 0;
+      uint32_t idle_iter = 0;
       while (ok && np < n) {
         bool did = false;
         // P.V of the oldest tile whose probabilities are ready
@@ -410,15 +411,15 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         }
         if (did) {
           t_idle = 0;
+          idle_iter = 0;
         } else {
           // nothing ready: park briefly on the event expected next
-          if (np < nq) mbar_try_wait_hint(b_p_full + 8 * ((gbase + np) & 1), ((gbase + np) >> 1) & 1, 100);
-          else if (nq < n)
-            mbar_try_wait_hint(b_kv_ready + 8 * ((gbase + nq) & 1), ((gbase + nq) >> 1) & 1, 100);
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (now - t_idle > tmo || *abort_flag) ok = false;
-          ok = __all_sync(0xffffffffu, ok);
+          if ((++idle_iter & 63u) == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t_idle == 0) t_idle = now;
+            if (now - t_idle > tmo || *abort_flag) ok = false;
+            ok = __all_sync(0xffffffffu, ok);
+          }
         }
       }
       gbase += n;
