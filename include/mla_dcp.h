@@ -54,7 +54,8 @@ typedef enum mla_status {
   MLA_ERR_CUDA = -3,          /* a CUDA runtime or driver call failed */
   MLA_ERR_TIMEOUT = -4,       /* a device-side wait gave up (from mla_get_device_error) */
   MLA_ERR_DEVICE_BOUNDS = -5, /* a block-table entry was outside [0, num_pages) */
-  MLA_ERR_WORKSPACE = -6      /* workspace missing or smaller than mla_workspace_size() */
+  MLA_ERR_WORKSPACE = -6,     /* workspace missing or smaller than mla_workspace_size() */
+  MLA_ERR_RANGE = -7          /* fp8 cache: a query value beyond the fp16 range (|q| >= 65520) */
 } mla_status;
 
 /* Which token positions of a request belong to shard s of N
@@ -67,7 +68,10 @@ typedef enum mla_layout { MLA_LAYOUT_INTERLEAVED = 0, MLA_LAYOUT_CONTIGUOUS = 1 
 
 typedef enum mla_kv_dtype { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 
-/* Decode-step shape.  num_heads must be a multiple of 16.  With causal != 0
+/* Decode-step shape.  num_heads must be a multiple of 16.  With an fp8
+ * cache the query is rounded to fp16 for the tensor cores: exact for
+ * magnitudes in [2^-17, 65504]; a finite |q| >= 65520 is reported as
+ * MLA_ERR_RANGE by mla_get_device_error.  With causal != 0
  * (a speculative verify step of q_len = 1 + drafts tokens whose KV is the
  * last q_len entries of the cache), query i sees tokens t <= L - q_len + i. */
 typedef struct mla_shape {
@@ -177,8 +181,8 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
 /*
  * Synchronises `stream`, reads and clears the device error word kept in
  * `workspace` by the last mla_decode_partial on it.  Returns MLA_OK,
- * MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT (timeout wins if both) or
- * MLA_ERR_CUDA.
+ * MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_RANGE (in that order of
+ * precedence when several occurred) or MLA_ERR_CUDA.
  */
 mla_status mla_get_device_error(void* workspace, void* stream);
 

@@ -23,7 +23,8 @@ LAYOUTS = {"interleaved": 0, "contiguous": 1}
 KV_BF16, KV_FP8 = 0, 1
 
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_CUDA",
-          -4: "MLA_ERR_TIMEOUT", -5: "MLA_ERR_DEVICE_BOUNDS", -6: "MLA_ERR_WORKSPACE"}
+          -4: "MLA_ERR_TIMEOUT", -5: "MLA_ERR_DEVICE_BOUNDS", -6: "MLA_ERR_WORKSPACE",
+          -7: "MLA_ERR_RANGE"}
 
 
 class MLAError(RuntimeError):

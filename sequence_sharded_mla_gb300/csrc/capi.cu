@@ -114,6 +114,7 @@ const char* mla_status_string(mla_status st) {
     case MLA_ERR_TIMEOUT: return "device wait timed out";
     case MLA_ERR_DEVICE_BOUNDS: return "block-table entry out of range";
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_RANGE: return "query value beyond the fp16 range (fp8 cache)";
   }
   return "unknown status";
 }
@@ -307,6 +308,7 @@ mla_status mla_get_device_error(void* workspace, void* stream) {
   }
   if (err & kErrTimeout) return MLA_ERR_TIMEOUT;
   if (err & kErrBadPage) return MLA_ERR_DEVICE_BOUNDS;
+  if (err & kErrQRange) return MLA_ERR_RANGE;
   return MLA_OK;
 }
 

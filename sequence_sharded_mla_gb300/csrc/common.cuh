@@ -22,6 +22,7 @@ constexpr int kMaxShards = 8;
 // Error bits written to the workspace error word.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadPage = 2u;
+constexpr unsigned kErrQRange = 4u;   // fp8 caches: a query value beyond the fp16 range
 
 enum Layout : int { kInterleaved = 0, kContiguous = 1 };
 

@@ -37,19 +37,23 @@
 //               O^T is rescaled in TMEM only when a running max grows by more
 //               than 2^8; the epilogue writes o = O / l and lse = m + ln l.
 //
-// fp8 caches (OCP e4m3 codes + one fp32 scale per token): the producer lands
-// a tile's codes (36 KB) in the upper half of the tile's 72 KB stage, one TMA
-// box per page, and the token scales next to it (4-byte cp.async counted on
-// the same barrier); warps 7..10 expand the codes to bf16 in place (e4m3 ->
-// bf16 is exact) in the swizzled layout the MMAs read.  The scales are folded
-// into the logits and into P before its bf16 rounding, so both MMAs see the
-// exact dequantised values.
+// fp8 caches (OCP e4m3 codes + one fp32 scale per token): the MMAs run on
+// fp16 operands.  The producer lands a tile's codes (36 KB) in the upper half
+// of the tile's 72 KB stage, one TMA box per page, and the token scales next
+// to it (4-byte cp.async counted on the same barrier); warps 7..10 expand the
+// codes to fp16 in place (e4m3 -> fp16 is exact and one instruction per two
+// codes) in the swizzled layout the MMAs read, and convert each piece's query
+// group from bf16 to fp16 once (exact for magnitudes in [2^-17, 65504]; a
+// larger value sets an error bit).  The scales are folded into the logits and
+// into P before its fp16 rounding, so both MMAs see the exact dequantised
+// values.
 //
 // Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
 // [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
 // written straight to out_partial; pieces of a split unit go to workspace
 // slots and are merged by mla_merge_kernel.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -77,12 +81,13 @@ struct Misc {
   // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
   // single barrier could complete two phases between tests and alias parities
   uint64_t p_full[2], pv_done[2];
-  uint64_t kv_conv[2];  // fp8: stage expanded to bf16
+  uint64_t kv_conv[2];  // fp8: stage expanded to fp16
   uint64_t q_full, q_empty, o_free;
+  uint64_t q_conv;      // fp8: query group converted to fp16
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
-  float inv_l[kRows];
+  alignas(16) float inv_l[kRows];
   float scale[2][kTile];  // fp8: per-token scales of the tile in each stage
 };
 
@@ -159,6 +164,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 }  // namespace
 
 template <bool kFp8>
@@ -191,6 +201,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   const uint32_t b_p_full = smem_u32(&misc->p_full[0]), b_pv_done = smem_u32(&misc->pv_done[0]);
   const uint32_t b_o_free = smem_u32(&misc->o_free);
   const uint32_t b_kv_conv = smem_u32(&misc->kv_conv[0]);
+  const uint32_t b_q_conv = smem_u32(&misc->q_conv);
+  // the MMAs wait for the query group in its operand type
+  const uint32_t b_q_ready = kFp8 ? b_q_conv : b_q_full;
   // the MMAs wait for the stage in bf16: straight from TMA, or after expansion
   const uint32_t b_kv_ready = kFp8 ? b_kv_conv : b_kv_full;
   volatile int* abort_flag = &misc->abort;
@@ -206,6 +219,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       mbar_init(b_pv_done + 8 * st, kIssuers);
     }
     mbar_init(b_q_full, 1);
+    mbar_init(b_q_conv, kConvThreads / 32);
     mbar_init(b_q_empty, kIssuers);
     mbar_init(b_o_free, kSoftmaxWarps);
     misc->abort = 0;
@@ -327,7 +341,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issue
     const int mi = warp == 6 ? 1 : 0;    // issuer index: chunk parity / latent half
-    const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
+    const uint32_t id_qk = kFp8 ? idesc_f16_f32(64, 64, false, false)
+                                : idesc_bf16_f32(64, 64, false, false);
     // descriptor bases; adding (byte offset >> 4) moves the start address
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
     // K (B of QK^T, K-major): 8-slot groups 9216 bytes apart; V^T (A of P.V,
@@ -341,8 +356,9 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit(pd, unit);
       const int n = t1 - t0;
-      const uint32_t id_pv = idesc_bf16_f32(128, x.rows, true, false);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
+      const uint32_t id_pv = kFp8 ? idesc_f16_f32(128, x.rows, true, false)
+                                  : idesc_bf16_f32(128, x.rows, true, false);
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_ready, pc & 1, tmo, abort_flag));
       int nq = 0, np = 0;
       uint64_t t_idle = 0;
       uint32_t idle_iter = 0;
@@ -427,18 +443,38 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
   } else if (kFp8 && warp >= 7) {
-    // ------------------------------------------------------------ fp8 -> bf16
-    // Thread t expands, for every 64-wide chunk c, 32 codes of tile row t/2
-    // (half t%2 of the chunk) into the row's swizzled bf16 atom of chunk c.
-    // Rows 0..31 (groups 0..3) land below the codes and are expanded at once;
-    // rows 32..63 land on top of the codes of every row, so their threads
-    // hold all their codes in registers until the barrier over the converter
-    // warps says every code has been read.
+    // ------------------------------------------------------------ fp8 -> fp16
+    // Per piece, the query group is converted bf16 -> fp16 in place first.
+    // Per tile, thread t expands the 16-code quarter t%4 of every 64-wide
+    // chunk of rows t/4 and 32 + t/4 into those rows' swizzled fp16 atoms.
+    // The low row lands below the codes and is expanded at once; the high row
+    // lands on top of the codes of every row, so its codes wait in registers
+    // for the barrier over the converter warps that says all codes were read.
     const int ct = threadIdx.x - 7 * 32;   // 0..127
-    const int row = ct >> 1, hh = ct & 1;
-    int gt = 0;
+    const int qq = ct & 3, row_lo = ct >> 2, row_hi = row_lo + kTile / 2;
+    int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
+      {
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
+        if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
+        uint4* q4 = reinterpret_cast<uint4*>(smem + kSmemQ);
+        bool big = false;
+#pragma unroll 4
+        for (int i = ct; i < kTileBytes / 16; i += kConvThreads) {
+          uint4 v = q4[i];
+          v.x = bf16x2_to_f16x2(v.x, big);
+          v.y = bf16x2_to_f16x2(v.y, big);
+          v.z = bf16x2_to_f16x2(v.z, big);
+          v.w = bf16x2_to_f16x2(v.w, big);
+          q4[i] = v;
+        }
+        if (big) atomicOr(&p.hdr->err, kErrQRange);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_q_conv);
+        ++pc;
+      }
       for (int j = t0; j < t1; ++j, ++gt) {
         const int st = gt & 1;
         ok = __all_sync(0xffffffffu,
@@ -447,38 +483,28 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         const bool any_fail = named_bar_or(kBarConv, kConvThreads, !ok);
         if (any_fail) { ok = false; break; }
         uint8_t* stage = smem + kSmemKV + st * kTileBytes;
-        const uint8_t* src = stage + kFp8Staging + row * kDqk + 32 * hh;
-        auto put = [&](int c, uint4 a, uint4 b) {
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const uint8_t* src_lo = stage + kFp8Staging + row_lo * kDqk + 16 * qq;
+        const uint8_t* src_hi = src_lo + (kTile / 2) * kDqk;
+        // 16 codes of chunk c of `row` -> 16 fp16 = the row's 16-byte chunks
+        // 2qq and 2qq+1 of the 128-byte atom row
+        auto put = [&](int row, int c, uint4 a) {
           uint8_t* dst = stage + (row >> 3) * kGroupBytes + c * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {     // 16-byte output chunk 4*hh + q
-            const uint2 lo2 = e4m3x4_to_bf16x4(w[2 * q]);
-            const uint2 hi2 = e4m3x4_to_bf16x4(w[2 * q + 1]);
-            const int ch = 4 * hh + q;
-            *reinterpret_cast<uint4*>(dst + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(lo2.x, lo2.y, hi2.x, hi2.y);
-          }
+          const uint2 h0 = e4m3x4_to_f16x4(a.x), h1 = e4m3x4_to_f16x4(a.y);
+          const uint2 h2 = e4m3x4_to_f16x4(a.z), h3 = e4m3x4_to_f16x4(a.w);
+          *reinterpret_cast<uint4*>(dst + (((2 * qq) ^ (row & 7)) << 4)) =
+              make_uint4(h0.x, h0.y, h1.x, h1.y);
+          *reinterpret_cast<uint4*>(dst + (((2 * qq + 1) ^ (row & 7)) << 4)) =
+              make_uint4(h2.x, h2.y, h3.x, h3.y);
         };
-        if (row < kTile / 2) {   // warp-uniform: warps 7, 8
+        uint4 hi[kChunks];
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            const uint4 a = *reinterpret_cast<const uint4*>(src + 64 * c);
-            const uint4 b = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
-            put(c, a, b);
-          }
-          named_bar_sync(kBarConv, kConvThreads);
-        } else {                 // warps 9, 10
-          uint4 hi[kChunks][2];
+        for (int c = 0; c < kChunks; ++c) hi[c] = *reinterpret_cast<const uint4*>(src_hi + 64 * c);
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-            hi[c][0] = *reinterpret_cast<const uint4*>(src + 64 * c);
-            hi[c][1] = *reinterpret_cast<const uint4*>(src + 64 * c + 16);
-          }
-          named_bar_sync(kBarConv, kConvThreads);   // every row's codes have been read
+        for (int c = 0; c < kChunks; ++c)
+          put(row_lo, c, *reinterpret_cast<const uint4*>(src_lo + 64 * c));
+        named_bar_sync(kBarConv, kConvThreads);   // every row's codes have been read
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) put(c, hi[c][0], hi[c][1]);
-        }
+        for (int c = 0; c < kChunks; ++c) put(row_hi, c, hi[c]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_kv_conv + 8 * st);
@@ -577,7 +603,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             const float p1 = ex2_approx(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
             if constexpr (kFp8) {
               // P.V multiplies the codes; the token scale rides on P
-              pk[a] = pack_bf16x2(p0 * sc[2 * a], p1 * sc[2 * a + 1]);
+              pk[a] = pack_f16x2(p0 * sc[2 * a], p1 * sc[2 * a + 1]);
             } else {
               pk[a] = pack_bf16x2(p0, p1);
             }

@@ -182,6 +182,32 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t codes) {
   return make_uint2(b01, b23);
 }
 
+// Four OCP e4m3 codes -> four fp16 values (exact: every e4m3 value, NaN
+// included, is an fp16 value), as two f16x2 words; byte k of `codes` becomes
+// half k.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(codes));
+  return make_uint2(h01, h23);
+}
+
+// Two bf16 (one word) -> two fp16, round to nearest even.  Exact for
+// magnitudes in [2^-17, 65504]; `overflow` is set when a finite value
+// rounds to infinity.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& overflow) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  overflow |= (fabsf(lo) >= 65520.0f && fabsf(lo) != __int_as_float(0x7f800000)) ||
+              (fabsf(hi) >= 65520.0f && fabsf(hi) != __int_as_float(0x7f800000));
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z, int w) {
   asm volatile(
@@ -312,6 +338,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+
+// The same with fp16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace mla

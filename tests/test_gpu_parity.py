@@ -169,3 +169,27 @@ def test_fp8_causal_verify_with_wuv(dev):
     w = mi.build_workload("fp8v", 3, 9, 32, [300, 9, 2000], 2, "interleaved", "fp8", True,
                           seed=410, kv_sigma=1.0, poison=True, with_w_uv=True)
     compare_all(w, dev)
+
+
+def test_fp8_query_beyond_fp16_range_is_reported(dev):
+    """With fp8 caches the tensor cores run on fp16 operands; a finite query
+    value that fp16 cannot hold is reported, not silently turned into inf."""
+    import sequence_sharded_mla_gb300 as mla
+    w = mi.build_workload("fp8big", 1, 1, 16, [100], 2, "interleaved", "fp8", False, seed=420,
+                          kv_sigma=1.0)
+    w.q[0, 0, 3, 7] = 0x4780          # bf16 65536.0
+    res = run_gpu(w, dev, with_wuv=False)
+    assert res["status"] == -7          # MLA_ERR_RANGE
+    assert mla.mla_get_device_error(res["workspace"]) == 0
+    w.q[0, 0, 3, 7] = 0x477F          # bf16 65280.0: representable in fp16
+    res = run_gpu(w, dev, with_wuv=False)
+    assert res["status"] == 0
+
+
+def test_fp8_small_query_values_stay_within_tolerance(dev):
+    """Query components far below the fp16 normal range (2^-14) are rounded
+    to fp16 subnormals; the result still matches the oracle, which keeps the
+    exact bf16 values."""
+    w = mi.build_workload("fp8tiny", 2, 1, 32, [700, 1300], 2, "contiguous", "fp8", False,
+                          seed=430, kv_sigma=1.0, q_sigma=1e-5)
+    compare_all(w, dev)
