@@ -63,8 +63,24 @@ typedef enum mla_status {
  *   INTERLEAVED  t mod N == s                  (N must divide 64)
  *   CONTIGUOUS   s*c <= t < min((s+1)*c, L),   c = ceil(L / N)
  * The section's worked example (a 200K-token request on 4 GPUs holding
- * 0-50K, 50K-100K, 100K-150K, 150K-200K) is the CONTIGUOUS layout. */
-typedef enum mla_layout { MLA_LAYOUT_INTERLEAVED = 0, MLA_LAYOUT_CONTIGUOUS = 1 } mla_layout;
+ * 0-50K, 50K-100K, 100K-150K, 150K-200K) is the CONTIGUOUS layout.
+ * With these two the cache and block table describe whole requests (every
+ * position t at page block_table[b][t / 64], row t % 64).
+ *
+ * The *_LOCAL layouts are the same shards, stored the way each GPU of a
+ * multi-GPU deployment holds its slice (section 4: each GPU stores only its
+ * chunk): the cache and block table hold only shard `shard_id`'s positions,
+ * in order, compactly -- local position p of request b is page
+ * block_table[b][p / 64], row p % 64, and is global position p*N + s
+ * (INTERLEAVED_LOCAL, any N <= 8) or s*c + p (CONTIGUOUS_LOCAL).  seq_lens
+ * stay the global lengths L_b: they fix the shard's token count and the
+ * causal mask.  shard_id must name one shard. */
+typedef enum mla_layout {
+  MLA_LAYOUT_INTERLEAVED = 0,
+  MLA_LAYOUT_CONTIGUOUS = 1,
+  MLA_LAYOUT_INTERLEAVED_LOCAL = 2,
+  MLA_LAYOUT_CONTIGUOUS_LOCAL = 3
+} mla_layout;
 
 typedef enum mla_kv_dtype { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 
@@ -115,8 +131,9 @@ size_t mla_workspace_size(const mla_shape* shape, int num_shards, int shard_id);
  *
  * Arguments: q, block_table, seq_lens, out_partial, lse_partial, workspace:
  * device pointers, layouts above.  max_pages_per_req: row stride of
- * block_table; it must cover ceil(L_b / 64) entries of every request (only
- * those entries are read).  num_shards: 1..8.  workspace_bytes must be at
+ * block_table; it must cover the pages of every request (ceil(L_b / 64), or
+ * ceil(n_s / 64) for a local layout holding n_s of the request's positions;
+ * only those entries are read).  num_shards: 1..8.  workspace_bytes must be at
  * least mla_workspace_size(shape, num_shards, shard_id).
  *
  * Errors: MLA_ERR_INVALID / MLA_ERR_UNSUPPORTED / MLA_ERR_WORKSPACE before

@@ -285,6 +285,58 @@ def build_workload(name, batch, q_len, num_heads, seq_lens, num_shards, layout,
                     kv_scale=kv_scale, block_table=bt, w_uv=w_uv)
 
 
+def local_shard_cache(w: Workload, num_shards: int, shard: int, layout: str, seed: int = 0):
+    """The slice of workload ``w``'s cache that shard ``shard`` of
+    ``num_shards`` holds on its own GPU in a multi-GPU deployment: only the
+    shard's token positions, in order, packed 64 to a page into a fresh page
+    pool (scattered by a seeded permutation).  Interleaved shards own
+    positions t = shard, shard + N, ...; contiguous shards own
+    [shard * c, min((shard + 1) * c, L)), c = ceil(L / N).  Rows of the pool
+    that hold no token are NaN-poisoned.
+
+    Returns dict(kv, kv_scale, block_table, local_lens): the local cache in
+    the same dtypes as ``w``, the local block table [B, max local pages] and
+    each request's local token count.  The global lengths stay ``w.seq_lens``.
+    """
+    N, s = int(num_shards), int(shard)
+    toks = []
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        if layout == "interleaved":
+            t = np.arange(s, L, N, dtype=np.int64)
+        elif layout == "contiguous":
+            c = -(-L // N)
+            t = np.arange(s * c, min((s + 1) * c, L), dtype=np.int64)
+        else:
+            raise ValueError(layout)
+        toks.append(t)
+    npages = [-(-len(t) // PAGE) for t in toks]
+    P = max(1, sum(npages))
+    perm = permutation(seed + 7919 * (s + 1), S_PERM + 50, P)
+    kv = np.empty((P, PAGE, D_QK), dtype=w.kv.dtype)
+    kv[...] = 0x7FC0 if w.kv.dtype == np.uint16 else 0x7F
+    kv_scale = None
+    if w.kv_scale is not None:
+        kv_scale = np.full((P, PAGE), np.nan, dtype=np.float32)
+    bt = np.full((w.batch, max(1, max(npages))), -1, dtype=np.int32)
+    off = 0
+    for b, t in enumerate(toks):
+        n = npages[b]
+        pages = perm[off:off + n]
+        off += n
+        bt[b, :n] = pages
+        if len(t) == 0:
+            continue
+        k = np.arange(len(t))
+        src_page = w.block_table[b, t // PAGE]
+        src_row = t % PAGE
+        kv[pages[k // PAGE], k % PAGE] = w.kv[src_page, src_row]
+        if kv_scale is not None:
+            kv_scale[pages[k // PAGE], k % PAGE] = w.kv_scale[src_page, src_row]
+    local_lens = np.array([len(t) for t in toks], dtype=np.int32)
+    return dict(kv=kv, kv_scale=kv_scale, block_table=bt, local_lens=local_lens)
+
+
 CONFIG_NAMES = {
     1: "tiny-b1-h16-l1024-n2-interleaved",
     2: "bimodal-agentic-b32-h64-n4-interleaved",

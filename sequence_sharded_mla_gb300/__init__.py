@@ -19,7 +19,7 @@ from . import build as _build
 D_QK, D_V, D_UV, PAGE = 576, 512, 128, 64
 ALL_SHARDS = -1
 DEFAULT_SCALE = 1.0 / math.sqrt(192.0)
-LAYOUTS = {"interleaved": 0, "contiguous": 1}
+LAYOUTS = {"interleaved": 0, "contiguous": 1, "interleaved_local": 2, "contiguous_local": 3}
 KV_BF16, KV_FP8 = 0, 1
 
 STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_CUDA",

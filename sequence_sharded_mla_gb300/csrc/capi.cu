@@ -136,7 +136,11 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (!shape_ok(shape)) return MLA_ERR_INVALID;
   if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
   if (shard_id != MLA_ALL_SHARDS && (shard_id < 0 || shard_id >= num_shards)) return MLA_ERR_INVALID;
-  if (layout != MLA_LAYOUT_INTERLEAVED && layout != MLA_LAYOUT_CONTIGUOUS) return MLA_ERR_INVALID;
+  if (layout != MLA_LAYOUT_INTERLEAVED && layout != MLA_LAYOUT_CONTIGUOUS &&
+      layout != MLA_LAYOUT_INTERLEAVED_LOCAL && layout != MLA_LAYOUT_CONTIGUOUS_LOCAL)
+    return MLA_ERR_INVALID;
+  const bool local = layout == MLA_LAYOUT_INTERLEAVED_LOCAL || layout == MLA_LAYOUT_CONTIGUOUS_LOCAL;
+  if (local && shard_id == MLA_ALL_SHARDS) return MLA_ERR_INVALID;   // a local cache is one shard's
   if (kv->data == nullptr || kv->num_pages < 1 || max_pages_per_req < 1) return MLA_ERR_INVALID;
   if (kv->page_size != kPage) return MLA_ERR_UNSUPPORTED;
   if (kv->dtype == MLA_KV_BF16) {
@@ -171,7 +175,10 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   pd.num_shards = num_shards;
   pd.shard_first = shard_id == MLA_ALL_SHARDS ? 0 : shard_id;
   pd.n_out = shard_id == MLA_ALL_SHARDS ? num_shards : 1;
-  pd.layout = layout == MLA_LAYOUT_INTERLEAVED ? kInterleaved : kContiguous;
+  pd.layout = (layout == MLA_LAYOUT_INTERLEAVED || layout == MLA_LAYOUT_INTERLEAVED_LOCAL)
+                  ? kInterleaved
+                  : kContiguous;
+  pd.local = local ? 1 : 0;
   pd.causal = shape->causal;
   pd.num_pages = kv->num_pages;
   pd.max_pages = max_pages_per_req;
@@ -208,7 +215,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // (-, 1152 nv, 128, 9216 nv, 1152) starts at cache row page*64 + residue
   // and lands the residue's 64/nv rows of a page, all 9 chunks, in one box in
   // the group-major shared-memory layout.
-  const int nv = pd.layout == kInterleaved ? num_shards : 1;
+  const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   if (fp8) {
     // e4m3 codes: view [page][row / nv][row % nv][3][192] read as

@@ -52,7 +52,10 @@ struct ProblemDesc {
   int num_shards;      // N
   int shard_first;     // first shard computed by this call
   int n_out;           // shards computed by this call (N, or 1)
-  int layout;          // Layout
+  int layout;          // Layout: which global positions shard s owns
+  int local;           // 1: the cache holds only the computed shard's tokens,
+                       // compactly in order (local position p of request b is
+                       // page block_table[b][p / 64], row p % 64)
   int causal;
   int num_pages;
   int max_pages;
@@ -82,7 +85,7 @@ struct Unit {
   int rows;         // valid query rows in this group (<= 64, multiple of 16)
   int tiles;        // pipeline tiles
   int tstart, tend; // contiguous layout: global token range of the shard
-  int p0;           // contiguous layout: first page slot
+  int p0;           // contiguous layout, global cache: first page slot
 };
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -108,19 +111,25 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
     int c = ceil_div(L, pd.num_shards);
     x.tstart = x.s * c;
     x.tend = min(x.tstart + c, L);
-    if (x.tstart < x.tend) {
+    if (x.tstart >= x.tend) {
+      x.tiles = 0;
+    } else if (pd.local) {
+      x.tiles = ceil_div(x.tend - x.tstart, kTile);
+    } else {
       x.p0 = x.tstart / kPage;
       x.tiles = (x.tend - 1) / kPage - x.p0 + 1;
-    } else {
-      x.tiles = 0;
     }
   }
   return x;
 }
 
-// Global token position of slot a (0..63) of tile j of unit x.
+// Global token position of slot a (0..63) of tile j of unit x.  Interleaved
+// shards: tile j holds the shard's positions 64j..64j+63 (in a local cache,
+// exactly local page j).  Contiguous shards: tile j is global page p0 + j, or
+// local page j of a local cache.
 __device__ __forceinline__ int slot_token(const ProblemDesc& pd, const Unit& x, int j, int a) {
   if (pd.layout == kInterleaved) return (j * kTile + a) * pd.num_shards + x.s;
+  if (pd.local) return x.tstart + j * kTile + a;
   return (x.p0 + j) * kPage + a;
 }
 

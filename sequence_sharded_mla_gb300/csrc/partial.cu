@@ -250,21 +250,23 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // ------------------------------------------------------------ producer
     // Lane k < nv issues the boxes of page k of the tile; lane 0 arms each
     // group barrier with the group's whole byte count first.
-    const int nv = pd.layout == kInterleaved ? pd.num_shards : 1;  // page boxes per tile
+    // page boxes per tile: N pages' residue rows for interleaved shards of a
+    // global cache, otherwise one whole page
+    const int nv = (pd.layout == kInterleaved && !pd.local) ? pd.num_shards : 1;
     const int box_bytes = kTileBytes / nv;   // bf16: the whole groups of one page
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit(pd, unit);
-      const int npages_b = ceil_div(x.L, kPage);
+      const int npages_b = pd.local ? x.tiles : ceil_div(x.L, kPage);   // block-table entries
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
-      const int res = pd.layout == kInterleaved ? x.s : 0;
+      const int res = nv > 1 ? x.s : 0;
       int win_base = -1, win_val = -1;
       for (int j = t0; j < t1 && ok; ++j, ++gt) {
         const int st = gt & 1;
         // page slot of this lane's box; nv divides 32, so a tile never
         // straddles two 32-entry windows of the block table
-        const int first_slot = pd.layout == kInterleaved ? j * nv : x.p0 + j;
+        const int first_slot = nv > 1 ? j * nv : (pd.local || pd.layout == kInterleaved ? j : x.p0 + j);
         const int wb = first_slot & ~31;
         if (wb != win_base && first_slot < npages_b) {
           win_base = wb;

@@ -74,3 +74,20 @@ def test_profile_events_take_both_or_neither():
     assert L.mla_set_profile_events(None, ctypes.c_void_p(64)) == -1
     assert L.mla_set_profile_events(ctypes.c_void_p(64), None) == -1
     assert L.mla_set_profile_events(None, None) == 0
+
+
+def test_local_layouts_need_one_shard():
+    """A local cache holds one shard's positions: computing every shard from
+    it is an argument error, found before any CUDA call."""
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    sh = mla.mla_shape(1, 1, 16, 0, 0.07)
+    kv = mla.mla_kv_pages(ctypes.c_void_p(256), None, 0, 1, 64)
+    fake = ctypes.c_void_p(512)
+    for layout in (2, 3):
+        st = L.mla_decode_partial(fake, ctypes.byref(kv), fake, 1, fake, ctypes.byref(sh), -1, 2,
+                                  layout, fake, fake, fake, 1 << 20, None)
+        assert st == -1
+    st = L.mla_decode_partial(fake, ctypes.byref(kv), fake, 1, fake, ctypes.byref(sh), 0, 2, 7,
+                              fake, fake, fake, 1 << 20, None)
+    assert st == -1

@@ -193,3 +193,46 @@ def test_fp8_small_query_values_stay_within_tolerance(dev):
     w = mi.build_workload("fp8tiny", 2, 1, 32, [700, 1300], 2, "contiguous", "fp8", False,
                           seed=430, kv_sigma=1.0, q_sigma=1e-5)
     compare_all(w, dev)
+
+
+@pytest.mark.parametrize("layout,N", [("interleaved", 2), ("interleaved", 3), ("interleaved", 8),
+                                      ("contiguous", 3), ("contiguous", 4)])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_local_shard_caches(dev, layout, N, kv_dtype):
+    """Each shard computed from a cache that holds only its own positions (the
+    layout each GPU of a multi-GPU deployment stores) equals that shard's
+    partial over the whole cache, causal verify included; the combine of all
+    shards equals unsharded attention."""
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    lens = [1, 100, 777, 4099]
+    w = mi.build_workload("local", len(lens), 2, 32, lens, N, layout, kv_dtype, True,
+                          seed=440 + N, kv_sigma=1.0 if kv_dtype == "fp8" else 0.5, poison=True)
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    rows = w.batch * w.q_len * w.num_heads
+    parts, lses = [], []
+    for s in range(N):
+        d = mi.local_shard_cache(w, N, s, layout, seed=s)
+        if kv_dtype == "bf16":
+            kv = torch.from_numpy(d["kv"].view(np.int16)).view(torch.bfloat16).to(dev)
+            sc = None
+        else:
+            kv = torch.from_numpy(d["kv"]).to(dev)
+            sc = torch.from_numpy(d["kv_scale"]).to(dev)
+        bt = torch.from_numpy(d["block_table"]).to(dev)
+        part, lse, ws = mla.mla_decode_partial(q, kv, bt, sl, N, layout + "_local", shard_id=s,
+                                               kv_scale=sc, causal=True)
+        torch.cuda.synchronize()
+        assert mla.mla_get_device_error(ws) == 0
+        ref_o, ref_l = oracle.attend(w, shard=s, num_shards=N, layout=layout)
+        check_close(part.cpu().numpy().reshape(rows, 512), ref_o, TOL_OUT, f"local shard {s}",
+                    rel=REL_OUT)
+        check_close(lse.cpu().numpy().reshape(rows), ref_l, TOL_LSE, f"local lse {s}")
+        parts.append(part[0])
+        lses.append(lse[0])
+    out, lse_out = mla.mla_shard_combine(torch.stack(parts), torch.stack(lses), causal=True)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = oracle.reference_step(w)
+    check_close(bf16_to_np(out).reshape(rows, 512), ref, TOL_OUT, "out", rel=REL_OUT)
+    check_close(lse_out.cpu().numpy().reshape(rows), ref_lse, TOL_LSE, "lse")
