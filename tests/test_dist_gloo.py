@@ -42,7 +42,7 @@ def _reduce_worker(rank, world, port, out):
 
 def test_reduce_over_ranks_takes_max_time_and_total_bytes():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_reduce_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
