@@ -194,6 +194,7 @@ class Workload:
     kv_scale: Optional[np.ndarray] = None  # float32 [P, 64] (fp8 only)
     block_table: np.ndarray = None     # int32 [B, max_pages]
     w_uv: Optional[np.ndarray] = None  # uint16 [H, 512, 128] or None
+    q_lens: Optional[np.ndarray] = None  # int32 [B]: query tokens per request (None: all q_len)
     softmax_scale: float = SOFTMAX_SCALE
     notes: dict = field(default_factory=dict)
 
@@ -219,7 +220,7 @@ class Workload:
 def build_workload(name, batch, q_len, num_heads, seq_lens, num_shards, layout,
                    kv_dtype, causal, seed, q_sigma=0.5, kv_sigma=0.5,
                    with_w_uv=False, w_sigma=0.02, extra_pages=0, poison=False,
-                   pinned=False, max_pages=None):
+                   pinned=False, max_pages=None, q_lens=None):
     """Generate every tensor of one workload.
 
     Pages are assigned to requests through a seeded random permutation of the
@@ -282,7 +283,8 @@ def build_workload(name, batch, q_len, num_heads, seq_lens, num_shards, layout,
     return Workload(name=name, batch=batch, q_len=q_len, num_heads=num_heads,
                     seq_lens=seq_lens, num_shards=num_shards, layout=layout,
                     kv_dtype=kv_dtype, causal=causal, seed=seed, q=q, kv=kv,
-                    kv_scale=kv_scale, block_table=bt, w_uv=w_uv)
+                    kv_scale=kv_scale, block_table=bt, w_uv=w_uv,
+                    q_lens=None if q_lens is None else np.asarray(q_lens, dtype=np.int32))
 
 
 def local_shard_cache(w: Workload, num_shards: int, shard: int, layout: str, seed: int = 0):

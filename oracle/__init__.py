@@ -24,7 +24,7 @@ def lib():
     if _LIB is None:
         L = ctypes.CDLL(_build.build())
         vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        L.oracle_attend.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp,
+        L.oracle_attend.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, vp,
                                     i32, dbl, i32, i32, i32, vp, i64, vp, vp]
         L.oracle_attend.restype = i32
         L.oracle_lse_merge.argtypes = [vp, vp, i32, i64, vp, vp]
@@ -51,18 +51,24 @@ def _p(a):
 
 
 def attend(w, shard=-1, num_shards=None, layout=None, rows=None, q=None, seq_lens=None,
-           block_table=None, kv=None, kv_scale=None):
+           block_table=None, kv=None, kv_scale=None, q_lens=None):
     """(out [n,512] fp64, lse [n] fp64) for query rows of workload ``w``.
 
     ``rows`` are flattened (b * q_len + i) * H + h indices (None = all rows).
     ``shard`` < 0 gives unsharded attention; otherwise shard ``shard`` of
     ``num_shards`` under ``layout``.  Individual tensors may be overridden.
+    ``q_lens`` (default ``w.q_lens``): per-request query counts of a padded
+    batch (rows i >= q_lens[b] are padding: lse -inf, out 0).
     """
     q = w.q if q is None else q
     seq_lens = w.seq_lens if seq_lens is None else seq_lens
     block_table = w.block_table if block_table is None else block_table
     kv = w.kv if kv is None else kv
     kv_scale = w.kv_scale if kv_scale is None else kv_scale
+    if q_lens is None and w is not None:
+        q_lens = getattr(w, "q_lens", None)
+    if q_lens is not None:
+        q_lens = np.ascontiguousarray(q_lens, dtype=np.int32)
     B, q_len, H = q.shape[0], q.shape[1], q.shape[2]
     seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     block_table = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -79,7 +85,8 @@ def attend(w, shard=-1, num_shards=None, layout=None, rows=None, q=None, seq_len
     scale = w.softmax_scale if w is not None else 1.0 / np.sqrt(192.0)
     causal = int(w.causal) if w is not None else 0
     st = lib().oracle_attend(_p(q), B, q_len, H, _p(kv), _p(kv_scale), fp8, kv.shape[0],
-                             _p(block_table), block_table.shape[1], _p(seq_lens), causal,
+                             _p(block_table), block_table.shape[1], _p(seq_lens), _p(q_lens),
+                             causal,
                              float(scale), int(shard), int(ns), lay, _p(rows), n,
                              _p(out), _p(lse))
     if st != 0:

@@ -135,12 +135,19 @@ int oracle_token_owner(long t, long L, int nshards, int layout) {
  * Attention for a list of query rows.  Row index r encodes
  * (b * q_len + i) * H + h.  rows == NULL means all B*q_len*H rows in order.
  * shard < 0 selects the unsharded token set.
+ *
+ * q_lens (may be NULL): request b carries q_lens[b] <= q_len query tokens;
+ * its rows i >= q_lens[b] are padding and see no token, and its causal
+ * query i sees t <= L - q_lens[b] + i.  This is a batch of verify steps
+ * with different draft counts padded to one q_len ("GLM-5.2" deployment
+ * post, sections 2.1-2.2: 1 + N tokens per request per step).
  */
 int oracle_attend(const uint16_t* q, int B, int q_len, int H, const void* kv,
                   const float* kv_scale, int kv_fp8, int num_pages,
                   const int32_t* block_table, int max_pages, const int32_t* seq_lens,
-                  int causal, double softmax_scale, int shard, int nshards, int layout,
-                  const int64_t* rows, int64_t n_rows, double* out, double* lse) {
+                  const int32_t* q_lens, int causal, double softmax_scale, int shard,
+                  int nshards, int layout, const int64_t* rows, int64_t n_rows, double* out,
+                  double* lse) {
   if (B <= 0 || q_len <= 0 || H <= 0) return ORACLE_BAD_ARG;
   if (shard >= 0 && (nshards <= 0 || shard >= nshards)) return ORACLE_BAD_ARG;
   cache_view cv = {kv, kv_scale, kv_fp8, num_pages, block_table, max_pages};
@@ -155,6 +162,13 @@ int oracle_attend(const uint16_t* q, int B, int q_len, int H, const void* kv,
     int i = (int)((r / H) % q_len);
     int b = (int)(r / ((int64_t)H * q_len));
     long L = seq_lens[b];
+    int qn = q_lens ? q_lens[b] : q_len;
+    if (i >= qn) { /* padding row */
+      double* o0 = out + (size_t)k * D_V;
+      for (int c = 0; c < D_V; ++c) o0[c] = 0.0;
+      lse[k] = -INFINITY;
+      continue;
+    }
     double qv[D_QK], kt[D_QK];
     const uint16_t* qrow = q + (size_t)r * D_QK;
     for (int d = 0; d < D_QK; ++d) qv[d] = bf16_value(qrow[d]);
@@ -168,7 +182,7 @@ int oracle_attend(const uint16_t* q, int B, int q_len, int H, const void* kv,
     double m = -INFINITY;
     int bad = 0;
     for (long t = 0; t < L; ++t) {
-      if (!token_visible(t, L, q_len, i, causal, shard, nshards, layout)) continue;
+      if (!token_visible(t, L, qn, i, causal, shard, nshards, layout)) continue;
       if (gather_row(&cv, b, t, kt) != ORACLE_OK) { bad = 1; break; }
       double acc = 0.0;
       for (int d = 0; d < D_QK; ++d) acc += qv[d] * kt[d];
@@ -191,12 +205,12 @@ int oracle_attend(const uint16_t* q, int B, int q_len, int H, const void* kv,
     /* pass 2: normaliser */
     double z = 0.0;
     for (long t = 0; t < L; ++t)
-      if (token_visible(t, L, q_len, i, causal, shard, nshards, layout)) z += exp(s[t] - m);
+      if (token_visible(t, L, qn, i, causal, shard, nshards, layout)) z += exp(s[t] - m);
     double l = m + log(z);
     lse[k] = l;
     /* pass 3: probability-weighted sum of the latent values */
     for (long t = 0; t < L; ++t) {
-      if (!token_visible(t, L, q_len, i, causal, shard, nshards, layout)) continue;
+      if (!token_visible(t, L, qn, i, causal, shard, nshards, layout)) continue;
       gather_row(&cv, b, t, kt);
       double p = exp(s[t] - l);
       for (int c = 0; c < D_V; ++c) o[c] += p * kt[c];

@@ -225,6 +225,54 @@ def test_causal_mask_changes_result():
     assert not np.allclose(oa[:2], ob[:2])
 
 
+def test_variable_query_counts_equal_shorter_decodes_and_pad_the_rest():
+    """A batch of verify steps with different draft counts, padded to one
+    q_len: query i < q_lens[b] of request b sees t <= L - q_lens[b] + i, the
+    same as a single-token decode of that query over the first
+    L - q_lens[b] + 1 + i tokens; rows i >= q_lens[b] see nothing."""
+    w = small(53, B=3, q_len=5, H=2, lens=(90, 64, 130), causal=True)
+    w.q_lens = np.array([1, 5, 3], dtype=np.int32)
+    out, lse = orc.attend(w, shard=-1)
+    for b in range(3):
+        qn = int(w.q_lens[b])
+        for i in range(5):
+            rows = [(b * 5 + i) * 2 + h for h in range(2)]
+            if i >= qn:
+                assert np.all(out[rows] == 0.0) and np.all(np.isneginf(lse[rows]))
+                continue
+            q1 = np.ascontiguousarray(w.q[b:b + 1, i:i + 1])
+            lens1 = np.array([w.seq_lens[b] - qn + 1 + i], dtype=np.int32)
+            w1 = mi.Workload("q1", 1, 1, 2, lens1, 1, "interleaved", "bf16", False, 0,
+                             q=q1, kv=w.kv, block_table=np.ascontiguousarray(w.block_table[b:b + 1]))
+            o1, l1 = orc.attend(w1, shard=-1)
+            for h in range(2):
+                assert np.array_equal(out[rows[h]], o1[h])
+                assert lse[rows[h]] == l1[h]
+
+
+def test_full_query_counts_equal_a_uniform_batch():
+    w = small(54, B=2, q_len=4, H=2, lens=(70, 200), causal=True)
+    o0, l0 = orc.attend(w, shard=-1)
+    w.q_lens = np.array([4, 4], dtype=np.int32)
+    o1, l1 = orc.attend(w, shard=-1)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_variable_query_counts_shard_and_merge():
+    """The shard invariant holds row by row for padded batches too."""
+    w = small(55, B=3, q_len=4, H=2, lens=(30, 150, 9), causal=True)
+    w.q_lens = np.array([2, 4, 1], dtype=np.int32)
+    ref, ref_lse = orc.attend(w, shard=-1)
+    for layout in ("interleaved", "contiguous"):
+        for N in (2, 3):
+            parts = [orc.attend(w, shard=s, num_shards=N, layout=layout) for s in range(N)]
+            o, l = orc.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+            fin = np.isfinite(ref_lse)
+            assert np.array_equal(np.isneginf(l), np.isneginf(ref_lse))
+            assert np.allclose(o, ref, rtol=0, atol=1e-12)
+            assert np.allclose(l[fin], ref_lse[fin], rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- fp8 codec
 def e4m3_closed_form(c):
     s = -1.0 if c & 0x80 else 1.0
