@@ -92,10 +92,19 @@ typedef enum mla_kv_dtype { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
  * last q_len entries of the cache), query i sees tokens t <= L - q_len + i. */
 typedef struct mla_shape {
   int batch;            /* B >= 1 */
-  int q_len;            /* query tokens per request >= 1 */
+  int q_len;            /* query tokens per request >= 1 (the padded count, see q_lens) */
   int num_heads;        /* H: multiple of 16 */
   int causal;           /* 0 or 1 */
   float softmax_scale;  /* logits = softmax_scale * q . k  (1/sqrt(192) for the workloads here) */
+  /* Optional (NULL = every request has q_len query tokens), device int32
+   * [B]: request b has q_lens[b] in [1, q_len] query tokens -- a batch of
+   * verify steps with different draft counts padded to q_len.  Rows
+   * i >= q_lens[b] are padding: their partials are o = 0, lse = -inf and
+   * their combined output is 0.  With causal, query i of request b sees
+   * t <= L_b - q_lens[b] + i.  A value outside [1, q_len] is clamped and
+   * reported as MLA_ERR_INVALID by mla_get_device_error.  Ignored by
+   * mla_shard_combine and mla_workspace_size. */
+  const int32_t* q_lens;
 } mla_shape;
 
 /* The paged latent cache (device memory, not modified). */
@@ -198,8 +207,9 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
 /*
  * Synchronises `stream`, reads and clears the device error word kept in
  * `workspace` by the last mla_decode_partial on it.  Returns MLA_OK,
- * MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_RANGE (in that order of
- * precedence when several occurred) or MLA_ERR_CUDA.
+ * MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_RANGE or MLA_ERR_INVALID (a
+ * q_lens entry out of range), in that order of precedence when several
+ * occurred, or MLA_ERR_CUDA.
  */
 mla_status mla_get_device_error(void* workspace, void* stream);
 
@@ -218,7 +228,8 @@ mla_status mla_set_profile_events(void* before_partial, void* after_partial);
 /* Static description of a status code. */
 const char* mla_status_string(mla_status status);
 
-/* Library version: major * 10000 + minor * 100 + patch. */
+/* Library version: major * 10000 + minor * 100 + patch.  0.2.0 added
+ * mla_shape.q_lens, the *_LOCAL layouts and MLA_ERR_RANGE. */
 int mla_version(void);
 
 #ifdef __cplusplus

@@ -35,7 +35,8 @@ class MLAError(RuntimeError):
 
 class mla_shape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("num_heads", ctypes.c_int),
-                ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+                ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+                ("q_lens", ctypes.c_void_p)]
 
 
 class mla_kv_pages(ctypes.Structure):
@@ -80,9 +81,9 @@ def lib():
     return _LIB
 
 
-def _shape(batch, q_len, num_heads, causal, softmax_scale):
+def _shape(batch, q_len, num_heads, causal, softmax_scale, q_lens=None):
     return mla_shape(int(batch), int(q_len), int(num_heads), int(bool(causal)),
-                     float(softmax_scale))
+                     float(softmax_scale), None if q_lens is None else q_lens.data_ptr())
 
 
 def _stream_ptr(stream):
@@ -118,13 +119,15 @@ def mla_workspace_size(batch, q_len, num_heads, num_shards, shard_id=ALL_SHARDS,
 def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
                        shard_id=ALL_SHARDS, kv_scale=None, causal=False,
                        softmax_scale=DEFAULT_SCALE, out_partial=None, lse_partial=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, q_lens=None):
     """Per-shard partial attention; returns (out_partial, lse_partial, workspace).
 
     q: bf16 [B, q_len, H, 576]; kv: bf16 [P, 64, 576] or e4m3 codes
     (uint8 / float8_e4m3fn) [P, 64, 576] with kv_scale fp32 [P, 64];
     block_table: int32 [B, max_pages]; seq_lens: int32 [B] (device).
     out_partial: fp32 [n_out, B, q_len, H, 512]; lse_partial: fp32 [n_out, B, q_len, H].
+    q_lens: optional int32 [B] (device) query tokens per request of a padded
+    batch (rows i >= q_lens[b] are padding).
     """
     _check(q, "q", (torch.bfloat16,), 4)
     dev = q.device
@@ -152,7 +155,9 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
         lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
     _check(out_partial, "out_partial", (torch.float32,), 5, dev)
     _check(lse_partial, "lse_partial", (torch.float32,), 4, dev)
-    sh = _shape(B, q_len, H, causal, softmax_scale)
+    if q_lens is not None:
+        _check(q_lens, "q_lens", (torch.int32,), 1, dev)
+    sh = _shape(B, q_len, H, causal, softmax_scale, q_lens)
     need = int(lib().mla_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
@@ -171,7 +176,7 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
 def mla_decode_partial_noalloc(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
                                shard_id=ALL_SHARDS, kv_scale=None, causal=False,
                                softmax_scale=DEFAULT_SCALE, out_partial=None, lse_partial=None,
-                               stream=None):
+                               stream=None, q_lens=None):
     """mla_decode_partial on the library's fixed scratch buffer (no workspace).
 
     For callers that may not allocate device memory; the output tensors are
@@ -188,7 +193,7 @@ def mla_decode_partial_noalloc(q, kv, block_table, seq_lens, num_shards, layout=
         out_partial = torch.empty((n_out, B, q_len, H, D_V), dtype=torch.float32, device=dev)
     if lse_partial is None:
         lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
-    sh = _shape(B, q_len, H, causal, softmax_scale)
+    sh = _shape(B, q_len, H, causal, softmax_scale, q_lens)
     pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
                          kv_dtype, kv.shape[0], kv.shape[1])
     st = lib().mla_decode_partial_noalloc(_ptr(q), ctypes.byref(pages), _ptr(block_table),

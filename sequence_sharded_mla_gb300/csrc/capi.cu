@@ -34,7 +34,7 @@ using namespace mla;
 
 namespace {
 
-constexpr int kVersion = 100;  // 0.1.0
+constexpr int kVersion = 200;  // 0.2.0
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // device waits give up after 2 s
 constexpr int kMinTilesPerCta = 4;
 // Work positions charged to a unit for its fixed costs (query load, pipeline
@@ -185,6 +185,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   pd.scale_log2 = shape->softmax_scale * 1.4426950408889634f;
   pd.block_table = block_table;
   pd.seq_lens = seq_lens;
+  pd.q_lens = shape->q_lens;
 
   // query rows: [B*q_len*H, 576] bf16.  Preferred view [rows][9 chunks][64]
   // read as (64 dims, rows, chunk) so one box lands a 64-row group in the
@@ -316,6 +317,7 @@ mla_status mla_get_device_error(void* workspace, void* stream) {
   if (err & kErrTimeout) return MLA_ERR_TIMEOUT;
   if (err & kErrBadPage) return MLA_ERR_DEVICE_BOUNDS;
   if (err & kErrQRange) return MLA_ERR_RANGE;
+  if (err & kErrQLens) return MLA_ERR_INVALID;
   return MLA_OK;
 }
 

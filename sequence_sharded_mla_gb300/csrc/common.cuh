@@ -23,6 +23,7 @@ constexpr int kMaxShards = 8;
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadPage = 2u;
 constexpr unsigned kErrQRange = 4u;   // fp8 caches: a query value beyond the fp16 range
+constexpr unsigned kErrQLens = 8u;    // a per-request query count outside [1, q_len]
 
 enum Layout : int { kInterleaved = 0, kContiguous = 1 };
 
@@ -62,6 +63,7 @@ struct ProblemDesc {
   float scale_log2;    // softmax scale * log2(e)
   const int32_t* block_table;  // [B, max_pages]
   const int32_t* seq_lens;     // [B]
+  const int32_t* q_lens;       // [B] query tokens per request, or null (all q_len)
 };
 
 struct PartialParams {
@@ -82,7 +84,9 @@ struct PartialParams {
 struct Unit {
   int b, so, s, g;
   int L;            // context length of request b
-  int rows;         // valid query rows in this group (<= 64, multiple of 16)
+  int qn;           // query tokens of request b (rows i >= qn are padding)
+  int rows;         // query rows of this group that attend (multiple of 16)
+  int rows_out;     // rows of this group in the output (<= 64)
   int tiles;        // pipeline tiles
   int tstart, tend; // contiguous layout: global token range of the shard
   int p0;           // contiguous layout, global cache: first page slot
@@ -98,12 +102,15 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
   x.b = bs / pd.n_out;
   x.s = pd.shard_first + x.so;
   x.L = pd.seq_lens[x.b];
+  x.qn = pd.q_lens ? min(max(pd.q_lens[x.b], 0), pd.q_len) : pd.q_len;
   int r0 = x.g * kRows;
-  x.rows = min(kRows, pd.R - r0);
+  x.rows_out = min(kRows, pd.R - r0);
+  x.rows = min(max(x.qn * pd.H - r0, 0), x.rows_out);
   x.tstart = 0;
   x.tend = 0;
   x.p0 = 0;
   int L = x.L > 0 ? x.L : 0;
+  if (x.rows == 0) L = 0;   // only padding rows: nothing to attend
   if (pd.layout == kInterleaved) {
     int n_local = L > x.s ? (L - 1 - x.s) / pd.num_shards + 1 : 0;
     x.tiles = ceil_div(n_local, kTile);
@@ -145,7 +152,7 @@ __device__ __forceinline__ bool tile_full(const ProblemDesc& pd, const Unit& x, 
   bool ok = slot_valid(pd, x, first) && slot_valid(pd, x, last);
   if (pd.causal) {
     int i_min = (x.g * kRows) / pd.H;  // smallest query position in the group
-    ok = ok && last <= x.L - pd.q_len + i_min;
+    ok = ok && last <= x.L - x.qn + i_min;
   }
   return ok;
 }

@@ -461,15 +461,18 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         ok = __all_sync(0xffffffffu, ok && mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
         if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
         uint4* q4 = reinterpret_cast<uint4*>(smem + kSmemQ);
+        const int rows_q = make_unit(pd, unit).rows;   // padding rows may hold anything
         bool big = false;
 #pragma unroll 4
         for (int i = ct; i < kTileBytes / 16; i += kConvThreads) {
           uint4 v = q4[i];
-          v.x = bf16x2_to_f16x2(v.x, big);
-          v.y = bf16x2_to_f16x2(v.y, big);
-          v.z = bf16x2_to_f16x2(v.z, big);
-          v.w = bf16x2_to_f16x2(v.w, big);
+          bool b = false;
+          v.x = bf16x2_to_f16x2(v.x, b);
+          v.y = bf16x2_to_f16x2(v.y, b);
+          v.z = bf16x2_to_f16x2(v.z, b);
+          v.w = bf16x2_to_f16x2(v.w, b);
           q4[i] = v;
+          big |= b && ((i % (kChunkBytes / 16)) / 8 < rows_q);   // [chunk][64 rows][8 x 16 B]
         }
         if (big) atomicOr(&p.hdr->err, kErrQRange);
         fence_proxy_async_smem();
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       Unit x = make_unit(pd, unit);
       const bool owner = r < x.rows;
       const int i_row = (x.g * kRows + r) / pd.H;           // query position of row r
-      const int vis_limit = x.L - pd.q_len + i_row;          // causal: t <= vis_limit
+      const int vis_limit = x.L - x.qn + i_row;              // causal: t <= vis_limit
       float m_run = -CUDART_INF_F, l_run = 0.0f;             // l_run: this half's sum
       for (int j = t0; j < t1; ++j, ++gt) {
         const int sb = gt & 1;
@@ -693,6 +696,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                                    : -CUDART_INF_F;
         misc->inv_l[r] = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
         dst_lse[r] = lse;
+      }
+      if (whole) {
+        // padding rows of a request with fewer query tokens: o = 0, lse = -inf
+        // (pieces of a split unit leave them to the merge kernel)
+        for (int e = tid; e < (x.rows_out - x.rows) * (kDv / 4); e += kSoftmaxThreads)
+          reinterpret_cast<float4*>(dst_o + (size_t)x.rows * kDv)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int rr = x.rows + tid; rr < x.rows_out; rr += kSoftmaxThreads)
+          dst_lse[rr] = -CUDART_INF_F;
       }
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       // O^T block k/2, rows 32*(k%2).. of this thread's latent dim, two TMEM

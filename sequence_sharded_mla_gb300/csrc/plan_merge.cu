@@ -21,8 +21,14 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
                                                         int grid, int min_tiles,
                                                         int unit_cost) {
   __shared__ int part[1024];
+  __shared__ unsigned bad_qlen;
   const int U = pd.B * pd.n_out * pd.G;
   const int tid = threadIdx.x;
+  if (tid == 0) bad_qlen = 0;
+  __syncthreads();
+  if (pd.q_lens != nullptr)
+    for (int b = tid; b < pd.B; b += 1024)
+      if (pd.q_lens[b] < 1 || pd.q_lens[b] > pd.q_len) atomicOr(&bad_qlen, kErrQLens);
   const int per_thread = ceil_div(U, 1024);
   const int u0 = tid * per_thread, u1 = min(U, u0 + per_thread);
   int sum = 0;
@@ -48,7 +54,7 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
   if (tid == 1023) {
     const int W = part[1023];
     prefix[U] = W;
-    hdr->err = 0;
+    hdr->err = bad_qlen;
     hdr->total_cost = W;
     hdr->per_cta = max(min_tiles, ceil_div(W, grid));
     hdr->grid = grid;
@@ -71,17 +77,21 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   const Unit x = make_unit(pd, u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kMergeRowsPerBlock + warp;
-  if (r >= x.rows) return;
+  if (r >= x.rows_out) return;
   const int ps = prefix[u], ue = prefix[u + 1];
   const int us = unit_tile_start(prefix, u, hdr->unit_cost);
   const size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
   float4* dst = reinterpret_cast<float4*>(out_partial + (row0 + r) * kDv);
-  if (us == ue) {  // the shard holds no token of this request
+  const int per = hdr->per_cta;
+  const bool split = us < ue && us / per != (ue - 1) / per;
+  // rows with no token to see: the shard holds none of the request's
+  // positions, or the row is padding of a request with fewer query tokens
+  // (a whole unit's padding rows are written by the partial kernel)
+  if (us == ue || (split && r >= x.rows)) {
     for (int v = lane; v < kDv / 4; v += 32) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane == 0) lse_partial[row0 + r] = -CUDART_INF_F;
     return;
   }
-  const int per = hdr->per_cta;
   const int c0 = us / per, c1 = (ue - 1) / per;
   if (c0 == c1) return;  // written directly by the partial kernel
   const int np = c1 - c0 + 1;

@@ -72,10 +72,10 @@ def exchange_head_slices(o: torch.Tensor, lse: torch.Tensor, group=None):
 
 
 def _cuda_partial(q_full, kv, block_table, seq_lens, num_shards, layout, shard_id, kv_scale,
-                  causal, softmax_scale):
+                  causal, softmax_scale, q_lens=None):
     o, lse, _ = mla_decode_partial(q_full, kv, block_table, seq_lens, num_shards,
                                    layout + "_local", shard_id=shard_id, kv_scale=kv_scale,
-                                   causal=causal, softmax_scale=softmax_scale)
+                                   causal=causal, softmax_scale=softmax_scale, q_lens=q_lens)
     return o[0], lse[0]
 
 
@@ -88,7 +88,8 @@ def dcp_decode_step(q_local: torch.Tensor, kv: torch.Tensor, block_table: torch.
                     seq_lens: torch.Tensor, *, group=None, layout: str = "interleaved",
                     kv_scale: Optional[torch.Tensor] = None, causal: bool = False,
                     softmax_scale: float = DEFAULT_SCALE, w_uv_local: Optional[torch.Tensor] = None,
-                    partial_fn: Optional[Callable] = None, combine_fn: Optional[Callable] = None):
+                    q_lens: Optional[torch.Tensor] = None, partial_fn: Optional[Callable] = None,
+                    combine_fn: Optional[Callable] = None):
     """One sharded decode step of attention on this rank.
 
     q_local: bf16 [B, q_len, H/N, 576], this rank's query heads.
@@ -96,6 +97,7 @@ def dcp_decode_step(q_local: torch.Tensor, kv: torch.Tensor, block_table: torch.
     latent cache (shard `rank` of N under `layout`, stored compactly: see
     mla_layout's *_LOCAL layouts).  seq_lens: the global lengths [B].
     w_uv_local: bf16 [H/N, 512, 128], W_UV of this rank's heads, or None.
+    q_lens: optional int32 [B] query tokens per request of a padded batch.
     Returns (out [B, q_len, H/N, 512 | 128] bf16, lse [B, q_len, H/N] fp32).
 
     partial_fn / combine_fn replace the library's CUDA calls (same arguments
@@ -106,6 +108,6 @@ def dcp_decode_step(q_local: torch.Tensor, kv: torch.Tensor, block_table: torch.
     combine_fn = combine_fn or _cuda_combine
     q_full = gather_query_heads(q_local, group)
     o, lse = partial_fn(q_full, kv, block_table, seq_lens, N, layout, rank, kv_scale, causal,
-                        softmax_scale)
+                        softmax_scale, q_lens)
     partials, lses = exchange_head_slices(o, lse, group)
     return combine_fn(partials, lses, w_uv_local, causal, softmax_scale)

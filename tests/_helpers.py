@@ -32,7 +32,8 @@ def to_device(w, dev):
     wuv = None
     if w.w_uv is not None:
         wuv = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16).to(dev)
-    return dict(q=q, kv=kv, kv_scale=sc, block_table=bt, seq_lens=sl, w_uv=wuv)
+    ql = None if w.q_lens is None else torch.from_numpy(w.q_lens).to(dev)
+    return dict(q=q, kv=kv, kv_scale=sc, block_table=bt, seq_lens=sl, w_uv=wuv, q_lens=ql)
 
 
 def run_gpu(w, dev, shard_id=-1, num_shards=None, layout=None, with_wuv=True):
@@ -43,7 +44,8 @@ def run_gpu(w, dev, shard_id=-1, num_shards=None, layout=None, with_wuv=True):
     lay = w.layout if layout is None else layout
     part, lse, ws = mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], N,
                                            lay, shard_id=shard_id, kv_scale=t["kv_scale"],
-                                           causal=w.causal, softmax_scale=w.softmax_scale)
+                                           causal=w.causal, softmax_scale=w.softmax_scale,
+                                           q_lens=t["q_lens"])
     res = {"partial": part, "lse_partial": lse, "workspace": ws}
     if shard_id == -1:
         out, lse_out = mla.mla_shard_combine(part, lse, causal=w.causal,

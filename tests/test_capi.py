@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
     L = mla.lib()
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert mla.mla_version() == 100
+    assert mla.mla_version() == 200
     assert mla.mla_status_string(-5) == "block-table entry out of range"
 
 

@@ -53,7 +53,8 @@ def _worker(rank, world, port, layout, causal, wuv, out):
                 rank * Hl:(rank + 1) * Hl].contiguous()
         seen = {}
 
-        def partial_fn(q_full, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale):
+        def partial_fn(q_full, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
+                       q_lens=None):
             seen["q"] = q_full
             assert N == world and shard_id == rank and lay == layout and causal_ == causal
             assert kv_ is kv and bt_ is bt and sl_ is sl

@@ -236,3 +236,52 @@ def test_local_shard_caches(dev, layout, N, kv_dtype):
     ref, ref_lse, _ = oracle.reference_step(w)
     check_close(bf16_to_np(out).reshape(rows, 512), ref, TOL_OUT, "out", rel=REL_OUT)
     check_close(lse_out.cpu().numpy().reshape(rows), ref_lse, TOL_LSE, "lse")
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_variable_query_counts(dev, layout, causal):
+    """A padded batch of verify steps with different draft counts: rows past
+    a request's count are padding (o = 0, lse = -inf); the causal mask uses
+    each request's own count.  32 heads x q_len 9 = 288 rows, so groups of
+    64 rows end inside requests' padding."""
+    lens = [1, 300, 5000, 64, 2222]
+    w = mi.build_workload("qlens", len(lens), 9, 32, lens, 2, layout, "bf16", causal,
+                          seed=460, poison=True, q_lens=[1, 9, 4, 2, 7])
+    compare_all(w, dev)
+
+
+def test_variable_query_counts_fp8_local_and_wuv(dev):
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    lens = [700, 65, 3000]
+    w = mi.build_workload("qlens8", len(lens), 4, 48, lens, 4, "interleaved", "fp8", True,
+                          seed=470, kv_sigma=1.0, with_w_uv=True, q_lens=[4, 1, 3])
+    compare_all(w, dev)
+    from _helpers import to_device
+    t = to_device(w, dev)
+    rows = w.batch * w.q_len * w.num_heads
+    for s in range(3):
+        d = mi.local_shard_cache(w, 3, s, "interleaved", seed=s)
+        part, lse, ws = mla.mla_decode_partial(
+            t["q"], torch.from_numpy(d["kv"]).to(dev), torch.from_numpy(d["block_table"]).to(dev),
+            t["seq_lens"], 3, "interleaved_local", shard_id=s,
+            kv_scale=torch.from_numpy(d["kv_scale"]).to(dev), causal=True, q_lens=t["q_lens"])
+        torch.cuda.synchronize()
+        assert mla.mla_get_device_error(ws) == 0
+        ro, rl = oracle.attend(w, shard=s, num_shards=3, layout="interleaved")
+        check_close(part.cpu().numpy().reshape(rows, 512), ro, TOL_OUT, f"shard {s}", rel=REL_OUT)
+        check_close(lse.cpu().numpy().reshape(rows), rl, TOL_LSE, f"lse {s}")
+
+
+def test_query_count_out_of_range_is_reported(dev):
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    w = mi.build_workload("qbad", 2, 3, 16, [100, 200], 2, "interleaved", "bf16", True, seed=480,
+                          q_lens=[3, 4])
+    res = run_gpu(w, dev)
+    assert res["status"] == -1           # MLA_ERR_INVALID: 4 > q_len
+    assert mla.mla_get_device_error(res["workspace"]) == 0
+    w.q_lens = np.array([0, 2], dtype=np.int32)
+    res = run_gpu(w, dev)
+    assert res["status"] == -1
