@@ -12,6 +12,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
@@ -32,6 +33,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
                                                           int num_shards, int rows,
                                                           uint16_t* __restrict__ out,
                                                           float* __restrict__ lse_out) {
+  griddep_wait();                // the partials
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
     uint16_t* __restrict__ y, float* __restrict__ lse_out) {
   __shared__ float so[kWuvRowsPerPass][kDv];
   __shared__ float red[4][kWuvRowsPerPass][64];
+  griddep_wait();                // the partials
   const int h = blockIdx.x, jb = blockIdx.y;
   const int tid = threadIdx.x;
   const int rows = rows_per_head_group * H;
@@ -160,18 +163,29 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
 
 cudaError_t launch_combine(const float* partials, const float* lses, int num_shards, int rows,
                            uint16_t* out, float* lse_out, cudaStream_t stream) {
-  mla_combine_kernel<<<ceil_div(rows, 8), 256, 0, stream>>>(partials, lses, num_shards, rows, out,
-                                                            lse_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ceil_div(rows, 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, partials, lses, num_shards, rows, out,
+                            lse_out);
 }
 
 cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
                                int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
                                float* lse_out, cudaStream_t stream) {
-  dim3 grid(H, kDuv / 64);
-  mla_combine_wuv_kernel<<<grid, 256, 0, stream>>>(partials, lses, num_shards,
-                                                   rows_per_head_group, H, w_uv, y, lse_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H, kDuv / 64);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_wuv_kernel, partials, lses, num_shards,
+                            rows_per_head_group, H, w_uv, y, lse_out);
 }
 
 }  // namespace mla

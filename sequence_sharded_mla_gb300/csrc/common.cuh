@@ -94,6 +94,16 @@ struct Unit {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Launch attribute for programmatic dependent launch: the kernel may be
+// scheduled while the previous kernel on the stream finishes; it waits for
+// that kernel's results with griddep_wait().
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
   Unit x;
   x.g = u % pd.G;

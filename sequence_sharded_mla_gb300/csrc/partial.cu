@@ -183,6 +183,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   Misc* misc = reinterpret_cast<Misc*>(smem + kSmemMisc);
   const ProblemDesc& pd = p.pd;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();                // the planning kernel's work list
+  griddep_launch_dependents();
 
   const int W = p.hdr->total_cost, per = p.hdr->per_cta;
   const int lo = blockIdx.x * per;
@@ -778,9 +780,15 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  mla_partial_kernel<kFp8><<<grid, kFp8 ? kThreadsFp8 : kThreads, kSmemBytes, stream>>>(tm_q, tm_kv,
-                                                                                       p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFp8 ? kThreadsFp8 : kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kFp8>, tm_q, tm_kv, p);
 }
 
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,

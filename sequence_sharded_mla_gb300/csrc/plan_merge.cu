@@ -14,12 +14,14 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
 __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader* hdr, int* prefix,
                                                         int grid, int min_tiles,
                                                         int unit_cost) {
+  griddep_launch_dependents();   // the partial kernel may start launching
   __shared__ int part[1024];
   __shared__ unsigned bad_qlen;
   const int U = pd.B * pd.n_out * pd.G;
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
     ProblemDesc pd, const WsHeader* hdr, const int* prefix, const float* ws_o,
     const float* ws_lse, float* out_partial, float* lse_partial) {
   __shared__ float wts[kMergeRowsPerBlock][kMaxPieces];
+  griddep_wait();                // the partial kernel's pieces and outputs
+  griddep_launch_dependents();
   const int u = blockIdx.x;
   const Unit x = make_unit(pd, u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -145,10 +149,15 @@ cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int g
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
                          const float* ws_o, const float* ws_lse, float* out_partial,
                          float* lse_partial, int num_units, cudaStream_t stream) {
-  dim3 grid(num_units, kRows / kMergeRowsPerBlock);
-  mla_merge_kernel<<<grid, 32 * kMergeRowsPerBlock, 0, stream>>>(pd, hdr, prefix, ws_o, ws_lse,
-                                                                 out_partial, lse_partial);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_units, kRows / kMergeRowsPerBlock);
+  cfg.blockDim = dim3(32 * kMergeRowsPerBlock);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel, pd, hdr, prefix, ws_o, ws_lse, out_partial,
+                            lse_partial);
 }
 
 }  // namespace mla

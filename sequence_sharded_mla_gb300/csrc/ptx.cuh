@@ -18,6 +18,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on the stream still runs; it must call griddep_wait()
+// before touching anything that kernel writes (or reads).  A kernel launched
+// without the attribute returns from griddep_wait() at once.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream begin launching (its griddep_wait()
+// still waits for this whole grid to finish and flush).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
