@@ -104,6 +104,14 @@ inline cudaLaunchAttribute pdl_attribute() {
   return a;
 }
 
+// kLocal: whether the cache is a local slice (pd.local), fixed at compile time
+// (0 or 1) in the partial kernel, read at run time (-1) elsewhere.
+template <int kLocal>
+__device__ __forceinline__ bool is_local(const ProblemDesc& pd) {
+  return kLocal < 0 ? pd.local != 0 : kLocal != 0;
+}
+
+template <int kLocal = -1>
 __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
   Unit x;
   x.g = u % pd.G;
@@ -130,7 +138,7 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
     x.tend = min(x.tstart + c, L);
     if (x.tstart >= x.tend) {
       x.tiles = 0;
-    } else if (pd.local) {
+    } else if (is_local<kLocal>(pd)) {
       x.tiles = ceil_div(x.tend - x.tstart, kTile);
     } else {
       x.p0 = x.tstart / kPage;
@@ -144,9 +152,10 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
 // shards: tile j holds the shard's positions 64j..64j+63 (in a local cache,
 // exactly local page j).  Contiguous shards: tile j is global page p0 + j, or
 // local page j of a local cache.
+template <int kLocal = -1>
 __device__ __forceinline__ int slot_token(const ProblemDesc& pd, const Unit& x, int j, int a) {
   if (pd.layout == kInterleaved) return (j * kTile + a) * pd.num_shards + x.s;
-  if (pd.local) return x.tstart + j * kTile + a;
+  if (is_local<kLocal>(pd)) return x.tstart + j * kTile + a;
   return (x.p0 + j) * kPage + a;
 }
 
@@ -157,8 +166,9 @@ __device__ __forceinline__ bool slot_valid(const ProblemDesc& pd, const Unit& x,
 
 // True when every slot of tile j is a valid token visible to every query row
 // of the unit (no masking needed).
+template <int kLocal = -1>
 __device__ __forceinline__ bool tile_full(const ProblemDesc& pd, const Unit& x, int j) {
-  int first = slot_token(pd, x, j, 0), last = slot_token(pd, x, j, kTile - 1);
+  int first = slot_token<kLocal>(pd, x, j, 0), last = slot_token<kLocal>(pd, x, j, kTile - 1);
   bool ok = slot_valid(pd, x, first) && slot_valid(pd, x, last);
   if (pd.causal) {
     int i_min = (x.g * kRows) / pd.H;  // smallest query position in the group
