@@ -55,11 +55,17 @@ def test_ragged_lengths(dev, H, layout):
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
 def test_shard_counts(dev, N, layout):
-    if layout == "interleaved" and 64 % N != 0:
-        pytest.skip("interleaved layout needs N | 64")
     lens = [5, 700, 2049, 130]
     w = mi.build_workload("shards", len(lens), 1, 32, lens, N, layout, "bf16", False,
                           seed=200 + N)
+    if layout == "interleaved" and 64 % N != 0:
+        # a whole-request cache interleaved over N shards needs N | 64 (one
+        # TMA box per page); such calls are refused before any launch
+        import sequence_sharded_mla_gb300 as mla
+        with pytest.raises(mla.MLAError) as e:
+            run_gpu(w, dev)
+        assert e.value.status == -2
+        return
     compare_all(w, dev)
 
 
