@@ -339,6 +339,87 @@ def local_shard_cache(w: Workload, num_shards: int, shard: int, layout: str, see
     return dict(kv=kv, kv_scale=kv_scale, block_table=bt, local_lens=local_lens)
 
 
+@dataclass
+class GqaWorkload:
+    """A grouped-query-attention decode batch: Hkv KV heads of width D shared
+    by groups of H / Hkv consecutive query heads, separate K and V caches."""
+    name: str
+    batch: int
+    q_len: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    seq_lens: np.ndarray               # int32 [B]
+    num_shards: int
+    layout: str
+    causal: bool
+    seed: int
+    q: np.ndarray = None               # uint16 (bf16 bits) [B, q_len, H, D]
+    k_cache: np.ndarray = None         # uint16 [P, 64, Hkv, D]
+    v_cache: np.ndarray = None         # uint16 [P, 64, Hkv, D]
+    block_table: np.ndarray = None     # int32 [B, max_pages]
+    softmax_scale: float = 0.0
+
+    @property
+    def num_pages(self):
+        return self.k_cache.shape[0]
+
+    @property
+    def total_tokens(self):
+        return int(np.sum(self.seq_lens.astype(np.int64)))
+
+    def kv_bytes(self):
+        """K and V bytes one full pass reads: every token < L_b once, all KV
+        heads (2 * Hkv * D bf16 values per token)."""
+        return self.total_tokens * 2 * self.num_kv_heads * self.head_dim * 2
+
+
+def build_gqa_workload(name, batch, q_len, num_heads, num_kv_heads, head_dim, seq_lens,
+                       num_shards, layout, causal, seed, q_sigma=0.5, kv_sigma=0.5,
+                       extra_pages=0, poison=False, pinned=False):
+    """Generate a GQA batch.  Pages are scattered by a seeded permutation of
+    the pool as for the latent cache; ``poison`` fills rows past each
+    request's end and unreferenced pages with NaN."""
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    assert seq_lens.shape == (batch,) and num_heads % num_kv_heads == 0
+    pages_per = (seq_lens.astype(np.int64) + PAGE - 1) // PAGE
+    P = int(pages_per.sum()) + extra_pages
+    perm = permutation(seed, S_PERM, max(P, 1))
+    bt = np.full((batch, max(1, int(pages_per.max()))), -1, dtype=np.int32)
+    off = 0
+    for b in range(batch):
+        n = int(pages_per[b])
+        bt[b, :n] = perm[off:off + n]
+        off += n
+
+    def alloc(shape):
+        if pinned:
+            import torch
+            return torch.empty(shape, dtype=torch.int16, pin_memory=True).numpy().view(np.uint16)
+        return np.empty(shape, dtype=np.uint16)
+
+    D, Hkv = head_dim, num_kv_heads
+    q = alloc((batch, q_len, num_heads, D))
+    normal_bf16(seed, S_Q, q.shape, q_sigma, out=q)
+    k = alloc((max(P, 1), PAGE, Hkv, D))
+    normal_bf16(seed, S_KV, k.shape, kv_sigma, out=k)
+    v = alloc((max(P, 1), PAGE, Hkv, D))
+    normal_bf16(seed, S_KV + 10, v.shape, kv_sigma, out=v)
+    if poison:
+        used = np.zeros((max(P, 1), PAGE), dtype=bool)
+        for b in range(batch):
+            L = int(seq_lens[b])
+            for kk in range(int(pages_per[b])):
+                used[bt[b, kk], :min(PAGE, L - kk * PAGE)] = True
+        k[~used] = 0x7FC0
+        v[~used] = 0x7FC0
+    return GqaWorkload(name=name, batch=batch, q_len=q_len, num_heads=num_heads,
+                       num_kv_heads=Hkv, head_dim=D, seq_lens=seq_lens,
+                       num_shards=num_shards, layout=layout, causal=causal, seed=seed, q=q,
+                       k_cache=k, v_cache=v, block_table=bt,
+                       softmax_scale=1.0 / math.sqrt(D))
+
+
 CONFIG_NAMES = {
     1: "tiny-b1-h16-l1024-n2-interleaved",
     2: "bimodal-agentic-b32-h64-n4-interleaved",

@@ -27,7 +27,10 @@ def lib():
         L.oracle_attend.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, vp,
                                     i32, dbl, i32, i32, i32, vp, i64, vp, vp]
         L.oracle_attend.restype = i32
-        L.oracle_lse_merge.argtypes = [vp, vp, i32, i64, vp, vp]
+        L.oracle_gqa_attend.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32, vp,
+                                        i32, dbl, i32, i32, i32, vp, i64, vp, vp]
+        L.oracle_gqa_attend.restype = i32
+        L.oracle_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, vp]
         L.oracle_lse_merge.restype = None
         L.oracle_project_wuv.argtypes = [vp, vp, vp, i64, vp]
         L.oracle_project_wuv.restype = None
@@ -94,14 +97,39 @@ def attend(w, shard=-1, num_shards=None, layout=None, rows=None, q=None, seq_len
     return out, lse
 
 
+def gqa_attend(w, shard=-1, num_shards=None, layout=None, rows=None):
+    """(out [n, D] fp64, lse [n] fp64) for query rows of GQA workload ``w``
+    (rows = (b * q_len + i) * H + h; None = all)."""
+    B, q_len, H, D = w.q.shape
+    seq_lens = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+    bt = np.ascontiguousarray(w.block_table, dtype=np.int32)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows.size
+    else:
+        n = B * q_len * H
+    out = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    ns = num_shards if num_shards is not None else w.num_shards
+    lay = LAYOUTS[layout if layout is not None else w.layout]
+    st = lib().oracle_gqa_attend(_p(w.q), B, q_len, H, w.num_kv_heads, D, _p(w.k_cache),
+                                 _p(w.v_cache), w.k_cache.shape[0], _p(bt), bt.shape[1],
+                                 _p(seq_lens), int(w.causal), float(w.softmax_scale), int(shard),
+                                 int(ns), lay, _p(rows), n, _p(out), _p(lse))
+    if st != 0:
+        raise RuntimeError(f"oracle_gqa_attend failed with status {st}")
+    return out, lse
+
+
 def lse_merge(outs, lses):
-    """Merge shard partials: outs [N, rows, 512], lses [N, rows] (fp64)."""
+    """Merge shard partials: outs [N, rows, dim], lses [N, rows] (fp64)."""
     outs = np.ascontiguousarray(outs, dtype=np.float64)
     lses = np.ascontiguousarray(lses, dtype=np.float64)
     N, rows = lses.shape
-    out = np.zeros((rows, D_V), dtype=np.float64)
+    dim = outs.shape[-1]
+    out = np.zeros((rows, dim), dtype=np.float64)
     lse = np.zeros((rows,), dtype=np.float64)
-    lib().oracle_lse_merge(_p(outs), _p(lses), N, rows, _p(out), _p(lse))
+    lib().oracle_lse_merge(_p(outs), _p(lses), N, rows, dim, _p(out), _p(lse))
     return out, lse
 
 

@@ -220,9 +220,99 @@ int oracle_attend(const uint16_t* q, int B, int q_len, int H, const void* kv,
   return status;
 }
 
+/* Row of token t of request b for KV head kh in a GQA cache, or NULL if the
+ * block-table entry is missing or out of range. */
+static const uint16_t* gqa_row(const uint16_t* cache, const int32_t* block_table, int max_pages,
+                               int num_pages, int Hkv, int D, int b, int kh, long t) {
+  long slot = t / PAGE;
+  if (slot >= max_pages) return NULL;
+  int32_t page = block_table[(size_t)b * max_pages + slot];
+  if (page < 0 || page >= num_pages) return NULL;
+  return cache + (((size_t)page * PAGE + (size_t)(t % PAGE)) * Hkv + kh) * D;
+}
+
+/*
+ * Grouped-query attention (GQA) over a paged cache, the second backend of
+ * "Decode Context Parallelism" (section 5.4): the cache stores Hkv KV heads
+ * of width D, separate K and V,
+ *   k_cache, v_cache: bf16 [num_pages][64][Hkv][D],
+ * and query head h attends with KV head h / (H / Hkv) -- the KV heads are
+ * broadcast over their groups of H / Hkv consecutive query heads.  Token
+ * sets, sharding, causal masking and the two-pass softmax are those of
+ * oracle_attend; rows r = (b * q_len + i) * H + h, out [n_rows][D].
+ */
+int oracle_gqa_attend(const uint16_t* q, int B, int q_len, int H, int Hkv, int D,
+                      const uint16_t* k_cache, const uint16_t* v_cache, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                      int causal, double softmax_scale, int shard, int nshards, int layout,
+                      const int64_t* rows, int64_t n_rows, double* out, double* lse) {
+  if (B <= 0 || q_len <= 0 || H <= 0 || Hkv <= 0 || D <= 0 || H % Hkv != 0)
+    return ORACLE_BAD_ARG;
+  if (shard >= 0 && (nshards <= 0 || shard >= nshards)) return ORACLE_BAD_ARG;
+  const int group = H / Hkv;
+  int64_t total = (int64_t)B * q_len * H;
+  if (rows == NULL) n_rows = total;
+  int status = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t k = 0; k < n_rows; ++k) {
+    int64_t r = rows ? rows[k] : k;
+    int h = (int)(r % H);
+    int i = (int)((r / H) % q_len);
+    int b = (int)(r / ((int64_t)H * q_len));
+    int kh = h / group;
+    long L = seq_lens[b];
+    double* o = out + (size_t)k * D;
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    if (!qv || !s) {
+      free(qv);
+      free(s);
+#pragma omp atomic write
+      status = ORACLE_NOMEM;
+      continue;
+    }
+    const uint16_t* qrow = q + (size_t)r * D;
+    for (int d = 0; d < D; ++d) qv[d] = bf16_value(qrow[d]);
+    double m = -INFINITY;
+    int bad = 0;
+    for (long t = 0; t < L; ++t) {
+      if (!token_visible(t, L, q_len, i, causal, shard, nshards, layout)) continue;
+      const uint16_t* kr = gqa_row(k_cache, block_table, max_pages, num_pages, Hkv, D, b, kh, t);
+      if (!kr) { bad = 1; break; }
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += qv[d] * bf16_value(kr[d]);
+      s[t] = softmax_scale * acc;
+      if (s[t] > m) m = s[t];
+    }
+    if (bad) {
+#pragma omp atomic write
+      status = ORACLE_BAD_PAGE;
+    } else if (m == -INFINITY) {
+      lse[k] = -INFINITY;
+    } else {
+      double z = 0.0;
+      for (long t = 0; t < L; ++t)
+        if (token_visible(t, L, q_len, i, causal, shard, nshards, layout)) z += exp(s[t] - m);
+      double l = m + log(z);
+      lse[k] = l;
+      for (long t = 0; t < L; ++t) {
+        if (!token_visible(t, L, q_len, i, causal, shard, nshards, layout)) continue;
+        const uint16_t* vr = gqa_row(v_cache, block_table, max_pages, num_pages, Hkv, D, b, kh, t);
+        double p = exp(s[t] - l);
+        for (int c = 0; c < D; ++c) o[c] += p * bf16_value(vr[c]);
+      }
+    }
+    free(qv);
+    free(s);
+  }
+  return status;
+}
+
 /* LSE merge of N shard partials.  outs: [N][rows][512], lses: [N][rows]. */
 void oracle_lse_merge(const double* outs, const double* lses, int nshards, int64_t rows,
-                      double* out, double* lse) {
+                      int dim, double* out, double* lse) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
     double M = -INFINITY;
@@ -230,8 +320,8 @@ void oracle_lse_merge(const double* outs, const double* lses, int nshards, int64
       double v = lses[(size_t)s * rows + r];
       if (v > M) M = v;
     }
-    double* o = out + (size_t)r * D_V;
-    for (int c = 0; c < D_V; ++c) o[c] = 0.0;
+    double* o = out + (size_t)r * dim;
+    for (int c = 0; c < dim; ++c) o[c] = 0.0;
     if (M == -INFINITY) {
       lse[r] = -INFINITY;
       continue;
@@ -240,10 +330,10 @@ void oracle_lse_merge(const double* outs, const double* lses, int nshards, int64
     for (int s = 0; s < nshards; ++s) {
       double w = exp(lses[(size_t)s * rows + r] - M);
       wsum += w;
-      const double* os = outs + ((size_t)s * rows + r) * D_V;
-      for (int c = 0; c < D_V; ++c) o[c] += w * os[c];
+      const double* os = outs + ((size_t)s * rows + r) * dim;
+      for (int c = 0; c < dim; ++c) o[c] += w * os[c];
     }
-    for (int c = 0; c < D_V; ++c) o[c] /= wsum;
+    for (int c = 0; c < dim; ++c) o[c] /= wsum;
     lse[r] = M + log(wsum);
   }
 }
