@@ -225,6 +225,63 @@ mla_status mla_get_device_error(void* workspace, void* stream);
  */
 mla_status mla_set_profile_events(void* before_partial, void* after_partial);
 
+/*
+ * Grouped-query attention (GQA) with the same sequence sharding ("Decode
+ * Context Parallelism", section 5.4, the GQA backend): the cache stores
+ * num_kv_heads KV heads of width head_dim in separate K and V caches, and
+ * query head h attends with KV head h / (num_heads / num_kv_heads) (each KV
+ * head broadcast over its group of consecutive query heads).
+ *
+ *   q            bf16  [B, q_len, H, D]
+ *   k, v         bf16  [num_pages, 64, Hkv, D]   (token t of request b at
+ *                                                 page block_table[b][t / 64],
+ *                                                 row t % 64)
+ *   out_partial  fp32  [n_out, B, q_len, H, D]
+ *   lse_partial  fp32  [n_out, B, q_len, H]
+ *   out          bf16  [B, q_len, H, D]
+ *
+ * This build supports head_dim = 128 and groups H / Hkv that are powers of
+ * two up to 64; layouts INTERLEAVED and CONTIGUOUS.  Everything else matches
+ * the MLA calls: logits scaled by softmax_scale (1/sqrt(D) for the workloads
+ * here), causal verify steps, shard_id / MLA_ALL_SHARDS, workspace, error
+ * reporting through mla_get_device_error, asynchronous on `stream`.
+ */
+typedef struct gqa_shape {
+  int batch;            /* B >= 1 */
+  int q_len;            /* query tokens per request >= 1 */
+  int num_heads;        /* H */
+  int num_kv_heads;     /* Hkv, divides H */
+  int head_dim;         /* D: 128 */
+  int causal;           /* 0 or 1 */
+  float softmax_scale;
+} gqa_shape;
+
+typedef struct gqa_kv_pages {
+  const void* k;        /* bf16 [num_pages, page_size, Hkv, D] */
+  const void* v;        /* bf16 [num_pages, page_size, Hkv, D] */
+  int num_pages;        /* >= 1 */
+  int page_size;        /* must be 64 */
+} gqa_kv_pages;
+
+/* Workspace bytes gqa_decode_partial needs (0 for invalid or unsupported shapes). */
+size_t gqa_workspace_size(const gqa_shape* shape, int num_shards, int shard_id);
+
+/* Per-shard partial GQA attention: for every request b, query row (i, h) and
+ * computed shard s, over the shard's visible tokens T_s:
+ *   s_t = softmax_scale * q[b,i,h,:] . K_t[kh,:],  kh = h / (H / Hkv)
+ *   lse_partial = ln sum exp(s_t)  (-inf if empty);
+ *   out_partial = sum exp(s_t - lse) V_t[kh,:]  (0 if empty). */
+mla_status gqa_decode_partial(const void* q, const gqa_kv_pages* kv, const int32_t* block_table,
+                              int max_pages_per_req, const int32_t* seq_lens,
+                              const gqa_shape* shape, int shard_id, int num_shards,
+                              mla_layout layout, float* out_partial, float* lse_partial,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* LSE combine of N GQA shard partials (head_dim wide) into bf16 out
+ * [B, q_len, H, D] and lse_out (may be NULL). */
+mla_status gqa_shard_combine(const float* partials, const float* lses, int num_shards,
+                             const gqa_shape* shape, void* out, float* lse_out, void* stream);
+
 /* Static description of a status code. */
 const char* mla_status_string(mla_status status);
 

@@ -420,6 +420,18 @@ def build_gqa_workload(name, batch, q_len, num_heads, num_kv_heads, head_dim, se
                        softmax_scale=1.0 / math.sqrt(D))
 
 
+GQA_CONFIG_NAME = "gqa-agentic-b32-h64-kv4-d128-n2"
+
+
+def config_gqa_workload(pinned=False):
+    """Grouped-query decode over the bimodal agentic length mix: 32 requests,
+    64 query heads sharing 4 KV heads of width 128 (groups of 16), bf16 K/V,
+    2 interleaved shards (the GQA backend's DCP degree is bounded by the
+    KV-head duplication factor)."""
+    return build_gqa_workload(GQA_CONFIG_NAME, 32, 1, 64, 4, 128, agentic_lengths(6, 32), 2,
+                              "interleaved", False, seed=6, pinned=pinned)
+
+
 CONFIG_NAMES = {
     1: "tiny-b1-h16-l1024-n2-interleaved",
     2: "bimodal-agentic-b32-h64-n4-interleaved",

@@ -44,10 +44,22 @@ class mla_kv_pages(ctypes.Structure):
                 ("num_pages", ctypes.c_int), ("page_size", ctypes.c_int)]
 
 
+class gqa_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("num_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+class gqa_kv_pages(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("page_size", ctypes.c_int)]
+
+
 _LIB = None
 EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
            "mla_workspace_size", "mla_get_device_error", "mla_set_profile_events",
-           "mla_status_string", "mla_version")
+           "mla_status_string", "mla_version", "gqa_workspace_size", "gqa_decode_partial",
+           "gqa_shard_combine")
 
 
 def lib():
@@ -77,6 +89,14 @@ def lib():
         L.mla_status_string.restype = ctypes.c_char_p
         L.mla_version.argtypes = []
         L.mla_version.restype = i32
+        L.gqa_workspace_size.argtypes = [ctypes.POINTER(gqa_shape), i32, i32]
+        L.gqa_workspace_size.restype = sz
+        L.gqa_decode_partial.argtypes = [vp, ctypes.POINTER(gqa_kv_pages), vp, i32, vp,
+                                         ctypes.POINTER(gqa_shape), i32, i32, i32, vp, vp, vp,
+                                         sz, vp]
+        L.gqa_decode_partial.restype = i32
+        L.gqa_shard_combine.argtypes = [vp, vp, i32, ctypes.POINTER(gqa_shape), vp, vp, vp]
+        L.gqa_shard_combine.restype = i32
         _LIB = L
     return _LIB
 
@@ -261,3 +281,79 @@ def mla_status_string(status: int) -> str:
 
 def mla_version() -> int:
     return int(lib().mla_version())
+
+
+# --------------------------------------------------------------------- GQA
+def _gqa_shape(batch, q_len, num_heads, num_kv_heads, head_dim, causal, softmax_scale):
+    return gqa_shape(int(batch), int(q_len), int(num_heads), int(num_kv_heads), int(head_dim),
+                     int(bool(causal)), float(softmax_scale))
+
+
+def gqa_workspace_size(batch, q_len, num_heads, num_kv_heads, num_shards,
+                       shard_id=ALL_SHARDS, head_dim=128, causal=False) -> int:
+    sh = _gqa_shape(batch, q_len, num_heads, num_kv_heads, head_dim, causal, 1.0)
+    return int(lib().gqa_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
+
+
+def gqa_decode_partial(q, k_cache, v_cache, block_table, seq_lens, num_shards,
+                       layout="interleaved", shard_id=ALL_SHARDS, causal=False,
+                       softmax_scale=None, out_partial=None, lse_partial=None, workspace=None,
+                       stream=None):
+    """Per-shard partial grouped-query attention; returns (out_partial, lse_partial, workspace).
+
+    q: bf16 [B, q_len, H, D]; k_cache, v_cache: bf16 [P, 64, Hkv, D];
+    block_table: int32 [B, max_pages]; seq_lens: int32 [B] (device).
+    out_partial: fp32 [n_out, B, q_len, H, D]; lse_partial: fp32 [n_out, B, q_len, H].
+    softmax_scale defaults to 1/sqrt(D).
+    """
+    _check(q, "q", (torch.bfloat16,), 4)
+    dev = q.device
+    B, q_len, H, D = q.shape
+    _check(k_cache, "k_cache", (torch.bfloat16,), 4, dev)
+    _check(v_cache, "v_cache", (torch.bfloat16,), 4, dev)
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("k_cache and v_cache must both be [P, 64, Hkv, D]")
+    Hkv = k_cache.shape[2]
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else softmax_scale
+    n_out = num_shards if shard_id == ALL_SHARDS else 1
+    if out_partial is None:
+        out_partial = torch.empty((n_out, B, q_len, H, D), dtype=torch.float32, device=dev)
+    if lse_partial is None:
+        lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
+    _check(out_partial, "out_partial", (torch.float32,), 5, dev)
+    _check(lse_partial, "lse_partial", (torch.float32,), 4, dev)
+    sh = _gqa_shape(B, q_len, H, Hkv, D, causal, scale)
+    need = int(lib().gqa_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    pages = gqa_kv_pages(k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape[0],
+                         k_cache.shape[1])
+    st = lib().gqa_decode_partial(_ptr(q), ctypes.byref(pages), _ptr(block_table),
+                                  block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
+                                  int(shard_id), int(num_shards), LAYOUTS[layout],
+                                  _ptr(out_partial), _ptr(lse_partial), _ptr(workspace),
+                                  workspace.numel(), _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "gqa_decode_partial")
+    return out_partial, lse_partial, workspace
+
+
+def gqa_shard_combine(partials, lses, out=None, lse_out=None, stream=None):
+    """LSE combine of GQA shard partials fp32 [N, B, q_len, H, D] -> bf16
+    [B, q_len, H, D] and fp32 lse [B, q_len, H]."""
+    _check(partials, "partials", (torch.float32,), 5)
+    dev = partials.device
+    N, B, q_len, H, D = partials.shape
+    _check(lses, "lses", (torch.float32,), 4, dev)
+    if out is None:
+        out = torch.empty((B, q_len, H, D), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    sh = _gqa_shape(B, q_len, H, 1, D, False, 1.0)
+    st = lib().gqa_shard_combine(_ptr(partials), _ptr(lses), int(N), ctypes.byref(sh), _ptr(out),
+                                 _ptr(lse_out), _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "gqa_shard_combine")
+    return out, lse_out

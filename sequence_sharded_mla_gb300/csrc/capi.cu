@@ -11,6 +11,7 @@
 
 #include "mla_dcp.h"
 #include "common.cuh"
+#include "host_util.h"
 
 namespace mla {
 int partial_smem_bytes();
@@ -41,32 +42,10 @@ constexpr int kMinTilesPerCta = 4;
 // refill, the epilogue's 128 KB of output): about two tiles' time.
 constexpr int kUnitCost = 2;
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-int device_sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
+using host::aligned16;
+using host::device_sm_count;
+using host::encode_fn;
+using host::EncodeTiledFn;
 
 struct WsLayout {
   size_t hdr, prefix, ws_o, ws_lse, total;
@@ -94,10 +73,6 @@ int units_for(const mla_shape* s, int num_shards, int shard_id) {
   int G = ceil_div(s->q_len * s->num_heads, kRows);
   return s->batch * n_out * G;
 }
-
-// Profiling events (cudaEvent_t) recorded around the partial-attention
-// kernel of every mla_decode_partial call while set.
-std::atomic<void*> g_ev_before{nullptr}, g_ev_after{nullptr};
 
 }  // namespace
 
@@ -261,8 +236,8 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, kUnitCost, st) != cudaSuccess) return MLA_ERR_CUDA;
-  void* ev0 = g_ev_before.load();
-  void* ev1 = g_ev_after.load();
+  void* ev0 = host::g_ev_before.load();
+  void* ev1 = host::g_ev_after.load();
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
     return MLA_ERR_CUDA;
   const cudaError_t le = fp8 ? launch_partial_fp8(tm_q, tm_kv, p, grid, st)
@@ -297,8 +272,8 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
 
 mla_status mla_set_profile_events(void* before_partial, void* after_partial) {
   if ((before_partial == nullptr) != (after_partial == nullptr)) return MLA_ERR_INVALID;
-  g_ev_before.store(before_partial);
-  g_ev_after.store(after_partial);
+  host::g_ev_before.store(before_partial);
+  host::g_ev_after.store(after_partial);
   return MLA_OK;
 }
 

@@ -94,6 +94,97 @@ struct Unit {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Walks the work pieces of one persistent CTA: the units whose tile positions
+// intersect the CTA's range [lo, hi) of work positions.
+struct PieceIter {
+  const int* prefix;
+  int U, lo, hi, pos, u, uc;
+  bool first;
+  __device__ void init(const int* pfx, int num_units, int lo_, int hi_, int unit_cost) {
+    prefix = pfx;
+    U = num_units;
+    lo = lo_;
+    hi = hi_;
+    pos = lo_;
+    uc = unit_cost;
+    first = true;
+    // last unit with prefix[u] <= lo
+    int a = 0, b = num_units - 1;
+    while (a < b) {
+      int m = (a + b + 1) >> 1;
+      if (prefix[m] <= lo_) a = m;
+      else b = m - 1;
+    }
+    u = a;
+  }
+  // Next piece: unit, tile range [t0, t1), whether it is the whole unit, and
+  // the workspace slot of a partial piece (0: the CTA's first piece, 1: its
+  // last).  Positions of a unit's fixed-cost part hold no tile.
+  __device__ bool next(int& unit, int& t0, int& t1, bool& whole, int& slot) {
+    while (pos < hi) {
+      while (u < U && prefix[u + 1] <= pos) ++u;
+      if (u >= U) return false;
+      const int ue = prefix[u + 1];
+      const int ts = unit_tile_start(prefix, u, uc);
+      const int a = max(pos, ts), b = min(hi, ue);
+      const int cur = u;
+      pos = b;
+      ++u;
+      if (a >= b) continue;
+      unit = cur;
+      t0 = a - ts;
+      t1 = b - ts;
+      whole = (a == ts) && (b == ue);
+      slot = first ? 0 : 1;
+      first = false;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Work plan over U units (one 1024-thread block): charges every unit with
+// tiles unit_cost extra positions, writes the exclusive prefix of positions
+// and the header (positions per CTA for `grid` persistent CTAs).
+template <class TilesFn>
+__device__ void plan_units(int U, TilesFn tiles_of, WsHeader* hdr, int* prefix, int grid,
+                           int min_tiles, int unit_cost, unsigned err_bits) {
+  __shared__ int part[1024];
+  const int tid = threadIdx.x;
+  const int per_thread = ceil_div(U, 1024);
+  const int u0 = tid * per_thread, u1 = min(U, u0 + per_thread);
+  auto cost = [&](int u) {
+    const int t = tiles_of(u);
+    return t > 0 ? t + unit_cost : 0;
+  };
+  int sum = 0;
+  for (int u = u0; u < u1; ++u) sum += cost(u);
+  part[tid] = sum;
+  __syncthreads();
+  // inclusive Hillis-Steele scan of the 1024 partial sums
+  for (int off = 1; off < 1024; off <<= 1) {
+    int v = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int run = part[tid] - sum;  // exclusive
+  for (int u = u0; u < u1; ++u) {
+    prefix[u] = run;
+    run += cost(u);
+  }
+  if (tid == 1023) {
+    const int W = part[1023];
+    prefix[U] = W;
+    hdr->err = err_bits;
+    hdr->total_cost = W;
+    hdr->per_cta = max(min_tiles, ceil_div(W, grid));
+    hdr->grid = grid;
+    hdr->num_units = U;
+    hdr->unit_cost = unit_cost;
+  }
+}
+
 // Launch attribute for programmatic dependent launch: the kernel may be
 // scheduled while the previous kernel on the stream finishes; it waits for
 // that kernel's results with griddep_wait().

@@ -107,53 +107,6 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256;
 
-struct PieceIter {
-  const int* prefix;
-  int U, lo, hi, pos, u, uc;
-  bool first;
-  __device__ void init(const int* pfx, int num_units, int lo_, int hi_, int unit_cost) {
-    prefix = pfx;
-    U = num_units;
-    lo = lo_;
-    hi = hi_;
-    pos = lo_;
-    uc = unit_cost;
-    first = true;
-    // last unit with prefix[u] <= lo
-    int a = 0, b = num_units - 1;
-    while (a < b) {
-      int m = (a + b + 1) >> 1;
-      if (prefix[m] <= lo_) a = m;
-      else b = m - 1;
-    }
-    u = a;
-  }
-  // Next piece: unit, tile range [t0, t1), whether it is the whole unit, and
-  // the workspace slot of a partial piece (0: the CTA's first piece, 1: its
-  // last).  Positions of a unit's fixed-cost part hold no tile.
-  __device__ bool next(int& unit, int& t0, int& t1, bool& whole, int& slot) {
-    while (pos < hi) {
-      while (u < U && prefix[u + 1] <= pos) ++u;
-      if (u >= U) return false;
-      const int ue = prefix[u + 1];
-      const int ts = unit_tile_start(prefix, u, uc);
-      const int a = max(pos, ts), b = min(hi, ue);
-      const int cur = u;
-      pos = b;
-      ++u;
-      if (a >= b) continue;
-      unit = cur;
-      t0 = a - ts;
-      t1 = b - ts;
-      whole = (a == ts) && (b == ue);
-      slot = first ? 0 : 1;
-      first = false;
-      return true;
-    }
-    return false;
-  }
-};
-
 __device__ __forceinline__ void set_error(PartialParams& p, Misc* misc, unsigned bits) {
   atomicOr(&p.hdr->err, bits);
   if (bits & kErrTimeout) *(volatile int*)&misc->abort = 1;

@@ -22,47 +22,15 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
                                                         int grid, int min_tiles,
                                                         int unit_cost) {
   griddep_launch_dependents();   // the partial kernel may start launching
-  __shared__ int part[1024];
   __shared__ unsigned bad_qlen;
-  const int U = pd.B * pd.n_out * pd.G;
-  const int tid = threadIdx.x;
-  if (tid == 0) bad_qlen = 0;
+  if (threadIdx.x == 0) bad_qlen = 0;
   __syncthreads();
   if (pd.q_lens != nullptr)
-    for (int b = tid; b < pd.B; b += 1024)
+    for (int b = threadIdx.x; b < pd.B; b += 1024)
       if (pd.q_lens[b] < 1 || pd.q_lens[b] > pd.q_len) atomicOr(&bad_qlen, kErrQLens);
-  const int per_thread = ceil_div(U, 1024);
-  const int u0 = tid * per_thread, u1 = min(U, u0 + per_thread);
-  int sum = 0;
-  auto cost = [&](int u) {
-    const int t = make_unit(pd, u).tiles;
-    return t > 0 ? t + unit_cost : 0;
-  };
-  for (int u = u0; u < u1; ++u) sum += cost(u);
-  part[tid] = sum;
   __syncthreads();
-  // inclusive Hillis-Steele scan of the 1024 partial sums
-  for (int off = 1; off < 1024; off <<= 1) {
-    int v = tid >= off ? part[tid - off] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
-  }
-  int run = part[tid] - sum;  // exclusive
-  for (int u = u0; u < u1; ++u) {
-    prefix[u] = run;
-    run += cost(u);
-  }
-  if (tid == 1023) {
-    const int W = part[1023];
-    prefix[U] = W;
-    hdr->err = bad_qlen;
-    hdr->total_cost = W;
-    hdr->per_cta = max(min_tiles, ceil_div(W, grid));
-    hdr->grid = grid;
-    hdr->num_units = U;
-    hdr->unit_cost = unit_cost;
-  }
+  plan_units(pd.B * pd.n_out * pd.G, [&](int u) { return make_unit(pd, u).tiles; }, hdr, prefix,
+             grid, min_tiles, unit_cost, bad_qlen);
 }
 
 // Block (u, y) handles query rows [4y, 4y + 4) of unit u, one warp per row:

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "mla_dcp.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, flags=re.M)
+    names = re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b((?:mla|gqa)_\w+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
