@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA sharded decode: KV HBM GB/s (% of ~8 TB/s peak), decode steps/s per layer"
 DEFAULT_CONFIG = 2     # the bimodal agentic batch the metric is quoted on
+GQA_CONFIG = 6         # the grouped-query backend on the same length mix
 
 
 def load_peaks():
@@ -197,18 +198,47 @@ def cpu_sample(w, budget_s, oracle):
     return kv_bytes, t_used, desc
 
 
+def gqa_cpu_sample(w, budget_s, oracle):
+    """The GQA oracle on whole requests (all heads, unsharded) until about
+    ``budget_s`` of CPU time; returns (K/V bytes covered, seconds, desc)."""
+    import numpy as np
+    order = np.argsort(w.seq_lens)
+    picked, t_used, kv_bytes = [], 0.0, 0
+    per = 2 * w.num_kv_heads * w.head_dim * 2
+    H, q_len = w.num_heads, w.q_len
+    for b in order[::max(1, len(order) // 8)]:
+        rows = np.arange(b * q_len * H, (b + 1) * q_len * H, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.gqa_attend(w, shard=-1, rows=rows)
+        t_used += time.perf_counter() - t0
+        picked.append(int(b))
+        kv_bytes += int(w.seq_lens[b]) * per
+        if t_used >= budget_s:
+            break
+    desc = (f"requests {picked} of the workload (all {H} heads each, unsharded attention), "
+            f"{int(sum(int(w.seq_lens[b]) for b in picked))} tokens")
+    return kv_bytes, t_used, desc
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
     import mla_inputs as mi
     import oracle
-    w = mi.config_workload(args.config)
+    if args.config == GQA_CONFIG:
+        w = mi.config_gqa_workload()
+        sample, name = gqa_cpu_sample, mi.GQA_CONFIG_NAME
+        kv_dtype = "bf16"
+    else:
+        w = mi.config_workload(args.config)
+        sample, name = cpu_sample, mi.CONFIG_NAMES[args.config]
+        kv_dtype = w.kv_dtype
     threads = oracle.num_threads()
     # one step = the oracle over a bounded sample of the workload
     budget = args.ref_step_seconds
     results = []
     for step in range(args.warmup + args.steps):
-        kv_bytes, dt, desc = cpu_sample(w, budget, oracle)
+        kv_bytes, dt, desc = sample(w, budget, oracle)
         if step >= args.warmup:
             results.append((kv_bytes, dt))
     tot_b = sum(r[0] for r in results)
@@ -218,9 +248,9 @@ def run_reference(args, world, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / len(results) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": mi.CONFIG_NAMES[args.config], "batch": w.batch,
+            "config": {"workload": name, "batch": w.batch,
                        "heads": w.num_heads, "q_len": w.q_len, "num_shards": w.num_shards,
-                       "layout": w.layout, "kv_dtype": w.kv_dtype,
+                       "layout": w.layout, "kv_dtype": kv_dtype,
                        "total_tokens": w.total_tokens},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
@@ -229,47 +259,128 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args, world, rank, local, dist):
+class Case:
+    """One benchmark workload on the device: pinned host inputs and their
+    device copies, output buffers, and the step (the library calls)."""
+
+    def __init__(self, name, kv_bytes, config, pairs, outputs, workspace, step, dtype, kernel,
+                 kernel_src, cpu):
+        self.name, self.kv_bytes, self.config = name, kv_bytes, config
+        self.pairs = pairs            # [(pinned host tensor, device tensor)] copied per e2e step
+        self.outputs = outputs        # [(device tensor, pinned host tensor)] read per e2e step
+        self.workspace, self.step, self.dtype, self.kernel = workspace, step, dtype, kernel
+        self.kernel_src = kernel_src  # source file of the timed kernel (traffic record key)
+        self.cpu = cpu                # cpu(budget_s, oracle) -> (KV bytes, seconds, sample)
+
+
+def _pinned_pair(h, dev):
+    h = h.pin_memory() if not h.is_pinned() else h
+    return h, h.to(dev)
+
+
+def mla_case(args, rank, dev, stream, ev_p, ev_k):
     import numpy as np
     import torch
 
     import mla_inputs as mi
     import sequence_sharded_mla_gb300 as mla
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    mla.lib()
-    # each rank decodes its own batch of the same shape (independent requests)
     w = rank_workload(args.config, rank, args.requests)
     B, H, q_len, N = w.batch, w.num_heads, w.q_len, w.num_shards
-    kv_bytes = w.kv_bytes()
-
-    h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
+    q = _pinned_pair(torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16), dev)
     if w.kv_dtype == "bf16":
-        h_kv = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16)
-        h_sc = None
+        kv = _pinned_pair(torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16), dev)
+        sc = None
     else:
-        h_kv = torch.from_numpy(w.kv)
-        h_sc = torch.from_numpy(w.kv_scale)
-    h_wuv = None if w.w_uv is None else torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16)
-    h_bt = torch.from_numpy(w.block_table).pin_memory()
-    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
-    d_q = h_q.to(dev)
-    d_kv = h_kv.to(dev)
-    d_sc = None if h_sc is None else h_sc.to(dev)
-    d_wuv = None if h_wuv is None else h_wuv.to(dev)
-    d_bt = h_bt.to(dev)
-    d_sl = h_sl.to(dev)
-    stream = torch.cuda.current_stream(dev)
+        kv = _pinned_pair(torch.from_numpy(w.kv), dev)
+        sc = _pinned_pair(torch.from_numpy(w.kv_scale), dev)
+    bt = _pinned_pair(torch.from_numpy(w.block_table), dev)
+    sl = _pinned_pair(torch.from_numpy(w.seq_lens), dev)
+    d_wuv = None
+    if w.w_uv is not None:
+        d_wuv = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16).to(dev)
     part = torch.empty((N, B, q_len, H, 512), dtype=torch.float32, device=dev)
     lsep = torch.empty((N, B, q_len, H), dtype=torch.float32, device=dev)
     out = torch.empty((B, q_len, H, 512 if d_wuv is None else 128), dtype=torch.bfloat16,
                       device=dev)
     lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
     ws = torch.empty((mla.mla_workspace_size(B, q_len, H, N),), dtype=torch.uint8, device=dev)
-    h_out = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
-    h_lse = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
 
+    def step(i=None):
+        if i is not None:
+            ev_p[2 * i].record(stream)
+            mla.mla_set_profile_events(ev_k[2 * i], ev_k[2 * i + 1])
+        mla.mla_decode_partial(q[1], kv[1], bt[1], sl[1], N, w.layout,
+                               kv_scale=None if sc is None else sc[1], causal=w.causal,
+                               out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
+        if i is not None:
+            mla.mla_set_profile_events(None, None)
+            ev_p[2 * i + 1].record(stream)
+        mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
+
+    pairs = [q, kv, bt, sl] + ([sc] if sc is not None else [])
+    outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
+               (lse, torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))]
+    config = {"workload": mi.CONFIG_NAMES[args.config], "batch": B, "heads": H, "q_len": q_len,
+              "num_shards": N, "layout": w.layout, "kv_dtype": w.kv_dtype,
+              "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
+              "total_tokens_per_gpu": w.total_tokens}
+    kernel = "mla_partial_kernel<%s,false>" % ("true" if w.kv_dtype == "fp8" else "false")
+    return Case(config["workload"], w.kv_bytes(), config, pairs, outputs, ws, step, "bf16",
+                kernel, "partial.cu", lambda budget, orc: cpu_sample(w, budget, orc))
+
+
+def gqa_case(args, rank, dev, stream, ev_p, ev_k):
+    import numpy as np
+    import torch
+
+    import mla_inputs as mi
+    import sequence_sharded_mla_gb300 as mla
+    w = mi.config_gqa_workload(pinned=True) if rank == 0 else mi.build_gqa_workload(
+        mi.GQA_CONFIG_NAME, 32, 1, 64, 4, 128, mi.agentic_lengths(6 + 1000 * rank, 32), 2,
+        "interleaved", False, seed=6 + 1000 * rank, pinned=True)
+    B, H, q_len, N, D = w.batch, w.num_heads, w.q_len, w.num_shards, w.head_dim
+    f = lambda a: _pinned_pair(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16), dev)
+    q, k, v = f(w.q), f(w.k_cache), f(w.v_cache)
+    bt = _pinned_pair(torch.from_numpy(w.block_table), dev)
+    sl = _pinned_pair(torch.from_numpy(w.seq_lens), dev)
+    part = torch.empty((N, B, q_len, H, D), dtype=torch.float32, device=dev)
+    lsep = torch.empty((N, B, q_len, H), dtype=torch.float32, device=dev)
+    out = torch.empty((B, q_len, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    ws = torch.empty((mla.gqa_workspace_size(B, q_len, H, w.num_kv_heads, N),), dtype=torch.uint8,
+                     device=dev)
+
+    def step(i=None):
+        if i is not None:
+            ev_p[2 * i].record(stream)
+            mla.mla_set_profile_events(ev_k[2 * i], ev_k[2 * i + 1])
+        mla.gqa_decode_partial(q[1], k[1], v[1], bt[1], sl[1], N, w.layout, causal=w.causal,
+                               out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
+        if i is not None:
+            mla.mla_set_profile_events(None, None)
+            ev_p[2 * i + 1].record(stream)
+        mla.gqa_shard_combine(part, lsep, out=out, lse_out=lse, stream=stream)
+
+    outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
+               (lse, torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))]
+    config = {"workload": mi.GQA_CONFIG_NAME, "batch": B, "heads": H,
+              "kv_heads": w.num_kv_heads, "head_dim": D, "q_len": q_len, "num_shards": N,
+              "layout": w.layout, "kv_dtype": "bf16", "causal": bool(w.causal),
+              "total_tokens_per_gpu": w.total_tokens}
+    return Case(mi.GQA_CONFIG_NAME, w.kv_bytes(), config, [q, k, v, bt, sl], outputs, ws, step,
+                "bf16", "gqa_partial_kernel", "gqa.cu",
+                lambda budget, orc: gqa_cpu_sample(w, budget, orc))
+
+
+def run_gpu(args, world, rank, local, dist):
+    import torch
+
+    import sequence_sharded_mla_gb300 as mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.lib()
+    stream = torch.cuda.current_stream(dev)
     # per timed step: events around the whole partial call (plan, partial
     # kernel, merge) and, recorded by the library itself, around the partial
     # kernel alone
@@ -277,17 +388,12 @@ def run_gpu(args, world, rank, local, dist):
     ev_k = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     for ev in ev_p + ev_k:
         ev.record(stream)
-
-    def step(i=None):
-        if i is not None:
-            ev_p[2 * i].record(stream)
-            mla.mla_set_profile_events(ev_k[2 * i], ev_k[2 * i + 1])
-        mla.mla_decode_partial(d_q, d_kv, d_bt, d_sl, N, w.layout, kv_scale=d_sc, causal=w.causal,
-                               out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
-        if i is not None:
-            mla.mla_set_profile_events(None, None)
-            ev_p[2 * i + 1].record(stream)
-        mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
+    # each rank decodes its own batch of the same shape (independent requests)
+    make = gqa_case if args.config == GQA_CONFIG else mla_case
+    case = make(args, rank, dev, stream, ev_p, ev_k)
+    kv_bytes = case.kv_bytes
+    ws = case.workspace
+    step = case.step
 
     def barrier():
         if dist is not None:
@@ -317,21 +423,16 @@ def run_gpu(args, world, rank, local, dist):
         raise RuntimeError(f"device error status {status}")
 
     # end to end through host buffers: copy the step's inputs in, read results out
-    h2d = (h_q.numel() * 2 + h_kv.numel() * h_kv.element_size() + h_bt.numel() * 4 +
-           h_sl.numel() * 4 + (0 if h_sc is None else h_sc.numel() * 4))
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    h2d = sum(h.numel() * h.element_size() for h, _ in case.pairs)
+    d2h = sum(d.numel() * d.element_size() for d, _ in case.outputs)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
     def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_kv.copy_(h_kv, non_blocking=True)
-        if h_sc is not None:
-            d_sc.copy_(h_sc, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
+        for h, d in case.pairs:
+            d.copy_(h, non_blocking=True)
         step()
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        for d, h in case.outputs:
+            h.copy_(d, non_blocking=True)
 
     e2e_step()
     barrier()
@@ -353,22 +454,19 @@ def run_gpu(args, world, rank, local, dist):
     value = total_kv * args.steps / elapsed / 1e9
     ms_per_step = elapsed / args.steps * 1e3
     achieved = kv_bytes / (kernel_avg_ms / 1e3) / 1e9
-    traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc", "partial.cu"),
-                          mi.CONFIG_NAMES[args.config])
+    traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc",
+                                       case.kernel_src), case.name)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": mi.CONFIG_NAMES[args.config], "batch": B, "heads": H,
-                   "q_len": q_len, "num_shards": N, "layout": w.layout, "kv_dtype": w.kv_dtype,
-                   "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
-                   "total_tokens_per_gpu": w.total_tokens, "kv_bytes_per_gpu": kv_bytes,
-                   "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per GPU vs 129 MB)",
-                   "parallelism": f"{world} GPU(s), independent batches; {N} logical shards each"},
+        "scaling": "weak", "vs_baseline": None, "dtype": case.dtype, "data": "synthetic",
+        "config": dict(case.config, kv_bytes_per_gpu=kv_bytes,
+                       l2=f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per GPU vs 129 MB)",
+                       parallelism=f"{world} GPU(s), independent batches; "
+                                   f"{case.config['num_shards']} logical shards each"),
         "steps_per_s": args.steps / elapsed,
         "pct_of_peak_hbm": value / world / peak,
-        "roofline": {"kernel": "mla_partial_kernel<%s>" % ("true" if w.kv_dtype == "fp8" else "false"),
-                     "bound": "hbm",
+        "roofline": {"kernel": case.kernel, "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": traffic},
@@ -377,12 +475,12 @@ def run_gpu(args, world, rank, local, dist):
         "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * args.steps,   # plan, partial, merge, combine
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
         import oracle
-        kvb, dt, desc = cpu_sample(w, args.cpu_seconds, oracle)
+        kvb, dt, desc = case.cpu(args.cpu_seconds, oracle)
         line["cpu_baseline"] = {"value": kvb / dt / 1e9, "unit": "GB/s",
                                 "cores": oracle.num_threads(), "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
@@ -398,8 +496,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5],
-                    help="workload: one of the five benchmark configurations (default 2)")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5, 6],
+                    help="workload: one of the five benchmark configurations (default 2), "
+                         "or 6: the grouped-query batch")
     ap.add_argument("--requests", type=int, default=0,
                     help="profiling only: keep the first K requests of the workload")
     args = ap.parse_args()
