@@ -56,6 +56,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Desc {
   int B, q_len, H, Hkv, G;   // G = H / Hkv, a power of two <= 64
+  int lg;                    // log2(G)
   int ni;                    // query positions per 64-row group (64 / G)
   int Gq;                    // row groups per (request, KV head)
   int num_shards, shard_first, n_out, layout, causal, num_pages, max_pages;
@@ -129,9 +130,9 @@ __device__ __forceinline__ bool tile_full(const Desc& d, const Unit& x, int j) {
 }
 
 // Output row of row r (< x.rows) of unit x: query position x.i0 + r / G,
-// head kh * G + r % G, in [n_out, B, q_len, H].
+// head kh * G + r % G, in [n_out, B, q_len, H].  G is a power of two.
 __device__ __forceinline__ size_t out_row(const Desc& d, const Unit& x, int r) {
-  const int i = x.i0 + r / d.G, h = x.kh * d.G + r % d.G;
+  const int i = x.i0 + (r >> d.lg), h = (x.kh << d.lg) + (r & (d.G - 1));
   return (((size_t)x.so * d.B + x.b) * d.q_len + i) * d.H + h;
 }
 
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       const Unit x = make_unit(d, unit);
       const bool owner = r < x.rows;
-      const int vis_limit = x.L - d.q_len + x.i0 + r / d.G;   // causal: t <= vis_limit
+      const int vis_limit = x.L - d.q_len + x.i0 + (r >> d.lg);   // causal: t <= vis_limit
       float m_run = -CUDART_INF_F, l_run = 0.0f;
       for (int j = t0; j < t1; ++j, ++gt) {
         const int st = gt % kStages, round = gt / kStages;
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // thread (quad, lane) holds latent dim 32*quad + lane of every row
       const int dim = 32 * quad + lane;
 #pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
+      for (int h2 = 0; h2 < 2 && 32 * h2 < x.rows; ++h2) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + kColO + 32 * h2, v);
         tmem_wait_ld();
@@ -513,14 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           il[4 * c4 + 2] = t.z;
           il[4 * c4 + 3] = t.w;
         }
+        // rows 32*h2 + c go to out_partial rows base + (c >> lg) * H + (c & (G-1))
+        // (whole unit) or to consecutive workspace rows (piece of a split unit)
+        float* base = whole ? p.out_partial + out_row(d, x, 32 * h2) * kD
+                            : p.ws_o + (sl * kRows + 32 * h2) * kD;
+        const size_t pos_stride = whole ? (size_t)d.H * kD : (size_t)d.G * kD;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const int row = 32 * h2 + c;
-          if (row < x.rows) {
-            float* dst = whole ? p.out_partial + out_row(d, x, row) * kD
-                               : p.ws_o + (sl * kRows + row) * kD;
-            dst[dim] = __uint_as_float(v[c]) * il[c];
-          }
+          if (32 * h2 + c < x.rows)
+            base[(size_t)(c >> d.lg) * pos_stride + (size_t)(c & (d.G - 1)) * kD + dim] =
+                __uint_as_float(v[c]) * il[c];
         }
       }
       tc_fence_before();
@@ -719,6 +722,8 @@ mla_status gqa_decode_partial(const void* q, const gqa_kv_pages* kv, const int32
   d.H = shape->num_heads;
   d.Hkv = shape->num_kv_heads;
   d.G = d.H / d.Hkv;
+  d.lg = 0;
+  while ((1 << d.lg) < d.G) ++d.lg;
   d.ni = kRows / d.G;
   d.Gq = ceil_div(d.q_len, d.ni);
   d.num_shards = num_shards;
