@@ -335,9 +335,12 @@ def gqa_case(args, rank, dev, stream, ev_p, ev_k):
 
     import mla_inputs as mi
     import sequence_sharded_mla_gb300 as mla
-    w = mi.config_gqa_workload(pinned=True) if rank == 0 else mi.build_gqa_workload(
-        mi.GQA_CONFIG_NAME, 32, 1, 64, 4, 128, mi.agentic_lengths(6 + 1000 * rank, 32), 2,
-        "interleaved", False, seed=6 + 1000 * rank, pinned=True)
+    lens = mi.agentic_lengths(6 + 1000 * rank, 32)
+    name = mi.GQA_CONFIG_NAME
+    if args.requests:   # a reduced copy (first K requests) for profiling runs
+        lens, name = lens[:args.requests], name + f"-first{args.requests}"
+    w = mi.build_gqa_workload(name, len(lens), 1, 64, 4, 128, lens, 2, "interleaved", False,
+                              seed=6 + 1000 * rank, pinned=True)
     B, H, q_len, N, D = w.batch, w.num_heads, w.q_len, w.num_shards, w.head_dim
     f = lambda a: _pinned_pair(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16), dev)
     q, k, v = f(w.q), f(w.k_cache), f(w.v_cache)
