@@ -91,3 +91,26 @@ def test_local_layouts_need_one_shard():
     st = L.mla_decode_partial(fake, ctypes.byref(kv), fake, 1, fake, ctypes.byref(sh), 0, 2, 7,
                               fake, fake, fake, 1 << 20, None)
     assert st == -1
+
+
+def test_gqa_arguments_checked_on_host():
+    """The GQA calls refuse bad arguments and unsupported shapes before any
+    CUDA call: null pointers, zero sizes, head widths other than 128,
+    groups that are not powers of two."""
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    fake = ctypes.c_void_p(512)
+    kv = mla.gqa_kv_pages(fake, fake, 4, 64)
+    good = mla.gqa_shape(2, 1, 16, 4, 128, 0, 0.088)
+    assert L.gqa_decode_partial(None, ctypes.byref(kv), fake, 1, fake, ctypes.byref(good), -1, 2,
+                                0, fake, fake, fake, 1 << 20, None) == -1
+    bad = mla.gqa_shape(0, 1, 16, 4, 128, 0, 0.088)
+    assert L.gqa_workspace_size(ctypes.byref(bad), 2, -1) == 0
+    for shape in (mla.gqa_shape(2, 1, 16, 4, 64, 0, 0.125),    # head width 64
+                  mla.gqa_shape(2, 1, 12, 4, 128, 0, 0.088),   # groups of 3
+                  mla.gqa_shape(2, 1, 16, 3, 128, 0, 0.088)):  # 3 does not divide 16
+        assert L.gqa_workspace_size(ctypes.byref(shape), 2, -1) == 0
+    nokv = mla.gqa_kv_pages(None, fake, 4, 64)
+    assert L.gqa_decode_partial(fake, ctypes.byref(nokv), fake, 1, fake, ctypes.byref(good), -1,
+                                2, 0, fake, fake, fake, 1 << 20, None) == -1
+    assert L.gqa_shard_combine(None, fake, 2, ctypes.byref(good), fake, None, None) == -1
