@@ -235,6 +235,22 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           page = pd.num_pages;
         }
         if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
+        // fp8: the sources of this lane's two token-scale copies (slots lane,
+        // lane + 32), formed before the stage is free; rows_per = 64 / nv is
+        // a power of two
+        const float* scale_src[2] = {nullptr, nullptr};
+        if constexpr (kFp8) {
+          const int lg_rows = 6 - (nv == 1 ? 0 : nv == 2 ? 1 : nv == 4 ? 2 : 3);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int a = lane + 32 * h;             // token slot
+            const int k = a >> lg_rows;              // page box of the slot
+            const int pg = __shfl_sync(0xffffffffu, page, k);
+            const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
+            scale_src[h] = p.kv_scale +
+                           (okpg ? (size_t)pg * kPage + (a & ((1 << lg_rows) - 1)) * nv + res : 0);
+          }
+        }
         if (gt >= 2) {
           ok = __all_sync(0xffffffffu,
                           mbar_wait(b_kv_empty + 8 * st, ((gt >> 1) - 1) & 1, tmo, abort_flag));
@@ -252,16 +268,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           if (lane < nv)
             tma_load_5d(sKV + st * kTileBytes + kFp8Staging + lane * (kTile / nv) * kDqk, &tm_kv,
                         full, 0, 0, res, 0, page);
-          const int rows_per = kTile / nv;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int a = lane + 32 * h;             // token slot
-            const int k = a / rows_per;              // page box of the slot
-            const int pg = __shfl_sync(0xffffffffu, page, k);
-            const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
-            const float* src = p.kv_scale + (okpg ? (size_t)pg * kPage + (a % rows_per) * nv + res : 0);
-            cp_async_4(smem_u32(&misc->scale[st][a]), src);
-          }
+          cp_async_4(smem_u32(&misc->scale[st][lane]), scale_src[0]);
+          cp_async_4(smem_u32(&misc->scale[st][lane + 32]), scale_src[1]);
           cp_async_mbar_arrive_noinc(full);
         } else if (lane < nv) {
           // cache row page*64 + res of the (row-in-group, chunk, group, row)
