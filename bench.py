@@ -46,6 +46,18 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the sustained measurement (the
+    partial kernel runs inside a long loop of steps), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured bf16_tflops_sustained"
+    except Exception:
+        return 1700.0, "fallback"
+
+
 def kernel_sha(kernel_src):
     return hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
 
@@ -264,13 +276,25 @@ class Case:
     device copies, output buffers, and the step (the library calls)."""
 
     def __init__(self, name, kv_bytes, config, pairs, outputs, workspace, step, dtype, kernel,
-                 kernel_src, cpu):
+                 kernel_src, cpu, flops=0.0, combine_bytes=0.0, tensor_bound=False):
         self.name, self.kv_bytes, self.config = name, kv_bytes, config
         self.pairs = pairs            # [(pinned host tensor, device tensor)] copied per e2e step
         self.outputs = outputs        # [(device tensor, pinned host tensor)] read per e2e step
         self.workspace, self.step, self.dtype, self.kernel = workspace, step, dtype, kernel
         self.kernel_src = kernel_src  # source file of the timed kernel (traffic record key)
         self.cpu = cpu                # cpu(budget_s, oracle) -> (KV bytes, seconds, sample)
+        self.flops = flops            # useful MMA flops of the partial kernel per step
+        self.combine_bytes = combine_bytes   # bytes the combine kernel reads and writes
+        self.tensor_bound = tensor_bound     # the dense contractions bound the partial kernel
+
+
+def visible_pairs(seq_lens, q_len, causal):
+    """Sum over requests and query positions of the tokens each query sees."""
+    tot = 0
+    for L in seq_lens:
+        L = int(L)
+        tot += sum(max(0, L - q_len + i + 1) for i in range(q_len)) if causal else L * q_len
+    return tot
 
 
 def _pinned_pair(h, dev):
@@ -278,7 +302,7 @@ def _pinned_pair(h, dev):
     return h, h.to(dev)
 
 
-def mla_case(args, rank, dev, stream, ev_p, ev_k):
+def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
     import numpy as np
     import torch
 
@@ -316,6 +340,8 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k):
             mla.mla_set_profile_events(None, None)
             ev_p[2 * i + 1].record(stream)
         mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
+        if i is not None:
+            ev_c[i].record(stream)
 
     pairs = [q, kv, bt, sl] + ([sc] if sc is not None else [])
     outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
@@ -325,11 +351,17 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k):
               "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
               "total_tokens_per_gpu": w.total_tokens}
     kernel = "mla_partial_kernel<%s,false>" % ("true" if w.kv_dtype == "fp8" else "false")
+    rows = B * q_len * H
+    flops = 2.0 * H * (576 + 512) * visible_pairs(w.seq_lens, q_len, w.causal)
+    comb = N * rows * (512 * 4 + 4) + rows * ((128 if d_wuv is not None else 512) * 2 + 4)
+    if d_wuv is not None:
+        comb += d_wuv.numel() * 2
     return Case(config["workload"], w.kv_bytes(), config, pairs, outputs, ws, step, "bf16",
-                kernel, "partial.cu", lambda budget, orc: cpu_sample(w, budget, orc))
+                kernel, "partial.cu", lambda budget, orc: cpu_sample(w, budget, orc), flops=flops,
+                combine_bytes=comb, tensor_bound=q_len * H > 64)
 
 
-def gqa_case(args, rank, dev, stream, ev_p, ev_k):
+def gqa_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
     import numpy as np
     import torch
 
@@ -363,6 +395,8 @@ def gqa_case(args, rank, dev, stream, ev_p, ev_k):
             mla.mla_set_profile_events(None, None)
             ev_p[2 * i + 1].record(stream)
         mla.gqa_shard_combine(part, lsep, out=out, lse_out=lse, stream=stream)
+        if i is not None:
+            ev_c[i].record(stream)
 
     outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
                (lse, torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))]
@@ -370,9 +404,12 @@ def gqa_case(args, rank, dev, stream, ev_p, ev_k):
               "kv_heads": w.num_kv_heads, "head_dim": D, "q_len": q_len, "num_shards": N,
               "layout": w.layout, "kv_dtype": "bf16", "causal": bool(w.causal),
               "total_tokens_per_gpu": w.total_tokens}
+    rows = B * q_len * H
     return Case(mi.GQA_CONFIG_NAME, w.kv_bytes(), config, [q, k, v, bt, sl], outputs, ws, step,
                 "bf16", "gqa_partial_kernel", "gqa.cu",
-                lambda budget, orc: gqa_cpu_sample(w, budget, orc))
+                lambda budget, orc: gqa_cpu_sample(w, budget, orc),
+                flops=2.0 * H * (D + D) * visible_pairs(w.seq_lens, q_len, w.causal),
+                combine_bytes=N * rows * (D * 4 + 4) + rows * (D * 2 + 4))
 
 
 def run_gpu(args, world, rank, local, dist):
@@ -389,11 +426,12 @@ def run_gpu(args, world, rank, local, dist):
     # kernel alone
     ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     ev_k = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    for ev in ev_p + ev_k:
+    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for ev in ev_p + ev_k + ev_c:
         ev.record(stream)
     # each rank decodes its own batch of the same shape (independent requests)
     make = gqa_case if args.config == GQA_CONFIG else mla_case
-    case = make(args, rank, dev, stream, ev_p, ev_k)
+    case = make(args, rank, dev, stream, ev_p, ev_k, ev_c)
     kv_bytes = case.kv_bytes
     ws = case.workspace
     step = case.step
@@ -421,6 +459,7 @@ def run_gpu(args, world, rank, local, dist):
     elapsed = t_start.elapsed_time(t_end) / 1e3
     partial_ms = [ev_p[2 * i].elapsed_time(ev_p[2 * i + 1]) for i in range(args.steps)]
     kernel_ms = [ev_k[2 * i].elapsed_time(ev_k[2 * i + 1]) for i in range(args.steps)]
+    combine_ms = [ev_p[2 * i + 1].elapsed_time(ev_c[i]) for i in range(args.steps)]
     status = mla.mla_get_device_error(ws, stream)
     if status != 0:
         raise RuntimeError(f"device error status {status}")
@@ -448,17 +487,28 @@ def run_gpu(args, world, rank, local, dist):
     barrier()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
 
-    (elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms), total_kv = reduce_over_ranks(
-        dist, [elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
-               statistics.mean(kernel_ms)], kv_bytes, dev)
+    (elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms, combine_avg_ms), total_kv = \
+        reduce_over_ranks(dist, [elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
+                                 statistics.mean(kernel_ms), statistics.mean(combine_ms)],
+                          kv_bytes, dev)
     if rank != 0:
         return
     peak, peak_kind = load_peaks()
+    tpeak, tpeak_kind = load_tensor_peak()
     value = total_kv * args.steps / elapsed / 1e9
     ms_per_step = elapsed / args.steps * 1e3
     achieved = kv_bytes / (kernel_avg_ms / 1e3) / 1e9
     traffic = traffic_for(os.path.join(ROOT, "sequence_sharded_mla_gb300", "csrc",
                                        case.kernel_src), case.name)
+    hbm_roof = {"kernel": case.kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": traffic}
+    tflops = case.flops / (kernel_avg_ms / 1e3) / 1e12
+    tensor_roof = {"kernel": case.kernel, "bound": "tensor", "achieved": tflops, "peak": tpeak,
+                   "unit": "TFLOP/s", "frac": tflops / tpeak,
+                   "peak_source": f"{tpeak_kind} (dense fp16/bf16 rate; useful MMA flops "
+                                  "2*H*(Dk+Dv) per visible token and query)",
+                   "traffic": traffic}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -469,10 +519,11 @@ def run_gpu(args, world, rank, local, dist):
                                    f"{case.config['num_shards']} logical shards each"),
         "steps_per_s": args.steps / elapsed,
         "pct_of_peak_hbm": value / world / peak,
-        "roofline": {"kernel": case.kernel, "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": traffic},
+        "roofline": hbm_roof if not case.tensor_bound else tensor_roof,
+        "roofline_other": tensor_roof if not case.tensor_bound else hbm_roof,
+        "combine": {"kernel_ms": combine_avg_ms,
+                    "gbps": case.combine_bytes / (combine_avg_ms / 1e3) / 1e9,
+                    "bytes_per_step": case.combine_bytes},
         "partial_kernel_ms": kernel_avg_ms,
         "partial_call_ms": partial_avg_ms,
         "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
