@@ -76,30 +76,45 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
 }
 
 // Fused combine + W_UV.  Block (h, jb) handles head h and output columns
-// [64*jb, 64*jb + 64) for every (b, i) row of that head, 16 rows at a time:
-// it merges the shard partials of those rows into shared memory (fp32), then
-// 256 threads (64 columns x 4 slices of 128 latent dims) accumulate
-// out . W_UV[h][:, col] and reduce the four slices.
-constexpr int kWuvRowsPerPass = 16;
+// [16*jb, 16*jb + 16) for every (b, i) row of that head, 8 rows at a time:
+// it merges the shard partials of those rows into shared memory (fp32, one
+// warp per row), then 256 threads (16 columns x 16 slices; slice s takes the
+// latent dims c = s mod 16) accumulate out . W_UV[h][:, col] and reduce the
+// slices.  128 / 16 column blocks per head keep 8 x H blocks in flight: at
+// small batches the projection is latency-bound, not bandwidth-bound.  The
+// block's W_UV columns (512 x 16 bf16) do not depend on the partials, so they
+// are staged in shared memory before the wait on the preceding kernel.
+constexpr int kWuvRowsPerPass = 8;
+constexpr int kWuvCols = 16;                  // output columns per block
+constexpr int kWuvSlices = 256 / kWuvCols;    // 16 slices of 32 latent dims
 
 __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
     const float* __restrict__ partials, const float* __restrict__ lses, int num_shards,
     int rows_per_head_group /* B*q_len */, int H, const uint16_t* __restrict__ w_uv,
     uint16_t* __restrict__ y, float* __restrict__ lse_out) {
   __shared__ float so[kWuvRowsPerPass][kDv];
-  __shared__ float red[4][kWuvRowsPerPass][64];
-  griddep_wait();                // the partials
+  __shared__ float red[kWuvSlices][kWuvRowsPerPass][kWuvCols];
+  __shared__ __align__(16) uint16_t wsm[kDv][kWuvCols];
   const int h = blockIdx.x, jb = blockIdx.y;
   const int tid = threadIdx.x;
+  {
+    // 512 rows x 32 bytes: two 16-byte pieces per row
+    const uint16_t* wblk = w_uv + (size_t)h * kDv * kDuv + kWuvCols * jb;
+    for (int i = tid; i < kDv * 2; i += blockDim.x) {
+      const int c = i >> 1, half = i & 1;
+      *reinterpret_cast<uint4*>(&wsm[c][8 * half]) =
+          __ldg(reinterpret_cast<const uint4*>(wblk + (size_t)c * kDuv + 8 * half));
+    }
+  }
+  griddep_wait();                // the partials
   const int rows = rows_per_head_group * H;
-  const int col = tid & 63, slice = tid >> 6;
-  const uint16_t* wcol = w_uv + (size_t)h * kDv * kDuv + 64 * jb + col;
+  const int col = tid & (kWuvCols - 1), slice = tid / kWuvCols;
+  const int warp = tid >> 5, lane = tid & 31;
   for (int base = 0; base < rows_per_head_group; base += kWuvRowsPerPass) {
     const int nr = min(kWuvRowsPerPass, rows_per_head_group - base);
-    // merge: warp w handles rows w, w+8 of this pass
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int rr = warp; rr < nr; rr += 8) {
-      const int row = (base + rr) * H + h;
+    // merge: warp w handles row w of this pass
+    if (warp < nr) {
+      const int row = (base + warp) * H + h;
       float M = -CUDART_INF_F;
       float l[kMaxShards];
 #pragma unroll
@@ -112,7 +127,9 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
       for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       float wsum = 0.f;
       if (M > -CUDART_INF_F) {
-        for (int s = 0; s < num_shards; ++s) {
+#pragma unroll
+        for (int s = 0; s < kMaxShards; ++s) {
+          if (s >= num_shards) break;
           const float w = __expf(l[s] - M);
           wsum += w;
           const float4* src =
@@ -131,7 +148,7 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<float4*>(&so[rr][4 * (lane + 32 * k)]) = v;
+        *reinterpret_cast<float4*>(&so[warp][4 * (lane + 32 * k)]) = v;
       }
       if (lse_out != nullptr && jb == 0 && lane == 0)
         lse_out[row] = M > -CUDART_INF_F ? M + __logf(wsum) : -CUDART_INF_F;
@@ -140,22 +157,23 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
     float acc[kWuvRowsPerPass];
 #pragma unroll
     for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] = 0.f;
-    const int c0 = slice * 128;
-#pragma unroll 4
-    for (int c = c0; c < c0 + 128; ++c) {
-      const float w = __uint_as_float(((uint32_t)__ldg(wcol + (size_t)c * kDuv)) << 16);
+#pragma unroll 8
+    for (int c = slice; c < kDv; c += kWuvSlices) {
+      const float w = __uint_as_float(((uint32_t)wsm[c][col]) << 16);
 #pragma unroll
       for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] += so[r][c] * w;
     }
 #pragma unroll
     for (int r = 0; r < kWuvRowsPerPass; ++r) red[slice][r][col] = acc[r];
     __syncthreads();
-    for (int e = tid; e < nr * 64; e += 256) {
-      const int r = e >> 6, c = e & 63;
-      const float v = red[0][r][c] + red[1][r][c] + red[2][r][c] + red[3][r][c];
+    if (tid < nr * kWuvCols) {
+      const int r = tid / kWuvCols, c = tid % kWuvCols;
+      float v = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < kWuvSlices; ++sl) v += red[sl][r][c];
       const int row = (base + r) * H + h;
       __nv_bfloat16 b = __float2bfloat16_rn(v);
-      y[(size_t)row * kDuv + 64 * jb + c] = *reinterpret_cast<uint16_t*>(&b);
+      y[(size_t)row * kDuv + kWuvCols * jb + c] = *reinterpret_cast<uint16_t*>(&b);
     }
     __syncthreads();
   }
@@ -178,7 +196,7 @@ cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num
                                int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
                                float* lse_out, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(H, kDuv / 64);
+  cfg.gridDim = dim3(H, kDuv / kWuvCols);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
