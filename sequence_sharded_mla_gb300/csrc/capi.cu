@@ -17,8 +17,8 @@ namespace mla {
 int partial_smem_bytes();
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const PartialParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                               const PartialParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_kv, const PartialParams& p, int grid,
+                               cudaStream_t stream);
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
                         int min_tiles, int unit_cost, cudaStream_t stream);
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
@@ -89,7 +89,7 @@ const char* mla_status_string(mla_status st) {
     case MLA_ERR_TIMEOUT: return "device wait timed out";
     case MLA_ERR_DEVICE_BOUNDS: return "block-table entry out of range";
     case MLA_ERR_WORKSPACE: return "workspace missing or too small";
-    case MLA_ERR_RANGE: return "query value beyond the fp16 range (fp8 cache)";
+    case MLA_ERR_RANGE: return "non-finite query value (fp8 cache)";
   }
   return "unknown status";
 }
@@ -194,17 +194,17 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   if (fp8) {
-    // e4m3 codes: view [page][row / nv][row % nv][3][192] read as
-    // (192 codes, third, residue, row / nv, page); a box lands the 64/nv rows
-    // of one page that one shard owns, each row's 576 codes contiguous
-    cuuint64_t dims[5] = {192, 3, (cuuint64_t)nv, (cuuint64_t)(kPage / nv),
-                          (cuuint64_t)kv->num_pages};
-    cuuint64_t strides[4] = {192, (cuuint64_t)kDqk, (cuuint64_t)kDqk * nv,
-                             (cuuint64_t)kDqk * kPage};
-    cuuint32_t box[5] = {192, 3, 1, (cuuint32_t)(kPage / nv), 1};
+    // e4m3 codes: the same view with 64-code chunks, strides (-, 576 nv, 64,
+    // 4608 nv, 576) and 64-byte swizzling: a box lands a page's residue rows,
+    // all nine chunks, in the group-major layout of the fp8 kernel
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
+                          (cuuint64_t)kv->num_pages * kPage};
+    cuuint64_t strides[4] = {(cuuint64_t)kDqk * nv, 64, (cuuint64_t)kDqk * 8 * nv,
+                             (cuuint64_t)kDqk};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kPage / 8 / nv), 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   } else {
@@ -232,6 +232,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.kv_scale = kv->scale;
   p.q_one_box = q_one_box;
   p.kv_fp8 = nullptr;
+  p.q = static_cast<const uint16_t*>(q);
   p.timeout_ns = kTimeoutNs;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -240,7 +241,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   void* ev1 = host::g_ev_after.load();
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const cudaError_t le = fp8 ? launch_partial_fp8(tm_q, tm_kv, p, grid, st)
+  const cudaError_t le = fp8 ? launch_partial_fp8(tm_kv, p, grid, st)
                              : launch_partial_bf16(tm_q, tm_kv, p, grid, st);
   if (ev1 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev1), st) != cudaSuccess)
     return MLA_ERR_CUDA;

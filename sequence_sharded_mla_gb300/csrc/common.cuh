@@ -22,7 +22,7 @@ constexpr int kMaxShards = 8;
 // Error bits written to the workspace error word.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadPage = 2u;
-constexpr unsigned kErrQRange = 4u;   // fp8 caches: a query value beyond the fp16 range
+constexpr unsigned kErrQRange = 4u;   // fp8 caches: a non-finite query value
 constexpr unsigned kErrQLens = 8u;    // a per-request query count outside [1, q_len]
 
 enum Layout : int { kInterleaved = 0, kContiguous = 1 };
@@ -75,6 +75,7 @@ struct PartialParams {
   float* ws_o;         // [grid * 2, 64, 512] split pieces
   float* ws_lse;       // [grid * 2, 64]
   const float* kv_scale;  // fp8 caches: [num_pages * 64]
+  const uint16_t* q;      // bf16 [B * R, 576]: the fp8 kernel reads it directly
   int q_one_box;        // 1: tm_q loads all 9 chunks of a 64-row group per box
   const uint8_t* kv_fp8;  // fp8 caches: [num_pages, 64, 576] codes
   unsigned long long timeout_ns;

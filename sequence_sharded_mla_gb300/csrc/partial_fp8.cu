@@ -1,0 +1,750 @@
+// Sequence-sharded MLA decode over an fp8 latent cache: per-shard partial
+// attention on the e4m3 tensor cores (tcgen05 kind::f8f6f4), straight from
+// the cache's codes.
+//
+// Same computation as the bf16 kernel ("Decode Context Parallelism",
+// sections 4.1 and 5.3: each rank attends over its local latent slice and
+// emits the partial output and its log-sum-exp), with the cache held as OCP
+// e4m3 codes plus one fp32 scale per token (K and V of token t are
+// code * scale_t).  The MMAs read the codes as they came from memory: nothing
+// is expanded, so a 64-token stage is 36 KB and four of them are in flight.
+//
+// Exactness.  Both other operands are carried as two-term e4m3 sums:
+//   - the query: per row a power-of-two scale s_r puts max|q| in [128, 256);
+//     q*s_r = hi + lo with hi = e4m3(q*s_r), lo = e4m3(q*s_r - hi).  That is
+//     exact for every component with |q*s_r| >= 2^-2 and within 2^-10 (in
+//     scaled units) below; S = (Q_hi + Q_lo) K^T is two accumulating MMAs.
+//   - the probabilities: with sigma_t = mant_t * 2^E_t (mant in [0.5, 1)),
+//     the softmax keeps its running max over b_t = a_t + E_t, where a_t is
+//     the log2-domain logit; e_t = 2^(b_t - m) is at most 2^8, P'_t = e_t *
+//     mant_t = 2^(a_t - m) * sigma_t carries the value scale, and the
+//     normaliser sums e_t * 2^-E_t = 2^(a_t - m).  P' = hi + lo as above
+//     (relative error about 2^-8, like a bf16 P), and O^T += V^T P'^T is two
+//     accumulating MMAs per 32-token step.
+// The tensor cores accumulate in fp32.
+//
+// Shared memory (1024-byte aligned base):
+//   Q_hi, Q_lo   2 x 36 KB  [chunk c][8-row group][8 rows][64 codes], 64-byte swizzle
+//   stages       4 x 36 KB  group-major: slot a's 64-code chunk c at
+//                           (a/8)*4608 + c*512 + (a%8)*64 (swizzled), one TMA box per page
+//   P_lo         4 KB       [8-row group][8 rows][64 tokens]; P_hi goes into the
+//                           stage's rope atoms once QK^T has read them
+//   misc         barriers, token scales and their exponent split, softmax exchange
+//
+// Warps: 0 producer (block table, TMA of the codes, cp.async of the scales);
+// 1 and 6 MMA issuers (even / odd chunks of QK^T into two accumulators, two of
+// the four 128-dim blocks of P.V each); 2..5 softmax and epilogue (two threads
+// per query row); 7..10 split each piece's query into Q_hi/Q_lo from global
+// memory, and warp 7 also splits every tile's token scales.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kThreads = 352;
+constexpr int kStages = 4;
+constexpr int kStageBytes = kTile * kDqk;        // 36864: codes of one 64-token tile
+constexpr int kAtom = 512;                       // 8 rows x 64 bytes
+constexpr int kGroupBytes = kChunks * kAtom;     // 4608: one 8-slot group, nine chunks
+constexpr int kRopeAtom = 8 * kAtom;             // rope chunk of a group (P_hi after QK^T)
+constexpr int kQTermBytes = kChunks * 8 * kAtom; // 36864: one term of a 64-row query group
+constexpr int kQChunkBytes = 8 * kAtom;          // 4096: 64 rows of one chunk
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = 2 * kQTermBytes;                         // 73728
+constexpr int kSmemPlo = kSmemKV + kStages * kStageBytes;        // 221184
+constexpr int kSmemMisc = kSmemPlo + 8 * kAtom;                  // 225280
+constexpr int kMiscBytes = 6144;
+constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;        // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr int kIssuers = 2;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kConvThreads = 128;
+constexpr uint32_t kBarSoftmax = 1;
+constexpr uint32_t kBarConv = 2;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: e_t <= 2^8 keeps P' inside e4m3
+
+struct Misc {
+  uint64_t kv_full[kStages], kv_empty[kStages], prep[kStages];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t q_conv, q_empty, o_free;
+  uint32_t tmem_base;
+  int abort;
+  float alpha[2][kRows];
+  alignas(16) float inv_l[kRows];
+  // per stage and token slot: the scale (cp.async target, then sanitised in
+  // place), E + 1 as a float, 2^-(E+1), and sigma * 2^-(E+1)
+  alignas(16) float sigma[kStages][kTile];
+  alignas(16) float lge[kStages][kTile];
+  alignas(16) float il[kStages][kTile];
+  alignas(16) float mant[kStages][kTile];
+};
+static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
+
+// TMEM: per S buffer two partial accumulators (M=64, 64 columns each), then
+// the four 128-dim blocks of O^T (M=128, 64 columns each).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColO = 256;
+
+__device__ __forceinline__ void set_error(PartialParams& p, Misc* misc, unsigned bits) {
+  atomicOr(&p.hdr->err, bits);
+  if (bits & kErrTimeout) *(volatile int*)&misc->abort = 1;
+}
+
+// Byte offset of (row, 16-byte unit u) in a run of 64-byte-swizzled atoms
+// whose 8-row groups are `group_stride` apart.
+__device__ __forceinline__ uint32_t sw64_off(int row, int u, int group_stride) {
+  return (uint32_t)((row >> 3) * group_stride + (row & 7) * 64 + ((u ^ ((row & 7) >> 1)) << 4));
+}
+
+// Largest |q| of a row half as a bf16 magnitude pattern (monotonic in |q|;
+// NaN sorts above inf), over 288 values from 36 16-byte loads.
+__device__ __forceinline__ uint32_t half_row_max(const uint4* src) {
+  uint32_t m = 0;
+#pragma unroll 6
+  for (int i = 0; i < 36; ++i) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+  }
+  return m;
+}
+
+// Biased exponent that fixes a row's power-of-two query scale: s_r =
+// 2^(134 - e) puts max|q| (exponent e) in [128, 256); clamped so that s_r and
+// 1/s_r are normal floats.
+__device__ __forceinline__ uint32_t row_scale_exp(uint32_t max_bits) {
+  return min(max(max_bits >> 7, 8u), 254u);
+}
+
+}  // namespace
+
+template <bool kLocal>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Misc* misc = reinterpret_cast<Misc*>(smem + kSmemMisc);
+  const ProblemDesc& pd = p.pd;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();                // the planning kernel's work list
+  griddep_launch_dependents();
+
+  const int W = p.hdr->total_cost, per = p.hdr->per_cta;
+  const int lo = blockIdx.x * per;
+  if (lo >= W) return;
+  const int hi = min(lo + per, W);
+  const int U = p.hdr->num_units;
+
+  const uint32_t sQ = smem_u32(smem + kSmemQ);
+  const uint32_t sKV = smem_u32(smem + kSmemKV);
+  const uint32_t sPlo = smem_u32(smem + kSmemPlo);
+  const uint32_t b_kv_full = smem_u32(&misc->kv_full[0]);
+  const uint32_t b_kv_empty = smem_u32(&misc->kv_empty[0]);
+  const uint32_t b_prep = smem_u32(&misc->prep[0]);
+  const uint32_t b_s_full = smem_u32(&misc->s_full[0]);
+  const uint32_t b_s_empty = smem_u32(&misc->s_empty[0]);
+  const uint32_t b_p_full = smem_u32(&misc->p_full[0]);
+  const uint32_t b_pv_done = smem_u32(&misc->pv_done[0]);
+  const uint32_t b_q_conv = smem_u32(&misc->q_conv), b_q_empty = smem_u32(&misc->q_empty);
+  const uint32_t b_o_free = smem_u32(&misc->o_free);
+  volatile int* abort_flag = &misc->abort;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(b_kv_full + 8 * st, 1 + 32);   // expect_tx arrival + one cp.async arrival per lane
+      mbar_init(b_kv_empty + 8 * st, kIssuers);
+      mbar_init(b_prep + 8 * st, 1);
+    }
+    for (int sb = 0; sb < 2; ++sb) {
+      mbar_init(b_s_full + 8 * sb, kIssuers);
+      mbar_init(b_s_empty + 8 * sb, kSoftmaxWarps);
+      mbar_init(b_p_full + 8 * sb, kSoftmaxWarps);
+      mbar_init(b_pv_done + 8 * sb, kIssuers);
+    }
+    mbar_init(b_q_conv, kConvThreads / 32);
+    mbar_init(b_q_empty, kIssuers);
+    mbar_init(b_o_free, kSoftmaxWarps);
+    misc->abort = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < kRows) misc->alpha[0][threadIdx.x] = misc->alpha[1][threadIdx.x] = 1.0f;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_kv);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const uint64_t tmo = p.timeout_ns;
+
+  PieceIter it;
+  it.init(p.prefix, U, lo, hi, p.hdr->unit_cost);
+  int armed_kv[kStages] = {-1, -1, -1, -1};
+  int unit, t0, t1, slot;
+  bool whole;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // nv page boxes per tile: N pages' residue rows for interleaved shards of
+    // a global cache, otherwise one whole page.  Lane k < nv issues box k;
+    // every lane copies the scales of token slots lane and lane + 32.
+    const int nv = (pd.layout == kInterleaved && !kLocal) ? pd.num_shards : 1;
+    const int lg_rows = 6 - (nv == 1 ? 0 : nv == 2 ? 1 : nv == 4 ? 2 : 3);   // log2(64 / nv)
+    const int box_bytes = kStageBytes / nv;
+    int gt = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit<kLocal>(pd, unit);
+      const int npages_b = kLocal ? x.tiles : ceil_div(x.L, kPage);
+      const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
+      const int res = nv > 1 ? x.s : 0;
+      int win_base = -1, win_val = -1;
+      for (int j = t0; j < t1 && ok; ++j, ++gt) {
+        const int st = gt & (kStages - 1);
+        const int first_slot = nv > 1 ? j * nv : (kLocal || pd.layout == kInterleaved ? j : x.p0 + j);
+        const int wb = first_slot & ~31;
+        if (wb != win_base && first_slot < npages_b) {
+          win_base = wb;
+          const int e = wb + lane;
+          win_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
+        }
+        const int idx = first_slot + lane;
+        int page = __shfl_sync(0xffffffffu, win_val, idx & 31);
+        if (lane < nv && idx < npages_b && (page < 0 || page >= pd.num_pages)) {
+          set_error(p, misc, kErrBadPage);
+          page = pd.num_pages;
+        }
+        if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
+        const float* scale_src[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int a = lane + 32 * h;
+          const int k = a >> lg_rows;
+          const int pg = __shfl_sync(0xffffffffu, page, k);
+          const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
+          scale_src[h] = p.kv_scale +
+                         (okpg ? (size_t)pg * kPage + (a & ((1 << lg_rows) - 1)) * nv + res : 0);
+        }
+        if (gt >= kStages) {
+          ok = __all_sync(0xffffffffu, mbar_wait(b_kv_empty + 8 * st, ((gt >> 2) - 1) & 1, tmo,
+                                                 abort_flag));
+          if (!ok) break;
+        }
+        const uint32_t full = b_kv_full + 8 * st;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, kStageBytes);
+          armed_kv[st] = gt;
+        }
+        __syncwarp();
+        if (lane < nv)
+          tma_load_5d(sKV + st * kStageBytes + lane * box_bytes, &tm_kv, full, 0, 0, 0, 0,
+                      page * kPage + res);
+        cp_async_4(smem_u32(&misc->sigma[st][lane]), scale_src[0]);
+        cp_async_4(smem_u32(&misc->sigma[st][lane + 32]), scale_src[1]);
+        cp_async_mbar_arrive_noinc(full);
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else if (warp == 1 || warp == 6) {
+    // ------------------------------------------------------------ MMA issue
+    const int mi = warp == 6 ? 1 : 0;
+    const uint32_t id_qk = idesc_e4m3_f32(64, 64, false, false);
+    // Q (A of QK^T, K-major): 8-row groups 512 bytes apart, chunks 4096;
+    // K (B of QK^T, K-major) and V^T (A of P.V, MN-major: 64-dim blocks 512
+    // apart): 8-slot groups 4608 apart; P_hi in the groups' rope atoms and
+    // P_lo in its own buffer (B of P.V, K-major)
+    const uint64_t dq0 = sw64_desc(sQ, 16, kAtom);
+    const uint64_t dk0 = sw64_desc(sKV, 16, kGroupBytes);
+    const uint64_t dv0 = sw64_desc(sKV, kAtom, kGroupBytes);
+    const uint64_t dph0 = sw64_desc(sKV + kRopeAtom, 16, kGroupBytes);
+    const uint64_t dpl = sw64_desc(sPlo, 16, kAtom);
+    int gbase = 0, pc = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit<kLocal>(pd, unit);
+      const int n = t1 - t0;
+      const uint32_t id_pv = idesc_e4m3_f32(128, x.rows, true, false);
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_conv, pc & 1, tmo, abort_flag));
+      int nq = 0, np = 0;
+      uint64_t t_idle = 0;
+      uint32_t idle_iter = 0;
+      while (ok && np < n) {
+        bool did = false;
+        if (np < nq) {
+          const int g = gbase + np;
+          bool ready = mbar_test(b_p_full + 8 * (g & 1), (g >> 1) & 1);
+          if (ready && np == 0 && pc >= 1) ready = mbar_test(b_o_free, (pc - 1) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            tc_fence_after();
+            if (lane == 0) {
+              const int st = g & (kStages - 1);
+              const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
+#pragma unroll
+              for (int blk = 2 * mi; blk < 2 * mi + 2; ++blk) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                  const uint64_t a =
+                      dv0 + st_off + (uint32_t)((2 * blk * kAtom + kk * 4 * kGroupBytes) >> 4);
+                  const uint32_t d = tmem + kColO + 64 * blk;
+                  mma_e4m3_ss(d, a, dph0 + st_off + (uint32_t)((32 * kk) >> 4), id_pv,
+                              (np == 0 && kk == 0) ? 0u : 1u);
+                  mma_e4m3_ss(d, a, dpl + (uint32_t)((32 * kk) >> 4), id_pv, 1u);
+                }
+              }
+              mma_commit(b_kv_empty + 8 * st);
+              mma_commit(b_pv_done + 8 * (g & 1));
+            }
+            __syncwarp();
+            ++np;
+            did = true;
+          }
+        }
+        if (!did && nq < n) {
+          const int g = gbase + nq;
+          const int st = g & (kStages - 1), sb = g & 1;
+          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 2) & 1);
+          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * sb, ((g >> 1) - 1) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
+              const uint32_t d = tmem + kColS0 + 128 * sb + 64 * mi;
+#pragma unroll
+              for (int c = mi; c < kChunks; c += kIssuers) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                  const uint64_t aq = dq0 + (uint32_t)((c * kQChunkBytes + 32 * k) >> 4);
+                  const uint64_t bk = dk0 + st_off + (uint32_t)((c * kAtom + 32 * k) >> 4);
+                  mma_e4m3_ss(d, aq, bk, id_qk, (c != mi || k != 0) ? 1u : 0u);
+                  mma_e4m3_ss(d, aq + (uint32_t)(kQTermBytes >> 4), bk, id_qk, 1u);
+                }
+              }
+              mma_commit(b_s_full + 8 * sb);
+              if (nq == n - 1) mma_commit(b_q_empty);
+            }
+            __syncwarp();
+            ++nq;
+            did = true;
+          }
+        }
+        if (did) {
+          t_idle = 0;
+          idle_iter = 0;
+        } else if ((++idle_iter & 63u) == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (now - t_idle > tmo || *abort_flag) ok = false;
+          ok = __all_sync(0xffffffffu, ok);
+        }
+      }
+      gbase += n;
+      ++pc;
+    }
+    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else if (warp >= 7) {
+    // ------------------------------------------------------------ splitters
+    // Per piece, thread (r, hh) = (ct / 2, ct % 2) splits dims [288 hh,
+    // 288 hh + 288) of query row r into Q_hi / Q_lo; warp 7 then splits the
+    // token scales of each of the piece's tiles as they land.
+    const int ct = threadIdx.x - 7 * 32;
+    const int r = ct >> 1, hh = ct & 1;
+    int gt = 0, pc = 0;
+    bool ok = true;
+    while (it.next(unit, t0, t1, whole, slot)) {
+      if (pc >= 1 && ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
+      // every splitter reaches this barrier once per piece, failure or not
+      if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
+      Unit x = make_unit<kLocal>(pd, unit);
+      {
+        const bool live = r < x.rows;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)x.b * pd.R + (size_t)x.g * kRows + r) * kDqk + 288 * hh);
+        uint32_t mx = live ? half_row_max(src) : 0u;
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        if (live && (mx >> 7) == 255u) atomicOr(&p.hdr->err, kErrQRange);   // inf or NaN
+        const float s = __uint_as_float((261u - row_scale_exp(mx)) << 23);
+        uint8_t* qh = smem + kSmemQ;
+        uint8_t* ql = qh + kQTermBytes;
+#pragma unroll 4
+        for (int i = 0; i < 36; ++i) {
+          uint32_t whi = 0, wlo = 0, whi2 = 0, wlo2 = 0;
+          if (live) {
+            const uint4 v = __ldg(src + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t sp[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              sp[k] = split_e4m3x2(__uint_as_float(w[k] << 16) * s,
+                                   __uint_as_float(w[k] & 0xFFFF0000u) * s);
+            whi = (sp[0] & 0xFFFFu) | (sp[1] << 16);
+            wlo = (sp[0] >> 16) | (sp[1] & 0xFFFF0000u);
+            whi2 = (sp[2] & 0xFFFFu) | (sp[3] << 16);
+            wlo2 = (sp[2] >> 16) | (sp[3] & 0xFFFF0000u);
+          }
+          const int d0 = 288 * hh + 8 * i;          // first of these 8 dims
+          const int c = d0 >> 6, within = d0 & 63;
+          const uint32_t off = c * kQChunkBytes + sw64_off(r, within >> 4, kAtom) + (within & 15);
+          *reinterpret_cast<uint2*>(qh + off) = make_uint2(whi, whi2);
+          *reinterpret_cast<uint2*>(ql + off) = make_uint2(wlo, wlo2);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_q_conv);
+      }
+      if (warp == 7) {
+        for (int j = t0; j < t1; ++j, ++gt) {
+          const int st = gt & (kStages - 1);
+          if (ok) ok = __all_sync(0xffffffffu,
+                                  mbar_wait(b_kv_full + 8 * st, (gt >> 2) & 1, tmo, abort_flag));
+          if (!ok) continue;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int a = lane + 32 * h;
+            float sg = misc->sigma[st][a];
+            uint32_t bits = __float_as_uint(sg);
+            uint32_t eb = (bits >> 23) & 0xFFu;
+            if (eb < 27u) {
+              // zero, subnormal or below 2^-100: as 2^-60 (its values are
+              // negligible next to any normal token's, its logit ~0)
+              sg = copysignf(8.6736174e-19f, sg);
+              bits = __float_as_uint(sg);
+              eb = (bits >> 23) & 0xFFu;
+            }
+            float lg, inv, mt;
+            if (eb >= 253u) {   // inf, NaN or >= 2^126: propagate, as the dequantised values would
+              lg = 0.0f;
+              inv = sg;
+              mt = sg;
+            } else {
+              lg = (float)((int)eb - 126);
+              inv = __uint_as_float((253u - eb) << 23);
+              mt = __uint_as_float((bits & 0x807FFFFFu) | (126u << 23));
+            }
+            misc->sigma[st][a] = sg;
+            misc->lge[st][a] = lg;
+            misc->il[st][a] = inv;
+            misc->mant[st][a] = mt;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_prep + 8 * st);
+        }
+      } else {
+        gt += t1 - t0;
+      }
+      ++pc;
+    }
+    if (!ok && ct == 0) set_error(p, misc, kErrTimeout);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;
+    const int tid = threadIdx.x - 64;    // 0..127
+    const int half = lane >> 4;
+    const int r = 16 * quad + (lane & 15);
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    uint8_t* plo_row = smem + kSmemPlo + (r >> 3) * kAtom + (r & 7) * 64;   // P_lo row r
+    int gt = 0, pc = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      Unit x = make_unit<kLocal>(pd, unit);
+      const bool owner = r < x.rows;
+      const int i_row = (x.g * kRows + r) / pd.H;
+      const int vis_limit = x.L - x.qn + i_row;
+      // the row's query scale, computed exactly as the splitters do
+      float qs;
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)x.b * pd.R + (size_t)x.g * kRows + r) * kDqk + 288 * half);
+        uint32_t mx = owner ? half_row_max(src) : 0u;
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        qs = __uint_as_float((row_scale_exp(mx) - 7u) << 23) * pd.scale_log2;
+      }
+      float m_run = -CUDART_INF_F, l_run = 0.0f;
+      for (int j = t0; j < t1; ++j, ++gt) {
+        const int sb = gt & 1, st = gt & (kStages - 1);
+        bool ok_s = __all_sync(
+            0xffffffffu, ok && mbar_wait(b_s_full + 8 * sb, (gt >> 1) & 1, tmo, abort_flag));
+        ok_s = __all_sync(0xffffffffu,
+                          ok_s && mbar_wait(b_prep + 8 * st, (gt >> 2) & 1, tmo, abort_flag));
+        bool resc = false;
+        uint32_t phi[8], plo[8];
+        const bool full = tile_full<kLocal>(pd, x, j);
+        if (ok_s) {
+          tc_fence_after();
+          uint32_t sr[32], sr2[32];
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb, sr);
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb + 64, sr2);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
+          // b_t = S_t sigma_t / s_r * scale * log2(e) + E_t + 1
+          float b[32];
+          {
+            const float4* sg4 = reinterpret_cast<const float4*>(&misc->sigma[st][32 * half]);
+            const float4* lg4 = reinterpret_cast<const float4*>(&misc->lge[st][32 * half]);
+#pragma unroll
+            for (int a4 = 0; a4 < 8; ++a4) {
+              const float4 sg = sg4[a4], lg = lg4[a4];
+              const float s0 = __uint_as_float(sr[4 * a4]) + __uint_as_float(sr2[4 * a4]);
+              const float s1 = __uint_as_float(sr[4 * a4 + 1]) + __uint_as_float(sr2[4 * a4 + 1]);
+              const float s2 = __uint_as_float(sr[4 * a4 + 2]) + __uint_as_float(sr2[4 * a4 + 2]);
+              const float s3 = __uint_as_float(sr[4 * a4 + 3]) + __uint_as_float(sr2[4 * a4 + 3]);
+              b[4 * a4] = fmaf(s0 * sg.x, qs, lg.x);
+              b[4 * a4 + 1] = fmaf(s1 * sg.y, qs, lg.y);
+              b[4 * a4 + 2] = fmaf(s2 * sg.z, qs, lg.z);
+              b[4 * a4 + 3] = fmaf(s3 * sg.w, qs, lg.w);
+            }
+          }
+          uint32_t vis_mask = 0xFFFFFFFFu;
+          if (!full) {
+#pragma unroll
+            for (int a = 0; a < 32; ++a) {
+              int t = slot_token<kLocal>(pd, x, j, 32 * half + a);
+              bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
+              if (!vis) {
+                b[a] = -CUDART_INF_F;
+                vis_mask &= ~(1u << a);
+              }
+            }
+          }
+          float m4[4] = {b[0], b[1], b[2], b[3]};
+#pragma unroll
+          for (int a = 4; a < 32; a += 4) {
+            m4[0] = fmaxf(m4[0], b[a]);
+            m4[1] = fmaxf(m4[1], b[a + 1]);
+            m4[2] = fmaxf(m4[2], b[a + 2]);
+            m4[3] = fmaxf(m4[3], b[a + 3]);
+          }
+          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run, mx);
+          float alpha = 1.0f;
+          if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
+            alpha = (m_run == -CUDART_INF_F) ? 0.0f : ex2_approx(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            resc = owner && (j != t0);
+          }
+          if (owner && half == 0) misc->alpha[gt & 1][r] = alpha;
+          const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+          // e_t = 2^(b_t - m); P'_t = e_t mant_t; l += e_t 2^-(E_t+1)
+          const float4* mt4 = reinterpret_cast<const float4*>(&misc->mant[st][32 * half]);
+          const float4* il4 = reinterpret_cast<const float4*>(&misc->il[st][32 * half]);
+          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int a4 = 0; a4 < 8; ++a4) {
+            float4 mt = mt4[a4], iv = il4[a4];
+            if (vis_mask != 0xFFFFFFFFu) {
+              // a masked slot's scale may be garbage (even NaN)
+              if (!(vis_mask >> (4 * a4) & 1u)) mt.x = iv.x = 0.0f;
+              if (!(vis_mask >> (4 * a4 + 1) & 1u)) mt.y = iv.y = 0.0f;
+              if (!(vis_mask >> (4 * a4 + 2) & 1u)) mt.z = iv.z = 0.0f;
+              if (!(vis_mask >> (4 * a4 + 3) & 1u)) mt.w = iv.w = 0.0f;
+            }
+            const float e0 = ex2_approx(b[4 * a4] - m_use);
+            const float e1 = ex2_approx(b[4 * a4 + 1] - m_use);
+            const float e2 = ex2_approx(b[4 * a4 + 2] - m_use);
+            const float e3 = ex2_approx(b[4 * a4 + 3] - m_use);
+            ls4[0] = fmaf(e0, iv.x, ls4[0]);
+            ls4[1] = fmaf(e1, iv.y, ls4[1]);
+            ls4[2] = fmaf(e2, iv.z, ls4[2]);
+            ls4[3] = fmaf(e3, iv.w, ls4[3]);
+            const uint32_t s01 = split_e4m3x2(e0 * mt.x, e1 * mt.y);
+            const uint32_t s23 = split_e4m3x2(e2 * mt.z, e3 * mt.w);
+            phi[a4] = (s01 & 0xFFFFu) | (s23 << 16);
+            plo[a4] = (s01 >> 16) | (s23 & 0xFFFF0000u);
+          }
+          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        }
+        bool waited_pv = false;
+        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, resc || !ok_s)) {
+          if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
+          // some row's running max grew: rescale O^T once the previous P.V landed
+          const bool ok_pv = __all_sync(
+              0xffffffffu, (gt == 0) || mbar_wait(b_pv_done + 8 * ((gt - 1) & 1),
+                                                  ((gt - 1) >> 1) & 1, tmo, abort_flag));
+          ok = ok_pv;
+          waited_pv = true;
+          if (!ok_pv) continue;  // caught by the next reduction (or the epilogue's)
+          tc_fence_after();
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v[32];
+              const uint32_t ta = tmem + lane_off + kColO + 64 * blk + 32 * h2;
+              tmem_ld32(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[gt & 1][32 * h2 + c]);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+        // P_lo has one buffer: the previous tile's P.V must have read it
+        if (!waited_pv && gt > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done + 8 * ((gt - 1) & 1),
+                                                 ((gt - 1) >> 1) & 1, tmo, abort_flag));
+          if (!ok) continue;
+        }
+        uint8_t* stage = smem + kSmemKV + st * kStageBytes;
+        if (owner) {
+          // this thread's 32 tokens are 16-byte units 2 half, 2 half + 1 of the row
+          uint8_t* hrow = stage + (r >> 3) * kGroupBytes + kRopeAtom + (r & 7) * 64;
+          const int sw = (r & 7) >> 1;
+          *reinterpret_cast<uint4*>(hrow + (((2 * half) ^ sw) << 4)) =
+              make_uint4(phi[0], phi[1], phi[2], phi[3]);
+          *reinterpret_cast<uint4*>(hrow + (((2 * half + 1) ^ sw) << 4)) =
+              make_uint4(phi[4], phi[5], phi[6], phi[7]);
+          *reinterpret_cast<uint4*>(plo_row + (((2 * half) ^ sw) << 4)) =
+              make_uint4(plo[0], plo[1], plo[2], plo[3]);
+          *reinterpret_cast<uint4*>(plo_row + (((2 * half + 1) ^ sw) << 4)) =
+              make_uint4(plo[4], plo[5], plo[6], plo[7]);
+        }
+        if (!full) {
+          // zero the value codes of slots that hold no valid token of this
+          // shard, so that garbage (even NaN codes) cannot reach O
+          for (int e = tid; e < kTile * 32; e += kSoftmaxThreads) {
+            const int a = e >> 5, c = (e >> 2) & 7, u = e & 3;
+            const int t = slot_token<kLocal>(pd, x, j, a);
+            if (!slot_valid(pd, x, t))
+              *reinterpret_cast<uint4*>(stage + (a >> 3) * kGroupBytes + c * kAtom + (a & 7) * 64 +
+                                        u * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p_full + 8 * (gt & 1));
+      }
+      // ---------------------------------------------------------- epilogue
+      const bool ok_e = __all_sync(
+          0xffffffffu, ok && mbar_wait(b_pv_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, tmo,
+                                       abort_flag));
+      if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_e)) { ok = false; break; }
+      tc_fence_after();
+      float* dst_o;
+      float* dst_lse;
+      if (whole) {
+        size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
+        dst_o = p.out_partial + row0 * kDv;
+        dst_lse = p.lse_partial + row0;
+      } else {
+        size_t sl = 2 * (size_t)blockIdx.x + slot;
+        dst_o = p.ws_o + sl * kRows * kDv;
+        dst_lse = p.ws_lse + sl * kRows;
+      }
+      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+      if (owner && half == 0) {
+        float lse = (l_tot > 0.0f) ? (m_run + __log2f(l_tot)) * 0.69314718055994530942f
+                                   : -CUDART_INF_F;
+        misc->inv_l[r] = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
+        dst_lse[r] = lse;
+      }
+      if (whole) {
+        for (int e = tid; e < (x.rows_out - x.rows) * (kDv / 4); e += kSoftmaxThreads)
+          reinterpret_cast<float4*>(dst_o + (size_t)x.rows * kDv)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int rr = x.rows + tid; rr < x.rows_out; rr += kSoftmaxThreads)
+          dst_lse[rr] = -CUDART_INF_F;
+      }
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      {
+        const uint32_t o_base = tmem + lane_off + kColO;
+        auto store32 = [&](int k, const uint32_t (&v)[32]) {
+          const int dim = 128 * (k >> 1) + 32 * quad + lane;
+          float il[32];
+          const float4* il4 = reinterpret_cast<const float4*>(misc->inv_l + 32 * (k & 1));
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 t = il4[c4];
+            il[4 * c4] = t.x;
+            il[4 * c4 + 1] = t.y;
+            il[4 * c4 + 2] = t.z;
+            il[4 * c4 + 3] = t.w;
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int row = 32 * (k & 1) + c;
+            if (row < x.rows) dst_o[(size_t)row * kDv + dim] = __uint_as_float(v[c]) * il[c];
+          }
+        };
+        uint32_t va[32], vb[32];
+        tmem_ld32(o_base, va);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          tmem_ld32(o_base + 32 * (k + 1), vb);
+          tmem_wait_ld();
+          store32(k, va);
+          if (k + 2 < 8) tmem_ld32(o_base + 32 * (k + 2), va);
+          store32(k + 1, vb);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_o_free);
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // inv_l reused by the next piece
+      ++pc;
+    }
+    if (!ok && tid == 0) set_error(p, misc, kErrTimeout);
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // after a failure, let this CTA's own copies land before it exits
+    int never = 0;
+    for (int st = 0; st < kStages; ++st)
+      if (armed_kv[st] >= 0)
+        mbar_wait(b_kv_full + 8 * st, (armed_kv[st] >> 2) & 1, tmo, &never);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool kLocal>
+static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_kv, const PartialParams& p,
+                                           int grid, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_fp8_kernel<kLocal>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_partial_fp8_kernel<kLocal>, tm_kv, p);
+}
+
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_kv, const PartialParams& p, int grid,
+                               cudaStream_t stream) {
+  return p.pd.local ? launch_partial_fp8_impl<true>(tm_kv, p, grid, stream)
+                    : launch_partial_fp8_impl<false>(tm_kv, p, grid, stream);
+}
+
+}  // namespace mla

@@ -268,6 +268,17 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D(tmem) (+)= A(smem) * B(smem)^T, kind::f8f6f4 (e4m3 in, fp32 accumulate).
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every previously issued tcgen05.mma completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -346,6 +357,20 @@ __host__ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t
   return d;
 }
 
+// The same with 64-byte swizzling (K-major: 8-row groups of 64-byte rows,
+// SBO apart; MN-major: LBO between 64-element MN blocks, SBO between 8-row K
+// groups).
+__host__ __device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t lbo,
+                                                       uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;   // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
@@ -359,6 +384,40 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
                                                      bool b_mn_major) {
   return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0)
+// and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Two fp32 values -> two OCP e4m3 codes (round to nearest even, finite
+// values beyond 448 saturate), x0 in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float x0, float x1) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+
+// Two e4m3 codes (low byte first) -> their two values as fp32 (exact).
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& x0, float& x1) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(codes & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(x0) : "h"((unsigned short)(h & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(x1) : "h"((unsigned short)(h >> 16)));
+}
+
+// x0, x1 as two-term e4m3 sums hi + lo: hi = e4m3(x), lo = e4m3(x - hi).
+// Returns the hi codes in bits 0..15 and the lo codes in bits 16..31.
+__device__ __forceinline__ uint32_t split_e4m3x2(float x0, float x1) {
+  const uint32_t hi = f32x2_to_e4m3x2(x0, x1);
+  float h0, h1;
+  e4m3x2_to_f32x2(hi, h0, h1);
+  const uint32_t lo = f32x2_to_e4m3x2(x0 - h0, x1 - h1);
+  return hi | (lo << 16);
 }
 
 }  // namespace mla

@@ -177,25 +177,66 @@ def test_fp8_causal_verify_with_wuv(dev):
     compare_all(w, dev)
 
 
-def test_fp8_query_beyond_fp16_range_is_reported(dev):
-    """With fp8 caches the tensor cores run on fp16 operands; a finite query
-    value that fp16 cannot hold is reported, not silently turned into inf."""
-    import sequence_sharded_mla_gb300 as mla
-    w = mi.build_workload("fp8big", 1, 1, 16, [100], 2, "interleaved", "fp8", False, seed=420,
+def test_fp8_query_of_any_finite_magnitude(dev):
+    """With fp8 caches the query enters the tensor cores as a two-term e4m3
+    sum under a per-row power-of-two scale.  The cache's scales are divided by
+    2^20 and one head's query multiplied by 2^20 (|q| up to ~1e6, beyond fp16),
+    another's divided by 2^100: all rows match the oracle."""
+    import numpy as np
+    w = mi.build_workload("fp8big", 2, 1, 16, [100, 700], 2, "interleaved", "fp8", False,
+                          seed=420, kv_sigma=1.0)
+    w.kv_scale *= np.float32(2.0 ** -20)
+
+    def shift_exponent(x, k):   # multiply nonzero bf16 patterns by 2^k
+        nz = (x & 0x7F80) != 0
+        x[nz] = (x[nz].astype(np.int32) + (k << 7)).astype(np.uint16)
+
+    for b in range(2):
+        shift_exponent(w.q[b, 0, 3, :], 20)
+        shift_exponent(w.q[b, 0, 5, :], -100)
+    assert np.max(np.abs(mi.bf16_bits_to_f32(w.q[0, 0, 3, :]))) > 65504.0
+    compare_all(w, dev)
+
+
+def test_fp8_nonfinite_query_is_reported(dev):
+    """An inf or NaN query component of a row that attends is reported as
+    MLA_ERR_RANGE; a padding row's garbage is not."""
+    w = mi.build_workload("fp8inf", 1, 1, 16, [100], 2, "interleaved", "fp8", False, seed=421,
                           kv_sigma=1.0)
-    w.q[0, 0, 3, 7] = 0x4780          # bf16 65536.0
+    w.q[0, 0, 3, 7] = 0x7F80          # bf16 +inf
     res = run_gpu(w, dev, with_wuv=False)
     assert res["status"] == -7          # MLA_ERR_RANGE
-    assert mla.mla_get_device_error(res["workspace"]) == 0
-    w.q[0, 0, 3, 7] = 0x477F          # bf16 65280.0: representable in fp16
+    w.q[0, 0, 3, 7] = 0x7FC0          # bf16 NaN
+    res = run_gpu(w, dev, with_wuv=False)
+    assert res["status"] == -7
+    # the second query slot of the request is padding (q_lens = 1)
+    w = mi.build_workload("fp8pad", 1, 2, 16, [100], 2, "interleaved", "fp8", True, seed=422,
+                          kv_sigma=1.0, q_lens=[1])
+    w.q[0, 1, :, :] = 0x7FC0
     res = run_gpu(w, dev, with_wuv=False)
     assert res["status"] == 0
 
 
+def test_fp8_token_scales_of_any_magnitude(dev):
+    """Token scales multiplied by 2^k, k uniform in [-40, 2] (logits stay of
+    order 10, the values span 2^42), some exactly zero and some negative: the
+    exponent split of the scales keeps P' inside e4m3 and the normaliser
+    exact, so the many near-zero-logit tokens keep their weight."""
+    import numpy as np
+    w = mi.build_workload("fp8sc", 3, 2, 32, [130, 1000, 4100], 4, "interleaved", "fp8", True,
+                          seed=450, kv_sigma=1.0)
+    rng = np.random.default_rng(451)
+    sc = w.kv_scale.reshape(-1)
+    sc *= np.exp2(rng.integers(-40, 3, size=sc.shape)).astype(np.float32)
+    sc[rng.random(sc.shape) < 0.02] = 0.0
+    neg = rng.random(sc.shape) < 0.05
+    sc[neg] = -sc[neg]
+    compare_all(w, dev)
+
+
 def test_fp8_small_query_values_stay_within_tolerance(dev):
-    """Query components far below the fp16 normal range (2^-14) are rounded
-    to fp16 subnormals; the result still matches the oracle, which keeps the
-    exact bf16 values."""
+    """Tiny query components (sigma 1e-5): the per-row power-of-two scale
+    brings them into the e4m3 range before the two-term split."""
     w = mi.build_workload("fp8tiny", 2, 1, 32, [700, 1300], 2, "contiguous", "fp8", False,
                           seed=430, kv_sigma=1.0, q_sigma=1e-5)
     compare_all(w, dev)
