@@ -276,7 +276,8 @@ class Case:
     device copies, output buffers, and the step (the library calls)."""
 
     def __init__(self, name, kv_bytes, config, pairs, outputs, workspace, step, dtype, kernel,
-                 kernel_src, cpu, flops=0.0, combine_bytes=0.0, tensor_bound=False):
+                 kernel_src, cpu, flops=0.0, combine_bytes=0.0, tensor_bound=False,
+                 tensor_fp8=False):
         self.name, self.kv_bytes, self.config = name, kv_bytes, config
         self.pairs = pairs            # [(pinned host tensor, device tensor)] copied per e2e step
         self.outputs = outputs        # [(device tensor, pinned host tensor)] read per e2e step
@@ -286,6 +287,7 @@ class Case:
         self.flops = flops            # useful MMA flops of the partial kernel per step
         self.combine_bytes = combine_bytes   # bytes the combine kernel reads and writes
         self.tensor_bound = tensor_bound     # the dense contractions bound the partial kernel
+        self.tensor_fp8 = tensor_fp8         # the contractions run on e4m3 operands
 
 
 def visible_pairs(seq_lens, q_len, causal):
@@ -350,15 +352,17 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
               "num_shards": N, "layout": w.layout, "kv_dtype": w.kv_dtype,
               "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
               "total_tokens_per_gpu": w.total_tokens}
-    kernel = "mla_partial_kernel<%s,false>" % ("true" if w.kv_dtype == "fp8" else "false")
+    fp8 = w.kv_dtype == "fp8"
+    kernel = "mla_partial_fp8_kernel<false>" if fp8 else "mla_partial_kernel<false>"
     rows = B * q_len * H
     flops = 2.0 * H * (576 + 512) * visible_pairs(w.seq_lens, q_len, w.causal)
     comb = N * rows * (512 * 4 + 4) + rows * ((128 if d_wuv is not None else 512) * 2 + 4)
     if d_wuv is not None:
         comb += d_wuv.numel() * 2
-    return Case(config["workload"], w.kv_bytes(), config, pairs, outputs, ws, step, "bf16",
-                kernel, "partial.cu", lambda budget, orc: cpu_sample(w, budget, orc), flops=flops,
-                combine_bytes=comb, tensor_bound=q_len * H > 64)
+    return Case(config["workload"], w.kv_bytes(), config, pairs, outputs, ws, step,
+                "e4m3" if fp8 else "bf16", kernel, "partial_fp8.cu" if fp8 else "partial.cu",
+                lambda budget, orc: cpu_sample(w, budget, orc), flops=flops,
+                combine_bytes=comb, tensor_bound=q_len * H > 64, tensor_fp8=fp8)
 
 
 def gqa_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
@@ -504,10 +508,18 @@ def run_gpu(args, world, rank, local, dist):
                 "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                 "traffic": traffic}
     tflops = case.flops / (kernel_avg_ms / 1e3) / 1e12
+    if case.tensor_fp8:
+        # e4m3 contractions: the measured bf16 rate x the nominal fp8 / bf16
+        # ratio (4.5 / 2.25); the kernel executes twice the useful flops
+        # (two-term query and probabilities)
+        tpeak = tpeak * 2.0
+        tsrc = (f"{tpeak_kind} x 2 (nominal e4m3 / bf16 dense ratio); useful MMA flops "
+                "2*H*(Dk+Dv) per visible token and query, executed twice (two-term q and P)")
+    else:
+        tsrc = (f"{tpeak_kind} (dense fp16/bf16 rate; useful MMA flops "
+                "2*H*(Dk+Dv) per visible token and query)")
     tensor_roof = {"kernel": case.kernel, "bound": "tensor", "achieved": tflops, "peak": tpeak,
-                   "unit": "TFLOP/s", "frac": tflops / tpeak,
-                   "peak_source": f"{tpeak_kind} (dense fp16/bf16 rate; useful MMA flops "
-                                  "2*H*(Dk+Dv) per visible token and query)",
+                   "unit": "TFLOP/s", "frac": tflops / tpeak, "peak_source": tsrc,
                    "traffic": traffic}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

@@ -17,8 +17,8 @@ namespace mla {
 int partial_smem_bytes();
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const PartialParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_partial_fp8(const CUtensorMap& tm_kv, const PartialParams& p, int grid,
-                               cudaStream_t stream);
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                               const PartialParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
                         int min_tiles, int unit_cost, cudaStream_t stream);
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
@@ -193,7 +193,19 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // the group-major shared-memory layout.
   const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
+  CUtensorMap tm_q8;
   if (fp8) {
+    // query rows for the fp8 kernel, by 8-row groups: view (64 dims, row in
+    // group, chunk, row group) with strides (-, 1152, 128, 9216); a box lands
+    // a 64-row group as [row group][chunk][row][64], 9216 bytes per row group
+    cuuint64_t qd[4] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)pd.B * pd.R / 8};
+    cuuint64_t qs[3] = {(cuuint64_t)kDqk * 2, 128, (cuuint64_t)kDqk * 2 * 8};
+    cuuint32_t qb[4] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kRows / 8)};
+    cuuint32_t qe[4] = {1, 1, 1, 1};
+    if (encode(&tm_q8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), qd, qs, qb, qe,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
     // e4m3 codes: the same view with 64-code chunks, strides (-, 576 nv, 64,
     // 4608 nv, 576) and 64-byte swizzling: a box lands a page's residue rows,
     // all nine chunks, in the group-major layout of the fp8 kernel
@@ -205,7 +217,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   } else {
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
@@ -216,7 +228,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   }
 
@@ -241,7 +253,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   void* ev1 = host::g_ev_after.load();
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const cudaError_t le = fp8 ? launch_partial_fp8(tm_kv, p, grid, st)
+  const cudaError_t le = fp8 ? launch_partial_fp8(tm_q8, tm_kv, p, grid, st)
                              : launch_partial_bf16(tm_q, tm_kv, p, grid, st);
   if (ev1 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev1), st) != cudaSuccess)
     return MLA_ERR_CUDA;

@@ -1,4 +1,5 @@
-// Sequence-sharded MLA decode: per-shard partial attention on tcgen05.
+// Sequence-sharded MLA decode: per-shard partial attention on tcgen05, bf16
+// caches (fp8 caches: partial_fp8.cu).
 //
 // Computes, for every (request b, shard s, group of 64 query rows), the
 // attention of the absorbed queries over the shard's slice of the paged
@@ -37,23 +38,11 @@
 //               O^T is rescaled in TMEM only when a running max grows by more
 //               than 2^8; the epilogue writes o = O / l and lse = m + ln l.
 //
-// fp8 caches (OCP e4m3 codes + one fp32 scale per token): the MMAs run on
-// fp16 operands.  The producer lands a tile's codes (36 KB) in the upper half
-// of the tile's 72 KB stage, one TMA box per page, and the token scales next
-// to it (4-byte cp.async counted on the same barrier); warps 7..10 expand the
-// codes to fp16 in place (e4m3 -> fp16 is exact and one instruction per two
-// codes) in the swizzled layout the MMAs read, and convert each piece's query
-// group from bf16 to fp16 once (exact for magnitudes in [2^-17, 65504]; a
-// larger value sets an error bit).  The scales are folded into the logits and
-// into P before its fp16 rounding, so both MMAs see the exact dequantised
-// values.
-//
 // Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
 // [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
 // written straight to out_partial; pieces of a split unit go to workspace
 // slots and are merged by mla_merge_kernel.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -64,11 +53,6 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 224;
-constexpr int kThreadsFp8 = 352;           // + four converter warps (7..10)
-constexpr int kConvThreads = 128;
-constexpr uint32_t kBarConv = 2;           // named barrier id for the converter warps
-constexpr int kFp8TileBytes = kTile * kDqk;  // 36864: codes of one tile
-constexpr int kFp8Staging = kTileBytes - kFp8TileBytes;  // codes land in the stage's upper half
 constexpr int kIssuers = 2;                // MMA-issuing warps (1 and 6)
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
@@ -81,14 +65,11 @@ struct Misc {
   // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
   // single barrier could complete two phases between tests and alias parities
   uint64_t p_full[2], pv_done[2];
-  uint64_t kv_conv[2];  // fp8: stage expanded to fp16
   uint64_t q_full, q_empty, o_free;
-  uint64_t q_conv;      // fp8: query group converted to fp16
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
   alignas(16) float inv_l[kRows];
-  float scale[2][kTile];  // fp8: per-token scales of the tile in each stage
 };
 
 constexpr int kSmemQ = 0;
@@ -117,15 +98,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 }  // namespace
 
-template <bool kFp8, bool kLocal>
-__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
+template <bool kLocal>
+__global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -155,18 +131,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   const uint32_t b_q_full = smem_u32(&misc->q_full), b_q_empty = smem_u32(&misc->q_empty);
   const uint32_t b_p_full = smem_u32(&misc->p_full[0]), b_pv_done = smem_u32(&misc->pv_done[0]);
   const uint32_t b_o_free = smem_u32(&misc->o_free);
-  const uint32_t b_kv_conv = smem_u32(&misc->kv_conv[0]);
-  const uint32_t b_q_conv = smem_u32(&misc->q_conv);
-  // the MMAs wait for the query group in its operand type
-  const uint32_t b_q_ready = kFp8 ? b_q_conv : b_q_full;
-  // the MMAs wait for the stage in bf16: straight from TMA, or after expansion
-  const uint32_t b_kv_ready = kFp8 ? b_kv_conv : b_kv_full;
   volatile int* abort_flag = &misc->abort;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
-      mbar_init(b_kv_full + 8 * st, kFp8 ? 1 + 32 : 1);  // fp8: + one cp.async arrival per lane
-      mbar_init(b_kv_conv + 8 * st, kConvThreads / 32);
+      mbar_init(b_kv_full + 8 * st, 1);
       mbar_init(b_kv_empty + 8 * st, kIssuers);
       mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
@@ -174,7 +143,6 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       mbar_init(b_pv_done + 8 * st, kIssuers);
     }
     mbar_init(b_q_full, 1);
-    mbar_init(b_q_conv, kConvThreads / 32);
     mbar_init(b_q_empty, kIssuers);
     mbar_init(b_o_free, kSoftmaxWarps);
     misc->abort = 0;
@@ -235,22 +203,6 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           page = pd.num_pages;
         }
         if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
-        // fp8: the sources of this lane's two token-scale copies (slots lane,
-        // lane + 32), formed before the stage is free; rows_per = 64 / nv is
-        // a power of two
-        const float* scale_src[2] = {nullptr, nullptr};
-        if constexpr (kFp8) {
-          const int lg_rows = 6 - (nv == 1 ? 0 : nv == 2 ? 1 : nv == 4 ? 2 : 3);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int a = lane + 32 * h;             // token slot
-            const int k = a >> lg_rows;              // page box of the slot
-            const int pg = __shfl_sync(0xffffffffu, page, k);
-            const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
-            scale_src[h] = p.kv_scale +
-                           (okpg ? (size_t)pg * kPage + (a & ((1 << lg_rows) - 1)) * nv + res : 0);
-          }
-        }
         if (gt >= 2) {
           ok = __all_sync(0xffffffffu,
                           mbar_wait(b_kv_empty + 8 * st, ((gt >> 1) - 1) & 1, tmo, abort_flag));
@@ -258,20 +210,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         }
         const uint32_t full = b_kv_full + 8 * st;
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, kFp8 ? kFp8TileBytes : kTileBytes);
+          mbar_arrive_expect_tx(full, kTileBytes);
           armed_kv[st] = gt;
         }
         __syncwarp();
-        if constexpr (kFp8) {
-          // codes: one box per page, rows of 576 codes (row-major) in the
-          // stage's upper half; scales: one 4-byte copy per token slot
-          if (lane < nv)
-            tma_load_5d(sKV + st * kTileBytes + kFp8Staging + lane * (kTile / nv) * kDqk, &tm_kv,
-                        full, 0, 0, res, 0, page);
-          cp_async_4(smem_u32(&misc->scale[st][lane]), scale_src[0]);
-          cp_async_4(smem_u32(&misc->scale[st][lane + 32]), scale_src[1]);
-          cp_async_mbar_arrive_noinc(full);
-        } else if (lane < nv) {
+        if (lane < nv) {
           // cache row page*64 + res of the (row-in-group, chunk, group, row)
           // view; a page of num_pages is out of range and fills zeros
           tma_load_5d(sKV + st * kTileBytes + lane * box_bytes, &tm_kv, full, 0, 0, 0, 0,
@@ -306,8 +249,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ MMA issue
     const int mi = warp == 6 ? 1 : 0;    // issuer index: chunk parity / latent half
-    const uint32_t id_qk = kFp8 ? idesc_f16_f32(64, 64, false, false)
-                                : idesc_bf16_f32(64, 64, false, false);
+    const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
     // descriptor bases; adding (byte offset >> 4) moves the start address
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
     // K (B of QK^T, K-major): 8-slot groups 9216 bytes apart; V^T (A of P.V,
@@ -321,9 +263,8 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
       const int n = t1 - t0;
-      const uint32_t id_pv = kFp8 ? idesc_f16_f32(128, x.rows, true, false)
-                                  : idesc_bf16_f32(128, x.rows, true, false);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_q_ready, pc & 1, tmo, abort_flag));
+      const uint32_t id_pv = idesc_bf16_f32(128, x.rows, true, false);
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
       int nq = 0, np = 0;
       uint64_t t_idle = 0;
       uint32_t idle_iter = 0;
@@ -365,7 +306,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         if (!did && nq < n) {
           const int g = gbase + nq;
           const int st = g & 1;
-          bool ready = mbar_test(b_kv_ready + 8 * st, (g >> 1) & 1);
+          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 1) & 1);
           if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * st, ((g >> 1) - 1) & 1);
           if (__all_sync(0xffffffffu, ready)) {
             tc_fence_after();
@@ -407,78 +348,6 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (kFp8 && warp >= 7) {
-    // ------------------------------------------------------------ fp8 -> fp16
-    // Per piece, the query group is converted bf16 -> fp16 in place first.
-    // Per tile, thread t expands the 16-code quarter t%4 of every 64-wide
-    // chunk of rows t/4 and 32 + t/4 into those rows' swizzled fp16 atoms.
-    // The low row lands below the codes and is expanded at once; the high row
-    // lands on top of the codes of every row, so its codes wait in registers
-    // for the barrier over the converter warps that says all codes were read.
-    const int ct = threadIdx.x - 7 * 32;   // 0..127
-    const int qq = ct & 3, row_lo = ct >> 2, row_hi = row_lo + kTile / 2;
-    int gt = 0, pc = 0;
-    bool ok = true;
-    while (ok && it.next(unit, t0, t1, whole, slot)) {
-      {
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
-        if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
-        uint4* q4 = reinterpret_cast<uint4*>(smem + kSmemQ);
-        const int rows_q = make_unit<kLocal>(pd, unit).rows;   // padding rows may hold anything
-        bool big = false;
-#pragma unroll 4
-        for (int i = ct; i < kTileBytes / 16; i += kConvThreads) {
-          uint4 v = q4[i];
-          bool b = false;
-          v.x = bf16x2_to_f16x2(v.x, b);
-          v.y = bf16x2_to_f16x2(v.y, b);
-          v.z = bf16x2_to_f16x2(v.z, b);
-          v.w = bf16x2_to_f16x2(v.w, b);
-          q4[i] = v;
-          big |= b && ((i % (kChunkBytes / 16)) / 8 < rows_q);   // [chunk][64 rows][8 x 16 B]
-        }
-        if (big) atomicOr(&p.hdr->err, kErrQRange);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_q_conv);
-        ++pc;
-      }
-      for (int j = t0; j < t1; ++j, ++gt) {
-        const int st = gt & 1;
-        ok = __all_sync(0xffffffffu,
-                        ok && mbar_wait(b_kv_full + 8 * st, (gt >> 1) & 1, tmo, abort_flag));
-        // every converter thread reaches the barrier, failure or not
-        const bool any_fail = named_bar_or(kBarConv, kConvThreads, !ok);
-        if (any_fail) { ok = false; break; }
-        uint8_t* stage = smem + kSmemKV + st * kTileBytes;
-        const uint8_t* src_lo = stage + kFp8Staging + row_lo * kDqk + 16 * qq;
-        const uint8_t* src_hi = src_lo + (kTile / 2) * kDqk;
-        // 16 codes of chunk c of `row` -> 16 fp16 = the row's 16-byte chunks
-        // 2qq and 2qq+1 of the 128-byte atom row
-        auto put = [&](int row, int c, uint4 a) {
-          uint8_t* dst = stage + (row >> 3) * kGroupBytes + c * 1024 + (row & 7) * 128;
-          const uint2 h0 = e4m3x4_to_f16x4(a.x), h1 = e4m3x4_to_f16x4(a.y);
-          const uint2 h2 = e4m3x4_to_f16x4(a.z), h3 = e4m3x4_to_f16x4(a.w);
-          *reinterpret_cast<uint4*>(dst + (((2 * qq) ^ (row & 7)) << 4)) =
-              make_uint4(h0.x, h0.y, h1.x, h1.y);
-          *reinterpret_cast<uint4*>(dst + (((2 * qq + 1) ^ (row & 7)) << 4)) =
-              make_uint4(h2.x, h2.y, h3.x, h3.y);
-        };
-        uint4 hi[kChunks];
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) hi[c] = *reinterpret_cast<const uint4*>(src_hi + 64 * c);
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          put(row_lo, c, *reinterpret_cast<const uint4*>(src_lo + 64 * c));
-        named_bar_sync(kBarConv, kConvThreads);   // every row's codes have been read
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) put(row_hi, c, hi[c]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_kv_conv + 8 * st);
-      }
-    }
-    if (!ok && ct == 0) set_error(p, misc, kErrTimeout);
   } else {
     // ------------------------------------------------------------ softmax
     // Thread (quadrant, lane) owns query row r = 16*quad + lane%16 and the
@@ -512,35 +381,15 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
-          float s[32], sc[32];
+          float s[32];
 #pragma unroll
           for (int a = 0; a < 32; ++a) s[a] = __uint_as_float(sr[a]) + __uint_as_float(sr2[a]);
-          if constexpr (kFp8) {
-            // the scales were copied with the codes; acquire them from the
-            // stage barrier (long complete: QK^T already consumed the stage)
-            int never = 0;
-            mbar_wait(b_kv_full + 8 * sb, (gt >> 1) & 1, tmo, &never);
-            const float4* scp = reinterpret_cast<const float4*>(&misc->scale[sb][32 * half]);
-#pragma unroll
-            for (int a4 = 0; a4 < 8; ++a4) {
-              const float4 v = scp[a4];
-              sc[4 * a4] = v.x;
-              sc[4 * a4 + 1] = v.y;
-              sc[4 * a4 + 2] = v.z;
-              sc[4 * a4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int a = 0; a < 32; ++a) s[a] *= sc[a];   // logits of the dequantised keys
-          }
           if (!full) {
 #pragma unroll
             for (int a = 0; a < 32; ++a) {
               int t = slot_token<kLocal>(pd, x, j, 32 * half + a);
               bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
-              if (!vis) {
-                s[a] = -CUDART_INF_F;
-                sc[a] = 0.0f;   // a masked slot's scale may be garbage (even NaN)
-              }
+              if (!vis) s[a] = -CUDART_INF_F;
             }
           }
           // tree reduction: independent partial maxima keep the chain short
@@ -569,12 +418,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           for (int a = 0; a < 16; ++a) {
             const float p0 = ex2_approx(fmaf(s[2 * a], pd.scale_log2, -m_use));
             const float p1 = ex2_approx(fmaf(s[2 * a + 1], pd.scale_log2, -m_use));
-            if constexpr (kFp8) {
-              // P.V multiplies the codes; the token scale rides on P
-              pk[a] = pack_f16x2(p0 * sc[2 * a], p1 * sc[2 * a + 1]);
-            } else {
-              pk[a] = pack_bf16x2(p0, p1);
-            }
+            pk[a] = pack_bf16x2(p0, p1);
             ls4[a & 3] += p0 + p1;
           }
           l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
@@ -729,41 +573,35 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-template <bool kFp8, bool kLocal>
+template <bool kLocal>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const PartialParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kFp8, kLocal>,
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kLocal>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kFp8 ? kThreadsFp8 : kThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kFp8, kLocal>, tm_q, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, p);
 }
 
 // The cache kind (local slice or whole requests) is a template parameter:
 // branching on it at run time cost about 2% on the bimodal batch.
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const PartialParams& p, int grid, cudaStream_t stream) {
-  return p.pd.local ? launch_partial<false, true>(tm_q, tm_kv, p, grid, stream)
-                    : launch_partial<false, false>(tm_q, tm_kv, p, grid, stream);
-}
-
-cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                               const PartialParams& p, int grid, cudaStream_t stream) {
-  return p.pd.local ? launch_partial<true, true>(tm_q, tm_kv, p, grid, stream)
-                    : launch_partial<true, false>(tm_q, tm_kv, p, grid, stream);
+  return p.pd.local ? launch_partial<true>(tm_q, tm_kv, p, grid, stream)
+                    : launch_partial<false>(tm_q, tm_kv, p, grid, stream);
 }
 
 }  // namespace mla

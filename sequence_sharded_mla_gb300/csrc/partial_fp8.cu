@@ -24,7 +24,10 @@
 // The tensor cores accumulate in fp32.
 //
 // Shared memory (1024-byte aligned base):
-//   Q_hi, Q_lo   2 x 36 KB  [chunk c][8-row group][8 rows][64 codes], 64-byte swizzle
+//   Q            72 KB      per 8-row group rg, 9216 bytes: Q_hi then Q_lo, each
+//                           [chunk c][8 rows][64 codes] with 64-byte swizzle; the
+//                           piece's bf16 rows land here by TMA first, in the same
+//                           9216 bytes per row group, and are split in place
 //   stages       4 x 36 KB  group-major: slot a's 64-code chunk c at
 //                           (a/8)*4608 + c*512 + (a%8)*64 (swizzled), one TMA box per page
 //   P_lo         4 KB       [8-row group][8 rows][64 tokens]; P_hi goes into the
@@ -34,8 +37,8 @@
 // Warps: 0 producer (block table, TMA of the codes, cp.async of the scales);
 // 1 and 6 MMA issuers (even / odd chunks of QK^T into two accumulators, two of
 // the four 128-dim blocks of P.V each); 2..5 softmax and epilogue (two threads
-// per query row); 7..10 split each piece's query into Q_hi/Q_lo from global
-// memory, and warp 7 also splits every tile's token scales.
+// per query row); 7..10 load each piece's query by TMA and split it into
+// Q_hi/Q_lo in place, and warp 7 also splits every tile's token scales.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -52,17 +55,16 @@ constexpr int kStageBytes = kTile * kDqk;        // 36864: codes of one 64-token
 constexpr int kAtom = 512;                       // 8 rows x 64 bytes
 constexpr int kGroupBytes = kChunks * kAtom;     // 4608: one 8-slot group, nine chunks
 constexpr int kRopeAtom = 8 * kAtom;             // rope chunk of a group (P_hi after QK^T)
-constexpr int kQTermBytes = kChunks * 8 * kAtom; // 36864: one term of a 64-row query group
-constexpr int kQChunkBytes = 8 * kAtom;          // 4096: 64 rows of one chunk
+constexpr int kQGroupBytes = 2 * kChunks * kAtom;  // 9216: Q_hi + Q_lo of 8 rows (= their bf16)
+constexpr int kQBytes = 8 * kQGroupBytes;          // 73728
 constexpr int kSmemQ = 0;
-constexpr int kSmemKV = 2 * kQTermBytes;                         // 73728
+constexpr int kSmemKV = kQBytes;                                 // 73728
 constexpr int kSmemPlo = kSmemKV + kStages * kStageBytes;        // 221184
 constexpr int kSmemMisc = kSmemPlo + 8 * kAtom;                  // 225280
 constexpr int kMiscBytes = 6144;
 constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;        // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr int kIssuers = 2;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kConvThreads = 128;
@@ -73,11 +75,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: e_t <= 2^8 keeps P' in
 struct Misc {
   uint64_t kv_full[kStages], kv_empty[kStages], prep[kStages];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
-  uint64_t q_conv, q_empty, o_free;
+  uint64_t q_full, q_conv, q_empty, o_free;
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];
   alignas(16) float inv_l[kRows];
+  float qsc[kRows];     // splitters: the row's power-of-two scale (0: padding row)
   // per stage and token slot: the scale (cp.async target, then sanitised in
   // place), E + 1 as a float, 2^-(E+1), and sigma * 2^-(E+1)
   alignas(16) float sigma[kStages][kTile];
@@ -97,17 +100,11 @@ __device__ __forceinline__ void set_error(PartialParams& p, Misc* misc, unsigned
   if (bits & kErrTimeout) *(volatile int*)&misc->abort = 1;
 }
 
-// Byte offset of (row, 16-byte unit u) in a run of 64-byte-swizzled atoms
-// whose 8-row groups are `group_stride` apart.
-__device__ __forceinline__ uint32_t sw64_off(int row, int u, int group_stride) {
-  return (uint32_t)((row >> 3) * group_stride + (row & 7) * 64 + ((u ^ ((row & 7) >> 1)) << 4));
-}
-
 // Largest |q| of a row half as a bf16 magnitude pattern (monotonic in |q|;
 // NaN sorts above inf), over 288 values from 36 16-byte loads.
 __device__ __forceinline__ uint32_t half_row_max(const uint4* src) {
   uint32_t m = 0;
-#pragma unroll 6
+#pragma unroll 12
   for (int i = 0; i < 36; ++i) {
     const uint4 v = __ldg(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -128,7 +125,8 @@ __device__ __forceinline__ uint32_t row_scale_exp(uint32_t max_bits) {
 
 template <bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
+    mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Misc* misc = reinterpret_cast<Misc*>(smem + kSmemMisc);
@@ -154,23 +152,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_p_full = smem_u32(&misc->p_full[0]);
   const uint32_t b_pv_done = smem_u32(&misc->pv_done[0]);
   const uint32_t b_q_conv = smem_u32(&misc->q_conv), b_q_empty = smem_u32(&misc->q_empty);
+  const uint32_t b_q_full = smem_u32(&misc->q_full);
   const uint32_t b_o_free = smem_u32(&misc->o_free);
   volatile int* abort_flag = &misc->abort;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(b_kv_full + 8 * st, 1 + 32);   // expect_tx arrival + one cp.async arrival per lane
-      mbar_init(b_kv_empty + 8 * st, kIssuers);
+      mbar_init(b_kv_empty + 8 * st, 1);
       mbar_init(b_prep + 8 * st, 1);
     }
     for (int sb = 0; sb < 2; ++sb) {
-      mbar_init(b_s_full + 8 * sb, kIssuers);
+      mbar_init(b_s_full + 8 * sb, 1);
       mbar_init(b_s_empty + 8 * sb, kSoftmaxWarps);
       mbar_init(b_p_full + 8 * sb, kSoftmaxWarps);
-      mbar_init(b_pv_done + 8 * sb, kIssuers);
+      mbar_init(b_pv_done + 8 * sb, 1);
     }
+    mbar_init(b_q_full, 1);
     mbar_init(b_q_conv, kConvThreads / 32);
-    mbar_init(b_q_empty, kIssuers);
+    mbar_init(b_q_empty, 1);
     mbar_init(b_o_free, kSoftmaxWarps);
     misc->abort = 0;
     fence_mbar_init();
@@ -180,7 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&misc->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   PieceIter it;
   it.init(p.prefix, U, lo, hi, p.hdr->unit_cost);
-  int armed_kv[kStages] = {-1, -1, -1, -1};
+  int armed_kv[kStages] = {-1, -1, -1, -1}, armed_q = -1;
   int unit, t0, t1, slot;
   bool whole;
 
@@ -256,16 +259,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (warp == 1 || warp == 6) {
-    // ------------------------------------------------------------ MMA issue
-    const int mi = warp == 6 ? 1 : 0;
-    const uint32_t id_qk = idesc_e4m3_f32(64, 64, false, false);
-    // Q (A of QK^T, K-major): 8-row groups 512 bytes apart, chunks 4096;
-    // K (B of QK^T, K-major) and V^T (A of P.V, MN-major: 64-dim blocks 512
-    // apart): 8-slot groups 4608 apart; P_hi in the groups' rope atoms and
-    // P_lo in its own buffer (B of P.V, K-major)
-    const uint64_t dq0 = sw64_desc(sQ, 16, kAtom);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ QK^T issue
+    // One QK^T unit per pair of tiles (g even, both in the piece: the two
+    // stages are adjacent, so the pair's 16 slot groups are 4608 bytes apart
+    // and one N=128 MMA chain covers them), else per single tile (N=64).
+    // Unit u accumulates into S buffer u & 1 (128 columns); tile g's logits
+    // are its columns 64 (g & 1) ..
+    const uint32_t id_qk1 = idesc_e4m3_f32(64, 64, false, false);
+    const uint32_t id_qk2 = idesc_e4m3_f32(64, 128, false, false);
+    // Q (A, K-major): 8-row groups 9216 bytes apart, chunks 512 (Q_lo 4608
+    // further); K (B, K-major): 8-slot groups 4608 apart
+    const uint64_t dq0 = sw64_desc(sQ, 16, kQGroupBytes);
     const uint64_t dk0 = sw64_desc(sKV, 16, kGroupBytes);
+    int gbase = 0, pc = 0, qu = 0;
+    bool ok = true;
+    while (ok && it.next(unit, t0, t1, whole, slot)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_conv, pc & 1, tmo, abort_flag));
+      for (int j = t0; ok && j < t1;) {
+        const int g = gbase + (j - t0);
+        const bool pair = (g & 1) == 0 && j + 1 < t1;
+        const int st = g & (kStages - 1), sb = qu & 1;
+        bool w = mbar_wait(b_kv_full + 8 * st, (g >> 2) & 1, tmo, abort_flag);
+        if (pair) w = w && mbar_wait(b_kv_full + 8 * (st + 1), ((g + 1) >> 2) & 1, tmo, abort_flag);
+        if (qu >= 2) w = w && mbar_wait(b_s_empty + 8 * sb, ((qu >> 1) - 1) & 1, tmo, abort_flag);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
+          const uint32_t d = tmem + kColS0 + 128 * sb + (pair ? 0 : 64 * (g & 1));
+          const uint32_t id = pair ? id_qk2 : id_qk1;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint64_t aq = dq0 + (uint32_t)((c * kAtom + 32 * k) >> 4);
+              const uint64_t bk = dk0 + st_off + (uint32_t)((c * kAtom + 32 * k) >> 4);
+              mma_e4m3_ss(d, aq, bk, id, (c != 0 || k != 0) ? 1u : 0u);
+              mma_e4m3_ss(d, aq + (uint32_t)((kChunks * kAtom) >> 4), bk, id, 1u);
+            }
+          }
+          mma_commit(b_s_full + 8 * sb);
+          if (j + (pair ? 2 : 1) >= t1) mma_commit(b_q_empty);
+        }
+        __syncwarp();
+        ++qu;
+        j += pair ? 2 : 1;
+      }
+      gbase += t1 - t0;
+      ++pc;
+    }
+    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ P.V issue
+    // O^T (4 blocks of 128 dims) += V^T P'^T per tile: V^T (A, MN-major)
+    // 64-dim blocks 512 bytes apart, 8-token groups 4608; P_hi in the
+    // groups' rope atoms, P_lo in its buffer (B, K-major)
     const uint64_t dv0 = sw64_desc(sKV, kAtom, kGroupBytes);
     const uint64_t dph0 = sw64_desc(sKV + kRopeAtom, 16, kGroupBytes);
     const uint64_t dpl = sw64_desc(sPlo, 16, kAtom);
@@ -273,90 +323,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
-      const int n = t1 - t0;
       const uint32_t id_pv = idesc_e4m3_f32(128, x.rows, true, false);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_q_conv, pc & 1, tmo, abort_flag));
-      int nq = 0, np = 0;
-      uint64_t t_idle = 0;
-      uint32_t idle_iter = 0;
-      while (ok && np < n) {
-        bool did = false;
-        if (np < nq) {
-          const int g = gbase + np;
-          bool ready = mbar_test(b_p_full + 8 * (g & 1), (g >> 1) & 1);
-          if (ready && np == 0 && pc >= 1) ready = mbar_test(b_o_free, (pc - 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            if (lane == 0) {
-              const int st = g & (kStages - 1);
-              const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
+      for (int j = t0; ok && j < t1; ++j) {
+        const int g = gbase + (j - t0);
+        bool w = mbar_wait(b_p_full + 8 * (g & 1), (g >> 1) & 1, tmo, abort_flag);
+        // the first P.V of a piece overwrites O^T: the previous epilogue must have read it
+        if (j == t0 && pc >= 1) w = w && mbar_wait(b_o_free, (pc - 1) & 1, tmo, abort_flag);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const int st = g & (kStages - 1);
+          const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
 #pragma unroll
-              for (int blk = 2 * mi; blk < 2 * mi + 2; ++blk) {
+          for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                  const uint64_t a =
-                      dv0 + st_off + (uint32_t)((2 * blk * kAtom + kk * 4 * kGroupBytes) >> 4);
-                  const uint32_t d = tmem + kColO + 64 * blk;
-                  mma_e4m3_ss(d, a, dph0 + st_off + (uint32_t)((32 * kk) >> 4), id_pv,
-                              (np == 0 && kk == 0) ? 0u : 1u);
-                  mma_e4m3_ss(d, a, dpl + (uint32_t)((32 * kk) >> 4), id_pv, 1u);
-                }
-              }
-              mma_commit(b_kv_empty + 8 * st);
-              mma_commit(b_pv_done + 8 * (g & 1));
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint64_t a =
+                  dv0 + st_off + (uint32_t)((2 * blk * kAtom + kk * 4 * kGroupBytes) >> 4);
+              const uint32_t d = tmem + kColO + 64 * blk;
+              mma_e4m3_ss(d, a, dph0 + st_off + (uint32_t)((32 * kk) >> 4), id_pv,
+                          (j == t0 && kk == 0) ? 0u : 1u);
+              mma_e4m3_ss(d, a, dpl + (uint32_t)((32 * kk) >> 4), id_pv, 1u);
             }
-            __syncwarp();
-            ++np;
-            did = true;
           }
+          mma_commit(b_kv_empty + 8 * st);
+          mma_commit(b_pv_done + 8 * (g & 1));
         }
-        if (!did && nq < n) {
-          const int g = gbase + nq;
-          const int st = g & (kStages - 1), sb = g & 1;
-          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 2) & 1);
-          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * sb, ((g >> 1) - 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            if (lane == 0) {
-              const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
-              const uint32_t d = tmem + kColS0 + 128 * sb + 64 * mi;
-#pragma unroll
-              for (int c = mi; c < kChunks; c += kIssuers) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                  const uint64_t aq = dq0 + (uint32_t)((c * kQChunkBytes + 32 * k) >> 4);
-                  const uint64_t bk = dk0 + st_off + (uint32_t)((c * kAtom + 32 * k) >> 4);
-                  mma_e4m3_ss(d, aq, bk, id_qk, (c != mi || k != 0) ? 1u : 0u);
-                  mma_e4m3_ss(d, aq + (uint32_t)(kQTermBytes >> 4), bk, id_qk, 1u);
-                }
-              }
-              mma_commit(b_s_full + 8 * sb);
-              if (nq == n - 1) mma_commit(b_q_empty);
-            }
-            __syncwarp();
-            ++nq;
-            did = true;
-          }
-        }
-        if (did) {
-          t_idle = 0;
-          idle_iter = 0;
-        } else if ((++idle_iter & 63u) == 0) {
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (now - t_idle > tmo || *abort_flag) ok = false;
-          ok = __all_sync(0xffffffffu, ok);
-        }
+        __syncwarp();
       }
-      gbase += n;
+      gbase += t1 - t0;
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
   } else if (warp >= 7) {
     // ------------------------------------------------------------ splitters
-    // Per piece, thread (r, hh) = (ct / 2, ct % 2) splits dims [288 hh,
-    // 288 hh + 288) of query row r into Q_hi / Q_lo; warp 7 then splits the
-    // token scales of each of the piece's tiles as they land.
+    // Per piece: thread ct = 0 loads the 64 bf16 query rows by TMA (8 rows x
+    // 9 chunks per row group, 128-byte swizzle); thread (r, hh) = (ct / 2,
+    // ct % 2) takes row r's largest |q| over half of its 16-byte units; then,
+    // two row groups at a time, every thread reads 9 units into registers and,
+    // after a barrier, writes their Q_hi / Q_lo codes over the same row groups.
     const int ct = threadIdx.x - 7 * 32;
     const int r = ct >> 1, hh = ct & 1;
     int gt = 0, pc = 0;
@@ -364,45 +370,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (it.next(unit, t0, t1, whole, slot)) {
       if (pc >= 1 && ok)
         ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
-      // every splitter reaches this barrier once per piece, failure or not
+      // every splitter reaches these barriers once per piece, failure or not
       if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
       Unit x = make_unit<kLocal>(pd, unit);
+      if (ct == 0) {
+        mbar_arrive_expect_tx(b_q_full, kQBytes);
+        armed_q = pc;
+        tma_load_4d(sQ, &tm_q, b_q_full, 0, 0, 0, (x.b * pd.R + x.g * kRows) >> 3);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
+      if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
+      uint8_t* q8 = smem + kSmemQ;
       {
-        const bool live = r < x.rows;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + ((size_t)x.b * pd.R + (size_t)x.g * kRows + r) * kDqk + 288 * hh);
-        uint32_t mx = live ? half_row_max(src) : 0u;
+        const int rg = r >> 3, rr = r & 7;
+        const uint8_t* row = q8 + rg * kQGroupBytes + rr * 128;
+        uint32_t mx = 0;
+#pragma unroll 12
+        for (int v = 0; v < 36; ++v) {
+          const int w = 36 * hh + v;   // 16-byte unit of the row: chunk w / 8, unit w % 8
+          const uint4 t = *reinterpret_cast<const uint4*>(row + (w >> 3) * 1024 + (w & 7) * 16);
+          const uint32_t ww[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx = max(mx, max(ww[k] & 0x7FFFu, (ww[k] >> 16) & 0x7FFFu));
+        }
         mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        const bool live = r < x.rows;
         if (live && (mx >> 7) == 255u) atomicOr(&p.hdr->err, kErrQRange);   // inf or NaN
-        const float s = __uint_as_float((261u - row_scale_exp(mx)) << 23);
-        uint8_t* qh = smem + kSmemQ;
-        uint8_t* ql = qh + kQTermBytes;
-#pragma unroll 4
-        for (int i = 0; i < 36; ++i) {
+        if (hh == 0) misc->qsc[r] = live ? __uint_as_float((261u - row_scale_exp(mx)) << 23) : 0.0f;
+      }
+      named_bar_sync(kBarConv, kConvThreads);
+#pragma unroll 1
+      for (int pr = 0; pr < 4; ++pr) {
+        uint4 in[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int i = ct + kConvThreads * k;   // 16-byte unit of row groups 2 pr, 2 pr + 1
+          in[k] = *reinterpret_cast<const uint4*>(q8 + 2 * pr * kQGroupBytes + i * 16);
+        }
+        named_bar_sync(kBarConv, kConvThreads);   // the pair's bf16 has been read
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int i = ct + kConvThreads * k;
+          const int rg = 2 * pr + i / 576, rem = i % 576;
+          const int c = rem >> 6, rr = (rem >> 3) & 7, u = (rem & 7) ^ rr;   // u: dims 8u.. of chunk c
+          const float sc = misc->qsc[rg * 8 + rr];
           uint32_t whi = 0, wlo = 0, whi2 = 0, wlo2 = 0;
-          if (live) {
-            const uint4 v = __ldg(src + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          if (sc != 0.0f) {
+            const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
             uint32_t sp[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              sp[k] = split_e4m3x2(__uint_as_float(w[k] << 16) * s,
-                                   __uint_as_float(w[k] & 0xFFFF0000u) * s);
+            for (int e = 0; e < 4; ++e)
+              sp[e] = split_e4m3x2(__uint_as_float(w[e] << 16) * sc,
+                                   __uint_as_float(w[e] & 0xFFFF0000u) * sc);
             whi = (sp[0] & 0xFFFFu) | (sp[1] << 16);
             wlo = (sp[0] >> 16) | (sp[1] & 0xFFFF0000u);
             whi2 = (sp[2] & 0xFFFFu) | (sp[3] << 16);
             wlo2 = (sp[2] >> 16) | (sp[3] & 0xFFFF0000u);
           }
-          const int d0 = 288 * hh + 8 * i;          // first of these 8 dims
-          const int c = d0 >> 6, within = d0 & 63;
-          const uint32_t off = c * kQChunkBytes + sw64_off(r, within >> 4, kAtom) + (within & 15);
-          *reinterpret_cast<uint2*>(qh + off) = make_uint2(whi, whi2);
-          *reinterpret_cast<uint2*>(ql + off) = make_uint2(wlo, wlo2);
+          uint8_t* dst = q8 + rg * kQGroupBytes + c * kAtom + rr * 64 +
+                         (((u >> 1) ^ (rr >> 1)) << 4) + (u & 1) * 8;
+          *reinterpret_cast<uint2*>(dst) = make_uint2(whi, whi2);
+          *reinterpret_cast<uint2*>(dst + kChunks * kAtom) = make_uint2(wlo, wlo2);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_q_conv);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_q_conv);
       if (warp == 7) {
         for (int j = t0; j < t1; ++j, ++gt) {
           const int st = gt & (kStages - 1);
@@ -454,11 +487,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 16 * quad + (lane & 15);
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     uint8_t* plo_row = smem + kSmemPlo + (r >> 3) * kAtom + (r & 7) * 64;   // P_lo row r
-    int gt = 0, pc = 0;
+    int gt = 0, pc = 0, qu = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
       const bool owner = r < x.rows;
+      int unit_left = 0;   // tiles of the current QK^T unit still to read
       const int i_row = (x.g * kRows + r) / pd.H;
       const int vis_limit = x.L - x.qn + i_row;
       // the row's query scale, computed exactly as the splitters do
@@ -472,9 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_run = -CUDART_INF_F, l_run = 0.0f;
       for (int j = t0; j < t1; ++j, ++gt) {
-        const int sb = gt & 1, st = gt & (kStages - 1);
-        bool ok_s = __all_sync(
-            0xffffffffu, ok && mbar_wait(b_s_full + 8 * sb, (gt >> 1) & 1, tmo, abort_flag));
+        const int sb = qu & 1, st = gt & (kStages - 1);
+        bool ok_s = ok;
+        if (unit_left == 0) {
+          // a new QK^T unit: a pair (gt even, next tile in the piece) or one tile
+          unit_left = ((gt & 1) == 0 && j + 1 < t1) ? 2 : 1;
+          ok_s = __all_sync(0xffffffffu,
+                            ok_s && mbar_wait(b_s_full + 8 * sb, (qu >> 1) & 1, tmo, abort_flag));
+        }
         ok_s = __all_sync(0xffffffffu,
                           ok_s && mbar_wait(b_prep + 8 * st, (gt >> 2) & 1, tmo, abort_flag));
         bool resc = false;
@@ -482,13 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = tile_full<kLocal>(pd, x, j);
         if (ok_s) {
           tc_fence_after();
-          uint32_t sr[32], sr2[32];
-          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb, sr);
-          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb + 64, sr2);
+          uint32_t sr[32];
+          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb + 64 * (gt & 1), sr);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
+          if (--unit_left == 0) {
+            if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
+            ++qu;
+          }
           // b_t = S_t sigma_t / s_r * scale * log2(e) + E_t + 1
           float b[32];
           {
@@ -497,10 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int a4 = 0; a4 < 8; ++a4) {
               const float4 sg = sg4[a4], lg = lg4[a4];
-              const float s0 = __uint_as_float(sr[4 * a4]) + __uint_as_float(sr2[4 * a4]);
-              const float s1 = __uint_as_float(sr[4 * a4 + 1]) + __uint_as_float(sr2[4 * a4 + 1]);
-              const float s2 = __uint_as_float(sr[4 * a4 + 2]) + __uint_as_float(sr2[4 * a4 + 2]);
-              const float s3 = __uint_as_float(sr[4 * a4 + 3]) + __uint_as_float(sr2[4 * a4 + 3]);
+              const float s0 = __uint_as_float(sr[4 * a4]);
+              const float s1 = __uint_as_float(sr[4 * a4 + 1]);
+              const float s2 = __uint_as_float(sr[4 * a4 + 2]);
+              const float s3 = __uint_as_float(sr[4 * a4 + 3]);
               b[4 * a4] = fmaf(s0 * sg.x, qs, lg.x);
               b[4 * a4 + 1] = fmaf(s1 * sg.y, qs, lg.y);
               b[4 * a4 + 2] = fmaf(s2 * sg.z, qs, lg.z);
@@ -703,6 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if (warp == 7 && lane == 0 && *abort_flag && armed_q >= 0) {
+    int never = 0;
+    mbar_wait(b_q_full, armed_q & 1, tmo, &never);
+  }
   if (warp == 0 && lane == 0 && *abort_flag) {
     // after a failure, let this CTA's own copies land before it exits
     int never = 0;
@@ -719,8 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kLocal>
-static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_kv, const PartialParams& p,
-                                           int grid, cudaStream_t stream) {
+static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                                           const PartialParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -738,13 +783,13 @@ static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_kv, const Parti
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_fp8_kernel<kLocal>, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_fp8_kernel<kLocal>, tm_q, tm_kv, p);
 }
 
-cudaError_t launch_partial_fp8(const CUtensorMap& tm_kv, const PartialParams& p, int grid,
-                               cudaStream_t stream) {
-  return p.pd.local ? launch_partial_fp8_impl<true>(tm_kv, p, grid, stream)
-                    : launch_partial_fp8_impl<false>(tm_kv, p, grid, stream);
+cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                               const PartialParams& p, int grid, cudaStream_t stream) {
+  return p.pd.local ? launch_partial_fp8_impl<true>(tm_q, tm_kv, p, grid, stream)
+                    : launch_partial_fp8_impl<false>(tm_q, tm_kv, p, grid, stream);
 }
 
 }  // namespace mla

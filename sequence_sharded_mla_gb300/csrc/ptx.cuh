@@ -92,17 +92,16 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 
 // Wait for the phase with the given parity to complete.  Returns false if
 // `limit_ns` elapsed first or if *abort became non-zero (another role gave up).
+// The waiting thread sleeps in the barrier (up to 0.2 ms per probe) instead
+// of spinning, so it does not take issue slots from the warps doing work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    if (mbar_try_wait_hint(bar, parity, 200000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -152,6 +151,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y, int z, int w, int v) {
   asm volatile(
@@ -178,57 +186,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Four OCP e4m3 codes -> four bf16 values (exact), as two bf16x2 words.
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t codes) {
-  uint32_t h01, h23;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((unsigned short)(codes & 0xFFFFu)));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((unsigned short)(codes >> 16)));
-  float f0, f1, f2, f3;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h01 & 0xFFFFu)));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h01 >> 16)));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f2) : "h"((unsigned short)(h23 & 0xFFFFu)));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f3) : "h"((unsigned short)(h23 >> 16)));
-  uint32_t b01, b23;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b01) : "f"(f1), "f"(f0));
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b23) : "f"(f3), "f"(f2));
-  return make_uint2(b01, b23);
-}
-
-// Four OCP e4m3 codes -> four fp16 values (exact: every e4m3 value, NaN
-// included, is an fp16 value), as two f16x2 words; byte k of `codes` becomes
-// half k.
-__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t codes) {
-  uint32_t h01, h23;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(h01), "=r"(h23)
-      : "r"(codes));
-  return make_uint2(h01, h23);
-}
-
-// Two bf16 (one word) -> two fp16, round to nearest even.  Exact for
-// magnitudes in [2^-17, 65504]; `overflow` is set when a finite value
-// rounds to infinity.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& overflow) {
-  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
-  overflow |= (fabsf(lo) >= 65520.0f && fabsf(lo) != __int_as_float(0x7f800000)) ||
-              (fabsf(hi) >= 65520.0f && fabsf(hi) != __int_as_float(0x7f800000));
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -377,13 +334,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
-}
-
-// The same with fp16 A and B (format code 0).
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
-                                                     bool b_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0)
