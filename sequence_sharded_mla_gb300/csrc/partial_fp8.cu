@@ -530,6 +530,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
             ++qu;
           }
+          // this tile's value factors, loaded early so their latency hides
+          // behind the logits and the max
+          float4 mtv[8], ilv[8];
+          {
+            const float4* mt4 = reinterpret_cast<const float4*>(&misc->mant[st][32 * half]);
+            const float4* il4 = reinterpret_cast<const float4*>(&misc->il[st][32 * half]);
+#pragma unroll
+            for (int a4 = 0; a4 < 8; ++a4) {
+              mtv[a4] = mt4[a4];
+              ilv[a4] = il4[a4];
+            }
+          }
           // b_t = S_t sigma_t / s_r * scale * log2(e) + E_t + 1
           float b[32];
           {
@@ -581,19 +593,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (owner && half == 0) misc->alpha[gt & 1][r] = alpha;
           const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
           // e_t = 2^(b_t - m); P'_t = e_t mant_t; l += e_t 2^-(E_t+1)
-          const float4* mt4 = reinterpret_cast<const float4*>(&misc->mant[st][32 * half]);
-          const float4* il4 = reinterpret_cast<const float4*>(&misc->il[st][32 * half]);
           float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
           for (int a4 = 0; a4 < 8; ++a4) {
-            float4 mt = mt4[a4], iv = il4[a4];
-            if (vis_mask != 0xFFFFFFFFu) {
-              // a masked slot's scale may be garbage (even NaN)
-              if (!(vis_mask >> (4 * a4) & 1u)) mt.x = iv.x = 0.0f;
-              if (!(vis_mask >> (4 * a4 + 1) & 1u)) mt.y = iv.y = 0.0f;
-              if (!(vis_mask >> (4 * a4 + 2) & 1u)) mt.z = iv.z = 0.0f;
-              if (!(vis_mask >> (4 * a4 + 3) & 1u)) mt.w = iv.w = 0.0f;
-            }
+            float4 mt = mtv[a4], iv = ilv[a4];
+            // a masked slot's scale may be garbage (even NaN): select, no branch
+            const uint32_t vm = vis_mask >> (4 * a4);
+            mt.x = (vm & 1u) ? mt.x : 0.0f;
+            iv.x = (vm & 1u) ? iv.x : 0.0f;
+            mt.y = (vm & 2u) ? mt.y : 0.0f;
+            iv.y = (vm & 2u) ? iv.y : 0.0f;
+            mt.z = (vm & 4u) ? mt.z : 0.0f;
+            iv.z = (vm & 4u) ? iv.z : 0.0f;
+            mt.w = (vm & 8u) ? mt.w : 0.0f;
+            iv.w = (vm & 8u) ? iv.w : 0.0f;
             const float e0 = ex2_approx(b[4 * a4] - m_use);
             const float e1 = ex2_approx(b[4 * a4 + 1] - m_use);
             const float e2 = ex2_approx(b[4 * a4 + 2] - m_use);
