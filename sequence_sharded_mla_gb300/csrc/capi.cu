@@ -208,7 +208,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
       return MLA_ERR_CUDA;
     // e4m3 codes: the same view with 64-code chunks, strides (-, 576 nv, 64,
     // 4608 nv, 576) and 64-byte swizzling: a box lands a page's residue rows,
-    // all nine chunks, in the group-major layout of the fp8 kernel
+    // all nine chunks, in the group-major layout of the fp8 kernel.  No L2
+    // promotion: a 576-byte row is 18 whole sectors, and promotion to 128
+    // bytes would fetch 640
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
                           (cuuint64_t)kv->num_pages * kPage};
     cuuint64_t strides[4] = {(cuuint64_t)kDqk * nv, 64, (cuuint64_t)kDqk * 8 * nv,
@@ -217,7 +219,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   } else {
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
