@@ -55,7 +55,7 @@ typedef enum mla_status {
   MLA_ERR_TIMEOUT = -4,       /* a device-side wait gave up (from mla_get_device_error) */
   MLA_ERR_DEVICE_BOUNDS = -5, /* a block-table entry was outside [0, num_pages) */
   MLA_ERR_WORKSPACE = -6,     /* workspace missing or smaller than mla_workspace_size() */
-  MLA_ERR_RANGE = -7          /* fp8 cache: a query value beyond the fp16 range (|q| >= 65520) */
+  MLA_ERR_RANGE = -7          /* fp8 cache: an inf or NaN query value in a row that attends */
 } mla_status;
 
 /* Which token positions of a request belong to shard s of N
@@ -85,9 +85,11 @@ typedef enum mla_layout {
 typedef enum mla_kv_dtype { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 
 /* Decode-step shape.  num_heads must be a multiple of 16.  With an fp8
- * cache the query is rounded to fp16 for the tensor cores: exact for
- * magnitudes in [2^-17, 65504]; a finite |q| >= 65520 is reported as
- * MLA_ERR_RANGE by mla_get_device_error.  With causal != 0
+ * cache the tensor cores take each query row as a two-term e4m3 sum under a
+ * power-of-two row scale (exact for components within 2^10 of the row's
+ * largest; any finite bf16 value is accepted); an inf or NaN component of a
+ * row that attends is reported as MLA_ERR_RANGE by mla_get_device_error.
+ * With causal != 0
  * (a speculative verify step of q_len = 1 + drafts tokens whose KV is the
  * last q_len entries of the cache), query i sees tokens t <= L - q_len + i. */
 typedef struct mla_shape {

@@ -35,10 +35,10 @@
 //   misc         barriers, token scales and their exponent split, softmax exchange
 //
 // Warps: 0 producer (block table, TMA of the codes, cp.async of the scales);
-// 1 and 6 MMA issuers (even / odd chunks of QK^T into two accumulators, two of
-// the four 128-dim blocks of P.V each); 2..5 softmax and epilogue (two threads
-// per query row); 7..10 load each piece's query by TMA and split it into
-// Q_hi/Q_lo in place, and warp 7 also splits every tile's token scales.
+// 1 issues QK^T (per pair of adjacent stages as one N=128 chain, else per
+// tile); 6 issues P.V; 2..5 softmax and epilogue (two threads per query row);
+// 7..10 load each piece's query by TMA and split it into Q_hi/Q_lo in place,
+// and warp 7 also splits every tile's token scales.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -90,8 +90,9 @@ struct Misc {
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 
-// TMEM: per S buffer two partial accumulators (M=64, 64 columns each), then
-// the four 128-dim blocks of O^T (M=128, 64 columns each).
+// TMEM: two S buffers of 128 columns (M=64: a QK^T unit of one or two tiles,
+// tile g at columns 64 (g & 1)), then the four 128-dim blocks of O^T (M=128,
+// 64 columns each).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256;
 
