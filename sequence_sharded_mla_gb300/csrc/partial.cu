@@ -8,7 +8,7 @@
 // each rank attends over its local latent slice; partial outputs and LSEs are
 // merged afterwards).
 //
-// Data flow per persistent CTA (one per SM, 192 threads):
+// Data flow per persistent CTA (one per SM, 224 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
 //               (one TMA box per page, 128-byte swizzle) into two stages; a
