@@ -73,6 +73,18 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   auto slot_of = [&](int c) -> size_t {
     return (c == c0 && c0 * per < ps) ? 2 * (size_t)c + 1 : 2 * (size_t)c;
   };
+  // the first two pieces' rows are loaded before the weights are known, so
+  // their latency overlaps the LSE reduction (most split units have two)
+  float4 o0[4], o1[4];
+  {
+    const float4* s0 = reinterpret_cast<const float4*>(ws_o + (slot_of(c0) * kRows + r) * kDv);
+    const float4* s1 = reinterpret_cast<const float4*>(ws_o + (slot_of(c0 + 1) * kRows + r) * kDv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o0[i] = s0[lane + 32 * i];
+      o1[i] = s1[lane + 32 * i];
+    }
+  }
   float M = -CUDART_INF_F;
   for (int k = lane; k < np; k += 32) M = fmaxf(M, ws_lse[slot_of(c0 + k) * kRows + r]);
 #pragma unroll
@@ -87,9 +99,17 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
   __syncwarp();
   float4 acc[4];
+  {
+    const float w0 = wts[warp][0], w1 = wts[warp][1];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < np; ++k) {
+    for (int i = 0; i < 4; ++i) {
+      acc[i].x = w0 * o0[i].x + w1 * o1[i].x;
+      acc[i].y = w0 * o0[i].y + w1 * o1[i].y;
+      acc[i].z = w0 * o0[i].z + w1 * o1[i].z;
+      acc[i].w = w0 * o0[i].w + w1 * o1[i].w;
+    }
+  }
+  for (int k = 2; k < np; ++k) {
     const float w = wts[warp][k];
     const float4* src = reinterpret_cast<const float4*>(ws_o + (slot_of(c0 + k) * kRows + r) * kDv);
 #pragma unroll
