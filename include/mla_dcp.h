@@ -12,7 +12,9 @@
  *
  * Conventions for every entry point:
  *   - Pointers named "device" must be device memory of the current CUDA
- *     device, 16-byte aligned.  The caller owns every buffer; the library
+ *     device, 16-byte aligned (4-byte for the int32 arrays block_table,
+ *     seq_lens and q_lens, so that views of a larger batch can be passed).
+ *     The caller owns every buffer; the library
  *     keeps no pointer after a call returns and allocates no device memory
  *     at run time (its one static buffer, the scratch of
  *     mla_decode_partial_noalloc, exists from library load to process exit).

@@ -43,6 +43,7 @@ constexpr int kMinTilesPerCta = 4;
 constexpr int kUnitCost = 2;
 
 using host::aligned16;
+using host::aligned4;
 using host::device_sm_count;
 using host::encode_fn;
 using host::EncodeTiledFn;
@@ -128,7 +129,8 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (shape->num_heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
   if (layout == MLA_LAYOUT_INTERLEAVED && kPage % num_shards != 0) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv->data) || !aligned16(out_partial) ||
-      !aligned16(lse_partial) || !aligned16(block_table) || !aligned16(seq_lens))
+      !aligned16(lse_partial) || !aligned4(block_table) || !aligned4(seq_lens) ||
+      !aligned4(shape->q_lens))
     return MLA_ERR_INVALID;
   if (workspace == nullptr || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   // one persistent CTA per SM (at most 512: the merge keeps per-piece

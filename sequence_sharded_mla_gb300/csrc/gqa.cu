@@ -695,6 +695,7 @@ mla_status gqa_decode_partial(const void* q, const gqa_kv_pages* kv, const int32
                               mla_layout layout, float* out_partial, float* lse_partial,
                               void* workspace, size_t workspace_bytes, void* stream) {
   using host::aligned16;
+  using host::aligned4;
   if (!q || !kv || !block_table || !seq_lens || !out_partial || !lse_partial) return MLA_ERR_INVALID;
   if (!gqa::shape_ok(shape)) return MLA_ERR_INVALID;
   if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
@@ -705,7 +706,7 @@ mla_status gqa_decode_partial(const void* q, const gqa_kv_pages* kv, const int32
   if (kv->page_size != kPage || !gqa::shape_supported(shape)) return MLA_ERR_UNSUPPORTED;
   if (layout == MLA_LAYOUT_INTERLEAVED && kPage % num_shards != 0) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv->k) || !aligned16(kv->v) || !aligned16(out_partial) ||
-      !aligned16(lse_partial) || !aligned16(block_table) || !aligned16(seq_lens))
+      !aligned16(lse_partial) || !aligned4(block_table) || !aligned4(seq_lens))
     return MLA_ERR_INVALID;
   if (workspace == nullptr || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   const int grid = std::min(host::device_sm_count(), 512);

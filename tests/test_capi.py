@@ -93,6 +93,27 @@ def test_local_layouts_need_one_shard():
     assert st == -1
 
 
+def test_index_arrays_need_only_4_byte_alignment():
+    """block_table and seq_lens may be views into a larger batch (4-byte
+    aligned); the query still has to be 16-byte aligned.  Without a GPU a
+    call that passes the host checks stops at the first CUDA query."""
+    import sequence_sharded_mla_gb300 as mla
+    L = mla.lib()
+    sh = mla.mla_shape(1, 1, 16, 0, 0.07)
+    kv = mla.mla_kv_pages(ctypes.c_void_p(256), None, 0, 1, 64)
+    fake, off4 = ctypes.c_void_p(512), ctypes.c_void_p(516)
+    st = L.mla_decode_partial(fake, ctypes.byref(kv), off4, 1, off4, ctypes.byref(sh), -1, 2, 0,
+                              fake, fake, fake, 1 << 20, None)
+    assert st != -1
+    st = L.mla_decode_partial(off4, ctypes.byref(kv), fake, 1, fake, ctypes.byref(sh), -1, 2, 0,
+                              fake, fake, fake, 1 << 20, None)
+    assert st == -1
+    off2 = ctypes.c_void_p(514)
+    st = L.mla_decode_partial(fake, ctypes.byref(kv), off2, 1, fake, ctypes.byref(sh), -1, 2, 0,
+                              fake, fake, fake, 1 << 20, None)
+    assert st == -1
+
+
 def test_gqa_arguments_checked_on_host():
     """The GQA calls refuse bad arguments and unsupported shapes before any
     CUDA call: null pointers, zero sizes, head widths other than 128,

@@ -5,7 +5,9 @@ The CUDA compute calls are replaced on CPU by the oracle: rank r's partial is
 the oracle's shard-r attention and the combine is the oracle's LSE merge and
 W_UV projection.  What is under test is the exchange: the query each rank
 computes with, which head slices travel where, and that every rank ends with
-exactly its heads of unsharded attention.
+exactly its heads of unsharded attention -- also when the requests are cut
+into groups whose exchanges run asynchronously behind the next group's
+compute.
 """
 import os
 import socket
@@ -33,7 +35,7 @@ def _workload(layout, N, causal, wuv):
                              "bf16", causal, seed=500 + N, with_w_uv=wuv, poison=True)
 
 
-def _worker(rank, world, port, layout, causal, wuv, out):
+def _worker(rank, world, port, layout, causal, wuv, chunks, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -51,47 +53,58 @@ def _worker(rank, world, port, layout, causal, wuv, out):
         if wuv:
             w_uv_local = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16)[
                 rank * Hl:(rank + 1) * Hl].contiguous()
-        seen = {}
+
+        seen = {"q": []}
 
         def partial_fn(q_full, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
                        q_lens=None):
-            seen["q"] = q_full
+            # the request group [b0, b1) is a view into the full batch
+            b0 = sl_.storage_offset()
+            b1 = b0 + sl_.shape[0]
+            seen["q"].append(q_full)
             assert N == world and shard_id == rank and lay == layout and causal_ == causal
-            assert kv_ is kv and bt_ is bt and sl_ is sl
+            assert kv_ is kv and bt_.storage_offset() == b0 * bt.shape[1]
+            assert torch.equal(bt_, bt[b0:b1]) and torch.equal(sl_, sl[b0:b1])
             o, l = oracle.attend(w, shard=shard_id, num_shards=N, layout=lay)
-            return (torch.from_numpy(o.astype(np.float32)).reshape(B, q_len, H, 512),
-                    torch.from_numpy(l.astype(np.float32)).reshape(B, q_len, H))
+            o = o.reshape(B, q_len, H, 512)[b0:b1]
+            l = l.reshape(B, q_len, H)[b0:b1]
+            return (torch.from_numpy(np.ascontiguousarray(o, dtype=np.float32)),
+                    torch.from_numpy(np.ascontiguousarray(l, dtype=np.float32)))
 
         def combine_fn(partials, lses, w_uv, causal_, scale):
-            n = partials.shape[0]
+            n, bc = partials.shape[0], partials.shape[1]
             o, l = oracle.lse_merge(partials.double().numpy().reshape(n, -1, 512),
                                     lses.double().numpy().reshape(n, -1))
+            l = torch.from_numpy(np.asarray(l)).reshape(bc, q_len, Hl)
             if w_uv is not None:
-                heads = np.tile(np.arange(Hl, dtype=np.int32), B * q_len)
+                heads = np.tile(np.arange(Hl, dtype=np.int32), bc * q_len)
                 y = oracle.project_wuv(o, heads, w_uv.view(torch.int16).numpy().view(np.uint16))
-                return torch.from_numpy(y).reshape(B, q_len, Hl, 128), l
-            return torch.from_numpy(o).reshape(B, q_len, Hl, 512), l
+                return torch.from_numpy(y).reshape(bc, q_len, Hl, 128), l
+            return torch.from_numpy(o).reshape(bc, q_len, Hl, 512), l
 
         res, lse = dcp.dcp_decode_step(q_local, kv, bt, sl, layout=layout, causal=causal,
                                        w_uv_local=w_uv_local, partial_fn=partial_fn,
-                                       combine_fn=combine_fn)
-        out[rank] = (torch.equal(seen["q"], q), res.numpy(), np.asarray(lse))
+                                       combine_fn=combine_fn, chunks=chunks)
+        assert len(seen["q"]) == min(chunks, B)
+        out[rank] = (torch.equal(torch.cat(seen["q"], 0), q), res.numpy(), lse.numpy())
     finally:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,layout,causal,wuv", [
-    (2, "interleaved", False, False),
-    (2, "contiguous", True, True),
-    (4, "interleaved", True, False),
-    (4, "contiguous", False, True),
+@pytest.mark.parametrize("world,layout,causal,wuv,chunks", [
+    (2, "interleaved", False, False, 1),
+    (2, "contiguous", True, True, 1),
+    (4, "interleaved", True, False, 1),
+    (4, "contiguous", False, True, 1),
+    (2, "interleaved", True, True, 3),
+    (4, "contiguous", False, False, 2),
 ])
 def test_dcp_exchange_gives_each_rank_its_heads_of_unsharded_attention(world, layout, causal,
-                                                                         wuv):
+                                                                         wuv, chunks):
     with mp.get_context("spawn").Manager() as m:
         out = m.dict()
-        mp.spawn(_worker, args=(world, _free_port(), layout, causal, wuv, out), nprocs=world,
-                 join=True)
+        mp.spawn(_worker, args=(world, _free_port(), layout, causal, wuv, chunks, out),
+                 nprocs=world, join=True)
         res = dict(out)
     w = _workload(layout, world, causal, wuv)
     ref, ref_lse, ref_y = oracle.reference_step(w)

@@ -54,16 +54,20 @@ def test_rank_calls_of_a_dcp_step(N, layout, wuv):
                     f"rank {r} lse")
 
 
-def test_single_rank_step_without_a_process_group():
+@pytest.mark.parametrize("chunks", [1, 2, 3])
+def test_single_rank_step_without_a_process_group(chunks):
+    """chunks > 1: the requests are run in groups (the CUDA partial on a slice
+    of the block table and lengths), which must not change the result."""
     import torch
     from sequence_sharded_mla_gb300 import dcp
     dev = torch.device("cuda:0")
-    w = mi.build_workload("dcp-1", 2, 1, 32, [77, 3000], 1, "interleaved", "bf16", False, seed=650)
+    w = mi.build_workload("dcp-1", 3, 1, 32, [77, 3000, 640], 1, "interleaved", "bf16", False,
+                          seed=650)
     d = mi.local_shard_cache(w, 1, 0, "interleaved")
     q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(dev)
     kv = torch.from_numpy(d["kv"].view(np.int16)).view(torch.bfloat16).to(dev)
     out, lse = dcp.dcp_decode_step(q, kv, torch.from_numpy(d["block_table"]).to(dev),
-                                   torch.from_numpy(w.seq_lens).to(dev))
+                                   torch.from_numpy(w.seq_lens).to(dev), chunks=chunks)
     torch.cuda.synchronize()
     ref, ref_lse, _ = oracle.reference_step(w)
     check_close(bf16_to_np(out).reshape(-1, 512), ref, TOL_OUT, "out", rel=REL_OUT)
