@@ -25,6 +25,59 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 }  // namespace
 
+// Merges one row of the N shard partials by their LSEs into acc (unscaled)
+// and returns M = max lse and wsum = sum of exp(lse - M).  Each lane owns 16
+// of the 512 dims (four float4 at dims 4*lane + 128*k).  The rows of up to
+// four shards and all the LSEs are loaded together, before the weights are
+// known, so their latencies overlap; the sum runs over s = 0..N-1 in order.
+__device__ __forceinline__ void merge_row(const float* __restrict__ partials,
+                                          const float* __restrict__ lses, int num_shards,
+                                          int rows, int row, int lane, float4 (&acc)[4], float& M,
+                                          float& wsum) {
+  float4 ob[4][4];
+  auto load4 = [&](int s0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < num_shards) {
+        const float4* src =
+            reinterpret_cast<const float4*>(partials + ((size_t)(s0 + j) * rows + row) * kDv);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ob[j][k] = __ldg(src + lane + 32 * k);
+      }
+  };
+  load4(0);
+  float l[kMaxShards];
+  M = -CUDART_INF_F;
+#pragma unroll
+  for (int s = 0; s < kMaxShards; ++s) {
+    l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
+    M = fmaxf(M, l[s]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  wsum = 0.f;
+  if (M == -CUDART_INF_F) return;
+#pragma unroll
+  for (int s0 = 0; s0 < kMaxShards; s0 += 4) {
+    if (s0 >= num_shards) break;
+    if (s0 > 0) load4(s0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < num_shards) {
+        const float w = __expf(l[s0 + j] - M);
+        wsum += w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[k].x += w * ob[j][k].x;
+          acc[k].y += w * ob[j][k].y;
+          acc[k].z += w * ob[j][k].z;
+          acc[k].w += w * ob[j][k].w;
+        }
+      }
+    }
+  }
+}
+
 // One warp per query row; each lane owns 16 of the 512 latent dims
 // (four float4 at dims 4*lane + 128*k), so every load instruction of the warp
 // reads 512 contiguous bytes.
@@ -37,34 +90,9 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restric
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  float l[kMaxShards];
-  float M = -CUDART_INF_F;
-#pragma unroll
-  for (int s = 0; s < kMaxShards; ++s) {
-    l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
-    M = fmaxf(M, l[s]);
-  }
   float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (M > -CUDART_INF_F) {
-#pragma unroll
-    for (int s = 0; s < kMaxShards; ++s) {
-      if (s >= num_shards) break;
-      const float w = __expf(l[s] - M);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(partials + ((size_t)s * rows + row) * kDv);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 o = __ldg(src + lane + 32 * k);
-        acc[k].x += w * o.x;
-        acc[k].y += w * o.y;
-        acc[k].z += w * o.z;
-        acc[k].w += w * o.w;
-      }
-    }
-  }
+  float M, wsum;
+  merge_row(partials, lses, num_shards, rows, row, lane, acc, M, wsum);
   const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
   uint2* dst = reinterpret_cast<uint2*>(out + (size_t)row * kDv);
 #pragma unroll
@@ -115,35 +143,9 @@ __global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
     // merge: warp w handles row w of this pass
     if (warp < nr) {
       const int row = (base + warp) * H + h;
-      float M = -CUDART_INF_F;
-      float l[kMaxShards];
-#pragma unroll
-      for (int s = 0; s < kMaxShards; ++s) {
-        l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
-        M = fmaxf(M, l[s]);
-      }
       float4 acc[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      float wsum = 0.f;
-      if (M > -CUDART_INF_F) {
-#pragma unroll
-        for (int s = 0; s < kMaxShards; ++s) {
-          if (s >= num_shards) break;
-          const float w = __expf(l[s] - M);
-          wsum += w;
-          const float4* src =
-              reinterpret_cast<const float4*>(partials + ((size_t)s * rows + row) * kDv);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float4 o = __ldg(src + lane + 32 * k);
-            acc[k].x += w * o.x;
-            acc[k].y += w * o.y;
-            acc[k].z += w * o.z;
-            acc[k].w += w * o.w;
-          }
-        }
-      }
+      float M, wsum;
+      merge_row(partials, lses, num_shards, rows, row, lane, acc, M, wsum);
       const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
