@@ -353,8 +353,7 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
               "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
               "total_tokens_per_gpu": w.total_tokens}
     fp8 = w.kv_dtype == "fp8"
-    kernel = ("mla_partial_fp8_kernel<false>" if fp8 else
-              "mla_partial_kernel<false,%s>" % ("true" if q_len * H <= 64 else "false"))
+    kernel = "mla_partial_fp8_kernel<false>" if fp8 else "mla_partial_kernel<false>"
     rows = B * q_len * H
     flops = 2.0 * H * (576 + 512) * visible_pairs(w.seq_lens, q_len, w.causal)
     comb = N * rows * (512 * 4 + 4) + rows * ((128 if d_wuv is not None else 512) * 2 + 4)

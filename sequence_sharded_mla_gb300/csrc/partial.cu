@@ -8,7 +8,7 @@
 // each rank attends over its local latent slice; partial outputs and LSEs are
 // merged afterwards).
 //
-// Data flow per persistent CTA (one per SM, 224 threads, 256 with kSplitPV):
+// Data flow per persistent CTA (one per SM, 352 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
 //               (one TMA box per page, 128-byte swizzle) into two stages; a
@@ -21,19 +21,15 @@
 // page's slots of one interleaved shard are whole groups, so one TMA box
 // brings every chunk of a page's slots: N boxes per tile for N interleaved
 // shards instead of 9N with a chunk-major layout.
-//   warps 1, 6  MMA issuers (two, on different SM sub-partitions: one issuing
-//               thread cannot keep the tensor pipe full with MMAs this small).
-//               Each issues half of S = Q K^T (M=64 rows, N=64 tokens; even /
-//               odd 64-wide chunks of K=576 into two TMEM accumulators that
-//               the softmax adds) and two of the four latent blocks of
-//               O^T += V^T P^T (M=128 latent dims x 4 blocks, N=rows,
-//               K=64 tokens) into a TMEM accumulator of 4 x 64 columns.  P.V
-//               of a tile is issued the moment its probabilities are ready;
-//               QK^T of the next tile is issued whole once its data is in, so
-//               it never queues in the tensor pipe ahead of a ready P.V.
-//               With kSplitPV (requests of at most 64 query rows, the
-//               HBM-bound case) warps 1 and 6 issue only QK^T and warp 7
-//               issues every P.V.
+//   warps 1, 6  QK^T issuers: each issues half of S = Q K^T (M=64 rows, N=64
+//               tokens; even / odd 64-wide chunks of K=576 into two TMEM
+//               accumulators that the softmax adds), once the tile's stage
+//               has landed.  One thread issues a tcgen05.mma about every 40
+//               cycles, so these small MMAs need several issuing warps.
+//   warps 7..10 P.V issuers: warp 7 + b issues latent block b of O^T += V^T P^T
+//               (M=128 latent dims, N=rows, K=64 tokens) the moment the
+//               tile's probabilities are ready, into a TMEM accumulator of
+//               4 x 64 columns; the stage is free when all four are done.
 //   warps 2..5  softmax: two threads per query row (32 logits each) read S
 //               from TMEM, mask, keep the running max / sum and write bf16
 //               probabilities into the tile's own rope-chunk slot (free once
@@ -41,8 +37,8 @@
 //               O^T is rescaled in TMEM only when a running max grows by more
 //               than 2^8; the epilogue writes o = O / l and lse = m + ln l.
 //
-// Work is a flat list of tiles over all units (stream-K): CTA c takes tiles
-// [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
+// Work is a flat list of tiles over all units (stream-K): CTA c takes work
+// positions [c*per, (c+1)*per).  A unit that lies wholly inside one CTA's range is
 // written straight to out_partial; pieces of a split unit go to workspace
 // slots and are merged by mla_merge_kernel.
 #include <cuda_bf16.h>
@@ -55,8 +51,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 224;              // + one P.V issuer warp (7) with kSplitPV
+constexpr int kThreads = 352;
 constexpr int kIssuers = 2;                // QK^T-issuing warps (1 and 6)
+constexpr int kPvIssuers = 4;              // P.V-issuing warps (7..10), one latent block each
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -103,8 +100,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-template <bool kLocal, bool kSplitPV>
-__global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
+template <bool kLocal>
+__global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -139,11 +136,11 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
       mbar_init(b_kv_full + 8 * st, 1);
-      mbar_init(b_kv_empty + 8 * st, kSplitPV ? 1 : kIssuers);
+      mbar_init(b_kv_empty + 8 * st, kPvIssuers);
       mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
       mbar_init(b_p_full + 8 * st, kSoftmaxWarps);
-      mbar_init(b_pv_done + 8 * st, kSplitPV ? 1 : kIssuers);
+      mbar_init(b_pv_done + 8 * st, kPvIssuers);
     }
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, kIssuers);
@@ -249,10 +246,8 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (kSplitPV && (warp == 1 || warp == 6)) {
+  } else if (warp == 1 || warp == 6) {
     // ------------------------------------------------------------ QK^T issue
-    // (kSplitPV: the QK^T issuers wait on one barrier at a time, warp 7 issues
-    // every P.V as soon as its probabilities are ready)
     const int mi = warp == 6 ? 1 : 0;
     const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
     const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
@@ -291,7 +286,8 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (kSplitPV && warp == 7) {
+  } else if (warp >= 7 && warp <= 10) {
+    const int pmi = warp - 7;   // the latent block this warp issues
     // ------------------------------------------------------------ P.V issue
     const uint64_t dv0 = sw128_desc(sKV, 1024, kGroupBytes);
     const uint64_t dp0 = sw128_desc(sKV + kGroupRope, 16, kGroupBytes);
@@ -311,7 +307,7 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
           const int st = g & 1;
           const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
+          for (int blk = pmi; blk < pmi + 1; ++blk) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a =
@@ -327,108 +323,6 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
         __syncwarp();
       }
       gbase += t1 - t0;
-      ++pc;
-    }
-    if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (!kSplitPV && (warp == 1 || warp == 6)) {
-    // ------------------------------------------------------------ MMA issue
-    const int mi = warp == 6 ? 1 : 0;    // issuer index: chunk parity / latent half
-    const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
-    // descriptor bases; adding (byte offset >> 4) moves the start address
-    const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
-    // K (B of QK^T, K-major): 8-slot groups 9216 bytes apart; V^T (A of P.V,
-    // MN-major): 64-dim blocks 1024 bytes apart, 8-token groups 9216 apart;
-    // P (B of P.V, K-major): query-row groups in the groups' rope atoms
-    const uint64_t dkv0 = sw128_desc(sKV, 16, kGroupBytes);
-    const uint64_t dv0 = sw128_desc(sKV, 1024, kGroupBytes);
-    const uint64_t dp0 = sw128_desc(sKV + kGroupRope, 16, kGroupBytes);  // P of stage 0
-    int gbase = 0, pc = 0;
-    bool ok = true;
-    while (ok && it.next(unit, t0, t1, whole, slot)) {
-      Unit x = make_unit<kLocal>(pd, unit);
-      const int n = t1 - t0;
-      const uint32_t id_pv = idesc_bf16_f32(128, x.rows, true, false);
-      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
-      int nq = 0, np = 0;
-      uint64_t t_idle = 0;
-      uint32_t idle_iter = 0;
-      while (ok && np < n) {
-        bool did = false;
-        // P.V of the oldest tile whose probabilities are ready
-        if (np < nq) {
-          const int g = gbase + np;
-          bool ready = mbar_test(b_p_full + 8 * (g & 1), (g >> 1) & 1);
-          if (ready && np == 0 && pc >= 1) ready = mbar_test(b_o_free, (pc - 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            if (lane == 0) {
-              const int st = g & 1;
-              const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
-#pragma unroll
-              for (int blk = 2 * mi; blk < 2 * mi + 2; ++blk) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t a =
-                      dv0 + st_off + (uint32_t)((2 * blk * 1024 + kk * 2 * kGroupBytes) >> 4);
-                  const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
-                  mma_bf16_ss(tmem + kColO + 64 * blk, a, bd, id_pv,
-                              (np == 0 && kk == 0) ? 0u : 1u);
-                }
-              }
-              mma_commit(b_kv_empty + 8 * st);
-              mma_commit(b_pv_done + 8 * st);
-            }
-            __syncwarp();
-            ++np;
-            did = true;
-          }
-        }
-        // QK^T of the next tile, issued whole once all its chunk groups have
-        // landed: issued piecemeal, its MMAs would queue in the tensor pipe
-        // ahead of a P.V that becomes ready meanwhile, and P.V is what frees
-        // a stage for the next load
-        if (!did && nq < n) {
-          const int g = gbase + nq;
-          const int st = g & 1;
-          bool ready = mbar_test(b_kv_full + 8 * st, (g >> 1) & 1);
-          if (ready && g >= 2) ready = mbar_test(b_s_empty + 8 * st, ((g >> 1) - 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            if (lane == 0) {
-              const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
-              const uint32_t d = tmem + kColS0 + 128 * st + 64 * mi;
-#pragma unroll
-              for (int c = mi; c < kChunks; c += kIssuers) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint32_t offq = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
-                  const uint32_t offk = (uint32_t)((c * 1024 + 32 * k) >> 4);
-                  mma_bf16_ss(d, dq0 + offq, dkv0 + st_off + offk, id_qk,
-                              (c != mi || k != 0) ? 1u : 0u);
-                }
-              }
-              mma_commit(b_s_full + 8 * st);
-              if (nq == n - 1) mma_commit(b_q_empty);
-            }
-            __syncwarp();
-            ++nq;
-            did = true;
-          }
-        }
-        if (did) {
-          t_idle = 0;
-          idle_iter = 0;
-        } else {
-          // nothing ready: park briefly on the event expected next
-          if ((++idle_iter & 63u) == 0) {
-            const uint64_t now = globaltimer_ns();
-            if (t_idle == 0) t_idle = now;
-            if (now - t_idle > tmo || *abort_flag) ok = false;
-            ok = __all_sync(0xffffffffu, ok);
-          }
-        }
-      }
-      gbase += n;
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
@@ -657,45 +551,35 @@ __global__ void __launch_bounds__(kSplitPV ? kThreads + 32 : kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-template <bool kLocal, bool kSplitPV>
+template <bool kLocal>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const PartialParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kLocal, kSplitPV>,
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kLocal>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kSplitPV ? kThreads + 32 : kThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal, kSplitPV>, tm_q, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, p);
 }
 
 // The cache kind (local slice or whole requests) is a template parameter:
 // branching on it at run time cost about 2% on the bimodal batch.
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const PartialParams& p, int grid, cudaStream_t stream) {
-  // Requests whose query rows fit one 64-row group read each KV tile once
-  // from HBM: there P.V gets its own issuing warp, so a stage is released as
-  // soon as its probabilities are ready (+1% on the bimodal batch).  With
-  // several groups per request (long verify steps) the tiles come from L2,
-  // the tensor pipe bounds the kernel, and P.V interleaved with QK^T on two
-  // issuers is faster (4% on 16 x 9 queries x 64 heads).
-  const bool split_pv = p.pd.R <= kRows;
-  if (p.pd.local)
-    return split_pv ? launch_partial<true, true>(tm_q, tm_kv, p, grid, stream)
-                    : launch_partial<true, false>(tm_q, tm_kv, p, grid, stream);
-  return split_pv ? launch_partial<false, true>(tm_q, tm_kv, p, grid, stream)
-                  : launch_partial<false, false>(tm_q, tm_kv, p, grid, stream);
+  return p.pd.local ? launch_partial<true>(tm_q, tm_kv, p, grid, stream)
+                    : launch_partial<false>(tm_q, tm_kv, p, grid, stream);
 }
 
 }  // namespace mla
