@@ -191,8 +191,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // are nv pages x 64/nv rows, slot a in 8-slot group a/8.  The bf16 view
   // (64 dims, row in group, chunk, group, cache row) with strides
   // (-, 1152 nv, 128, 9216 nv, 1152) starts at cache row page*64 + residue
-  // and lands the residue's 64/nv rows of a page, all 9 chunks, in one box in
-  // the group-major shared-memory layout.
+  // and lands the residue's 64/nv rows of a page in the group-major
+  // shared-memory layout: all 9 chunks in one box (fp8), or three chunks per
+  // box, one box per chunk group (bf16).
   const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   CUtensorMap tm_q8;
@@ -228,7 +229,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
                           (cuuint64_t)kv->num_pages * kPage};
     cuuint64_t strides[4] = {(cuuint64_t)kDqk * 2 * nv, 128, (cuuint64_t)kDqk * 2 * 8 * nv,
                              (cuuint64_t)kDqk * 2};
-    cuuint32_t box[5] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kPage / 8 / nv), 1};
+    cuuint32_t box[5] = {64, 8, (cuuint32_t)kCgChunks, (cuuint32_t)(kPage / 8 / nv), 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

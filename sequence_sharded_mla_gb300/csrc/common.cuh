@@ -17,6 +17,7 @@ constexpr int kRows = 64;        // query rows per work unit (MMA M of QK^T)
 constexpr int kChunks = 9;       // 576 / 64: 128-byte swizzle chunks per row
 constexpr int kChunkBytes = 64 * 128;            // 64 rows x 64 bf16
 constexpr int kTileBytes = kChunks * kChunkBytes;  // 73728
+constexpr int kCgChunks = 3;     // bf16 kernel: chunks per KV TMA box (one chunk group)
 constexpr int kMaxShards = 8;
 
 // Error bits written to the workspace error word.

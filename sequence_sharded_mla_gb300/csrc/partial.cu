@@ -11,21 +11,25 @@
 // Data flow per persistent CTA (one per SM, 352 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
-//               (one TMA box per page, 128-byte swizzle) into two stages; a
+//               (TMA boxes per page and chunk group, 128-byte swizzle) into two stages; a
 //               stage is refilled as soon as its P.V is done.
 //
-// Stage layout ("group-major"): token slot a of a tile lies in 8-slot group
-// a/8 at byte (a/8)*9216 + c*1024 + (a%8)*128 for 64-wide chunk c, i.e. each
-// 8-row x 128-byte swizzle atom of a group's nine chunks is contiguous.  The
-// MMAs only need a uniform stride between 8-row groups (9216 bytes), and a
+// Stage layout: the nine 64-wide chunks of a row form three chunk groups
+// (chunks 3c..3c+2 in group c, 24576 bytes each); inside a chunk group,
+// token slot a lies in 8-slot group a/8 at byte (a/8)*3072 + (c%3)*1024 +
+// (a%8)*128 for chunk c, so each 8-row x 128-byte swizzle atom is whole.  The
+// MMAs only need a uniform stride between 8-row groups (3072 bytes), and a
 // page's slots of one interleaved shard are whole groups, so one TMA box
-// brings every chunk of a page's slots: N boxes per tile for N interleaved
-// shards instead of 9N with a chunk-major layout.
+// brings a chunk group of a page's slots: 3N boxes per tile for N
+// interleaved shards.  Each chunk group of a stage has its own barrier, and
+// QK^T starts on the first chunk group while the others are in flight, which
+// shortens the time a stage is held after its last byte lands.
 //   warps 1, 6  QK^T issuers: each issues half of S = Q K^T (M=64 rows, N=64
-//               tokens; even / odd 64-wide chunks of K=576 into two TMEM
-//               accumulators that the softmax adds), once the tile's stage
-//               has landed.  One thread issues a tcgen05.mma about every 40
-//               cycles, so these small MMAs need several issuing warps.
+//               tokens; two of the four K16 steps of every 64-wide chunk of
+//               K=576, into two TMEM accumulators that the softmax adds), a
+//               chunk group at a time as each lands.  One thread issues a
+//               tcgen05.mma about every 40 cycles, so these small MMAs need
+//               several issuing warps.
 //   warps 7..10 P.V issuers: warp 7 + b issues latent block b of O^T += V^T P^T
 //               (M=128 latent dims, N=rows, K=64 tokens) the moment the
 //               tile's probabilities are ready, into a TMEM accumulator of
@@ -60,7 +64,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kSoftmaxWarps = 4;
 
 struct Misc {
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t kv_full[2 * 3], kv_empty[2];   // kv_full: per stage, one per chunk group
   uint64_t s_full[2], s_empty[2];
   // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
   // single barrier could complete two phases between tests and alias parities
@@ -74,9 +78,16 @@ struct Misc {
 
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kTileBytes;
-constexpr int kGroupBytes = kChunks * 1024;          // 9216: one 8-slot group, all chunks
-constexpr int kGroupRope = 8 * 1024;                 // rope atom inside a group (P after QK^T)
-static_assert(kTileBytes == 8 * kGroupBytes, "tile = 8 groups");
+// A stage holds three chunk groups of three 64-wide chunks each
+// (chunks 3c..3c+2 in group c); inside a chunk group, 8-slot group a/8 of
+// the tile lies at (a/8)*3072, chunk at +1024*(chunk%3), slot at +128*(a%8).
+constexpr int kCg = kChunks / kCgChunks;             // chunk groups per tile
+constexpr int kGroupBytes = kCgChunks * 1024;        // 3072: one 8-slot group of a chunk group
+constexpr int kCgBytes = 8 * kGroupBytes;            // 24576: one chunk group of a tile
+static_assert(kTileBytes == kCg * kCgBytes, "tile = 3 chunk groups");
+// byte offset of 64-wide chunk c (of 8-slot group 0) inside a stage
+__host__ __device__ constexpr int chunk_off(int c) { return (c / kCgChunks) * kCgBytes + (c % kCgChunks) * 1024; }
+constexpr int kGroupRope = chunk_off(kChunks - 1);   // rope chunk (P after QK^T)
 constexpr int kSmemMisc = 3 * kTileBytes;
 constexpr int kSmemBytes = kSmemMisc + 2048 + 1024;  // + misc + alignment slack
 static_assert(sizeof(Misc) <= 2048, "misc block");
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
-      mbar_init(b_kv_full + 8 * st, 1);
+      for (int cg = 0; cg < kCg; ++cg) mbar_init(b_kv_full + 8 * (kCg * st + cg), 1);
       mbar_init(b_kv_empty + 8 * st, kPvIssuers);
       mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // page boxes per tile: N pages' residue rows for interleaved shards of a
     // global cache, otherwise one whole page
     const int nv = (pd.layout == kInterleaved && !kLocal) ? pd.num_shards : 1;
-    const int box_bytes = kTileBytes / nv;   // bf16: the whole groups of one page
+    const int box_bytes = kCgBytes / nv;     // one chunk group of one page's slots
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -208,17 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                           mbar_wait(b_kv_empty + 8 * st, ((gt >> 1) - 1) & 1, tmo, abort_flag));
           if (!ok) break;
         }
-        const uint32_t full = b_kv_full + 8 * st;
+        const uint32_t full = b_kv_full + 8 * kCg * st;
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, kTileBytes);
+#pragma unroll
+          for (int cg = 0; cg < kCg; ++cg) mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
           armed_kv[st] = gt;
         }
         __syncwarp();
         if (lane < nv) {
           // cache row page*64 + res of the (row-in-group, chunk, group, row)
-          // view; a page of num_pages is out of range and fills zeros
-          tma_load_5d(sKV + st * kTileBytes + lane * box_bytes, &tm_kv, full, 0, 0, 0, 0,
-                      page * kPage + res);
+          // view; a page of num_pages is out of range and fills zeros.  The
+          // chunk groups go out in order, each on its own barrier, so QK^T
+          // can start on the first while the others are still in flight.
+#pragma unroll
+          for (int cg = 0; cg < kCg; ++cg)
+            tma_load_5d(sKV + st * kTileBytes + cg * kCgBytes + lane * box_bytes, &tm_kv,
+                        full + 8 * cg, 0, 0, kCgChunks * cg, 0, page * kPage + res);
         }
         __syncwarp();
         if (ok && j == t0) {
@@ -259,24 +275,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = t0; ok && j < t1; ++j) {
         const int g = gbase + (j - t0);
         const int st = g & 1;
-        bool w = mbar_wait(b_kv_full + 8 * st, (g >> 1) & 1, tmo, abort_flag);
-        if (g >= 2) w = w && mbar_wait(b_s_empty + 8 * st, ((g >> 1) - 1) & 1, tmo, abort_flag);
-        ok = __all_sync(0xffffffffu, w);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
-          const uint32_t d = tmem + kColS0 + 128 * st + 64 * mi;
+        if (g >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(b_s_empty + 8 * st, ((g >> 1) - 1) & 1, tmo,
+                                                 abort_flag));
+          if (!ok) break;
+        }
+        const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
+        const uint32_t d = tmem + kColS0 + 128 * st + 64 * mi;
+        // issuer mi takes K16 steps 2mi, 2mi+1 of every chunk, chunk group by
+        // chunk group as each lands
 #pragma unroll
-          for (int c = mi; c < kChunks; c += kIssuers) {
+        for (int cg = 0; cg < kCg; ++cg) {
+          ok = __all_sync(0xffffffffu, mbar_wait(b_kv_full + 8 * (kCg * st + cg), (g >> 1) & 1,
+                                                 tmo, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t offq = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
-              const uint32_t offk = (uint32_t)((c * 1024 + 32 * k) >> 4);
-              mma_bf16_ss(d, dq0 + offq, dkv0 + st_off + offk, id_qk,
-                          (c != mi || k != 0) ? 1u : 0u);
+            for (int c = kCgChunks * cg; c < kCgChunks * (cg + 1); ++c) {
+#pragma unroll
+              for (int k = 2 * mi; k < 2 * mi + 2; ++k) {
+                const uint32_t offq = (uint32_t)((c * kChunkBytes + 32 * k) >> 4);
+                const uint32_t offk = (uint32_t)((chunk_off(c) + 32 * k) >> 4);
+                mma_bf16_ss(d, dq0 + offq, dkv0 + st_off + offk, id_qk,
+                            (c != 0 || k != 2 * mi) ? 1u : 0u);
+              }
             }
           }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) {
           mma_commit(b_s_full + 8 * st);
           if (j == t1 - 1) mma_commit(b_q_empty);
         }
@@ -289,7 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 7 && warp <= 10) {
     const int pmi = warp - 7;   // the latent block this warp issues
     // ------------------------------------------------------------ P.V issue
-    const uint64_t dv0 = sw128_desc(sKV, 1024, kGroupBytes);
+    // V^T of latent block pmi: chunks 2 pmi and 2 pmi + 1, the two 64-dim
+    // swizzle atoms of M, lie chunk_off(2 pmi + 1) - chunk_off(2 pmi) apart
+    const uint64_t dv0 = sw128_desc(sKV + chunk_off(2 * pmi),
+                                    chunk_off(2 * pmi + 1) - chunk_off(2 * pmi), kGroupBytes);
     const uint64_t dp0 = sw128_desc(sKV + kGroupRope, 16, kGroupBytes);
     int gbase = 0, pc = 0;
     bool ok = true;
@@ -307,15 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = g & 1;
           const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
 #pragma unroll
-          for (int blk = pmi; blk < pmi + 1; ++blk) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a =
-                  dv0 + st_off + (uint32_t)((2 * blk * 1024 + kk * 2 * kGroupBytes) >> 4);
-              const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
-              mma_bf16_ss(tmem + kColO + 64 * blk, a, bd, id_pv,
-                          (j == t0 && kk == 0) ? 0u : 1u);
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = dv0 + st_off + (uint32_t)((kk * 2 * kGroupBytes) >> 4);
+            const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
+            mma_bf16_ss(tmem + kColO + 64 * pmi, a, bd, id_pv, (j == t0 && kk == 0) ? 0u : 1u);
           }
           mma_commit(b_kv_empty + 8 * st);
           mma_commit(b_pv_done + 8 * st);
@@ -448,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int a = e >> 6, plane = (e >> 3) & 7, ch = e & 7;
             int t = slot_token<kLocal>(pd, x, j, a);
             if (!slot_valid(pd, x, t))
-              *reinterpret_cast<uint4*>(st + (a >> 3) * kGroupBytes + plane * 1024 +
+              *reinterpret_cast<uint4*>(st + chunk_off(plane) + (a >> 3) * kGroupBytes +
                                         (a & 7) * 128 + ch * 16) =
                   make_uint4(0, 0, 0, 0);
           }
@@ -538,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after a failure, let this CTA's own TMA copies land before it exits
     int never = 0;
     for (int st = 0; st < 2; ++st)
-      if (armed_kv[st] >= 0) mbar_wait(b_kv_full + 8 * st, (armed_kv[st] >> 1) & 1, tmo, &never);
+      for (int cg = 0; cg < kCg && armed_kv[st] >= 0; ++cg)
+        mbar_wait(b_kv_full + 8 * (kCg * st + cg), (armed_kv[st] >> 1) & 1, tmo, &never);
     if (armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, tmo, &never);
   }
   tc_fence_before();
