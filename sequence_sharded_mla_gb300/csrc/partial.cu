@@ -12,7 +12,10 @@
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
 //               (TMA boxes per page and chunk group, 128-byte swizzle) into two stages; a
-//               stage is refilled as soon as its P.V is done.
+//               stage is refilled as soon as its P.V is done.  The next
+//               tile of the piece is prefetched into L2 (TMA prefetch, no
+//               shared memory) when a tile's load is issued: the two stages
+//               alone keep too few bytes in flight to cover DRAM latency.
 //
 // Stage layout: the nine 64-wide chunks of a row form three chunk groups
 // (chunks 3c..3c+2 in group c, 24576 bytes each); inside a chunk group,
@@ -62,6 +65,7 @@ constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kSoftmaxWarps = 4;
+constexpr int kPrefetch = 1;               // tiles of a piece prefetched into L2 ahead of the stage loads
 
 struct Misc {
   uint64_t kv_full[2 * 3], kv_empty[2];   // kv_full: per stage, one per chunk group
@@ -196,8 +200,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
       const int res = nv > 1 ? x.s : 0;
       int win_base = -1, win_val = -1;
+      int pwin_base = -1, pwin_val = -1;   // block-table window of the L2 prefetches
       for (int j = t0; j < t1 && ok; ++j, ++gt) {
         const int st = gt & 1;
+        // L2 prefetch of the piece's tiles up to kPrefetch ahead: with two
+        // stages, an SM's own loads keep too few bytes in flight to cover
+        // the DRAM latency; a stage load then reads L2
+        for (int jp = (j == t0 ? j + 1 : j + kPrefetch); jp <= j + kPrefetch && jp < t1; ++jp) {
+          const int fs = nv > 1 ? jp * nv : (kLocal || pd.layout == kInterleaved ? jp : x.p0 + jp);
+          const int pwb = fs & ~31;
+          if (pwb != pwin_base && fs < npages_b) {
+            pwin_base = pwb;
+            const int e = pwb + lane;
+            pwin_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
+          }
+          const int pidx = fs + lane;
+          const int pg = __shfl_sync(0xffffffffu, pwin_val, pidx & 31);
+          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages) {
+#pragma unroll
+            for (int cg = 0; cg < kCg; ++cg)
+              tma_prefetch_l2_5d(&tm_kv, 0, 0, kCgChunks * cg, 0, pg * kPage + res);
+          }
+        }
         // page slot of this lane's box; nv divides 32, so a tile never
         // straddles two 32-entry windows of the block table
         const int first_slot = nv > 1 ? j * nv : (kLocal || pd.layout == kInterleaved ? j : x.p0 + j);
