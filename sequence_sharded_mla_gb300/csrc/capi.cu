@@ -39,8 +39,10 @@ constexpr int kVersion = 200;  // 0.2.0
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // device waits give up after 2 s
 constexpr int kMinTilesPerCta = 4;
 // Work positions charged to a unit for its fixed costs (query load, pipeline
-// refill, the epilogue's 128 KB of output): about two tiles' time.
-constexpr int kUnitCost = 2;
+// refill without the L2 prefetch, the epilogue's 128 KB of output): about
+// three tiles' time (measured: 2, 3, 4 and 5 on the bimodal batch 0.546,
+// 0.532, 0.530, 0.530 ms; on the q_len-9 batch 3 is best).
+constexpr int kUnitCost = 3;
 
 using host::aligned16;
 using host::aligned4;
