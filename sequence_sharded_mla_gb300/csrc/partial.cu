@@ -11,11 +11,12 @@
 // Data flow per persistent CTA (one per SM, 352 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
-//               (TMA boxes per page and chunk group, 128-byte swizzle) into two stages; a
-//               stage is refilled as soon as its P.V is done.  The next
-//               tile of the piece is prefetched into L2 (TMA prefetch, no
-//               shared memory) when a tile's load is issued: the two stages
-//               alone keep too few bytes in flight to cover DRAM latency.
+//               (one box per page and chunk group, 128-byte swizzle) into
+//               two stages; a stage is refilled as soon as its P.V is done.
+//               The next tile of the piece is prefetched into L2 (TMA
+//               prefetch, no shared memory) when a tile's load is issued:
+//               the two stages alone keep too few bytes in flight to cover
+//               the DRAM latency.
 //
 // Stage layout: the nine 64-wide chunks of a row form three chunk groups
 // (chunks 3c..3c+2 in group c, 24576 bytes each); inside a chunk group,
