@@ -193,9 +193,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // are nv pages x 64/nv rows, slot a in 8-slot group a/8.  The bf16 view
   // (64 dims, row in group, chunk, group, cache row) with strides
   // (-, 1152 nv, 128, 9216 nv, 1152) starts at cache row page*64 + residue
-  // and lands the residue's 64/nv rows of a page in the group-major
-  // shared-memory layout: all 9 chunks in one box (fp8), or three chunks per
-  // box, one box per chunk group (bf16).
+  // and lands the residue's 64/nv rows of a page in the kernels'
+  // shared-memory layouts: all 9 chunks of each 8-slot group in one box
+  // (fp8), or three chunks per box, one box per chunk group (bf16).
   const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   CUtensorMap tm_q8;
