@@ -16,7 +16,8 @@
 namespace mla {
 int partial_smem_bytes();
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                const PartialParams& p, int grid, cudaStream_t stream);
+                                const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
+                                cudaStream_t stream);
 cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                const PartialParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
@@ -169,7 +170,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   // query rows: [B*q_len*H, 576] bf16.  Preferred view [rows][9 chunks][64]
   // read as (64 dims, rows, chunk) so one box lands a 64-row group in the
   // [chunk][row][64] shared-memory layout; fallback: one box per chunk.
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_kv, tm_kv_pf;
   int q_one_box = 1;
   {
     cuuint64_t dims[3] = {64, (cuuint64_t)pd.B * pd.R, (cuuint64_t)kChunks};
@@ -237,6 +238,12 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
+    // the same view with all nine chunks in one box, for the L2 prefetch
+    box[2] = (cuuint32_t)kChunks;
+    if (encode(&tm_kv_pf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -261,7 +268,7 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
     return MLA_ERR_CUDA;
   const cudaError_t le = fp8 ? launch_partial_fp8(tm_q8, tm_kv, p, grid, st)
-                             : launch_partial_bf16(tm_q, tm_kv, p, grid, st);
+                             : launch_partial_bf16(tm_q, tm_kv, tm_kv_pf, p, grid, st);
   if (ev1 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev1), st) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (le != cudaSuccess) return MLA_ERR_CUDA;

@@ -119,7 +119,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
+                       const __grid_constant__ CUtensorMap tm_kv,
+                       const __grid_constant__ CUtensorMap tm_kv_pf, PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, formed by pointer arithmetic on the shared array
   // (not through an integer) so that the compiler keeps every access through
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_kv_pf);
   }
   tc_fence_before();
   __syncthreads();
@@ -217,11 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int pidx = fs + lane;
           const int pg = __shfl_sync(0xffffffffu, pwin_val, pidx & 31);
-          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages) {
-#pragma unroll
-            for (int cg = 0; cg < kCg; ++cg)
-              tma_prefetch_l2_5d(&tm_kv, 0, 0, kCgChunks * cg, 0, pg * kPage + res);
-          }
+          // one box per page: the prefetch needs no chunk-group barriers,
+          // and every TMA box costs issue throughput
+          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages)
+            tma_prefetch_l2_5d(&tm_kv_pf, 0, 0, 0, 0, pg * kPage + res);
         }
         // page slot of this lane's box; nv divides 32, so a tile never
         // straddles two 32-entry windows of the block table
@@ -606,7 +607,8 @@ int partial_smem_bytes() { return kSmemBytes; }
 
 template <bool kLocal>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                  const PartialParams& p, int grid, cudaStream_t stream) {
+                                  const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
+                                  cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -624,15 +626,16 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, tm_kv_pf, p);
 }
 
 // The cache kind (local slice or whole requests) is a template parameter:
 // branching on it at run time cost about 2% on the bimodal batch.
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
-                                const PartialParams& p, int grid, cudaStream_t stream) {
-  return p.pd.local ? launch_partial<true>(tm_q, tm_kv, p, grid, stream)
-                    : launch_partial<false>(tm_q, tm_kv, p, grid, stream);
+                                const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
+                                cudaStream_t stream) {
+  return p.pd.local ? launch_partial<true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
+                    : launch_partial<false>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
 }
 
 }  // namespace mla
