@@ -44,6 +44,11 @@ constexpr int kMinTilesPerCta = 4;
 // three tiles' time (measured: 2, 3, 4 and 5 on the bimodal batch 0.546,
 // 0.532, 0.530, 0.530 ms; on the q_len-9 batch 3 is best).
 constexpr int kUnitCost = 3;
+// The fp8 kernel's fixed cost per piece is far larger in tiles (its tiles
+// are half the bytes, and a piece splits its query into two e4m3 terms and
+// refills four stages): per CTA, one more piece ended the CTA ≈13.5 µs
+// later, about 22 of its tiles.
+constexpr int kUnitCostFp8 = 16;
 
 using host::aligned16;
 using host::aligned4;
@@ -262,7 +267,9 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.timeout_ns = kTimeoutNs;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, kUnitCost, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, fp8 ? kUnitCostFp8 : kUnitCost,
+                  st) != cudaSuccess)
+    return MLA_ERR_CUDA;
   void* ev0 = host::g_ev_before.load();
   void* ev1 = host::g_ev_after.load();
   if (ev0 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev0), st) != cudaSuccess)
