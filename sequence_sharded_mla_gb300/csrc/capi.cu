@@ -47,8 +47,9 @@ constexpr int kUnitCost = 3;
 // The fp8 kernel's fixed cost per piece is far larger in tiles (its tiles
 // are half the bytes, and a piece splits its query into two e4m3 terms and
 // refills four stages): per CTA, one more piece ended the CTA ≈13.5 µs
-// later, about 22 of its tiles.
-constexpr int kUnitCostFp8 = 16;
+// later, about 22 of its tiles.  Measured on the long-tail fp8 batch: 3, 10,
+// 16 and 24 gave 0.296, 0.291, 0.293 and 0.295 ms.
+constexpr int kUnitCostFp8 = 10;
 
 using host::aligned16;
 using host::aligned4;
