@@ -37,7 +37,9 @@
  * form, so that it shares no structure with the kernel.
  *
  * Parity pins (tests/test_oracle_pins.py): brute force in extended precision
- * without max subtraction; single-token and identical-key closed forms; the
+ * without max subtraction, for bf16 caches and for fp8 caches with
+ * row-varying token scales; single-token (bf16 and fp8) and identical-key
+ * closed forms; the
  * sharded-then-merged result equals the unsharded one for every N and both
  * layouts; block-table page permutation invariance; causal row i equals a
  * q_len = 1 query at context L - q_len + 1 + i; e4m3 decoding against the

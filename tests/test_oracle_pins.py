@@ -33,6 +33,17 @@ def _bf16(bits):
     return float(mi.bf16_bits_to_f32(np.array([bits], dtype=np.uint16))[0])
 
 
+def cache_row_decimal(w, page, row):
+    """Row ``row`` of page ``page`` as exact Decimals: bf16 bits decoded, or
+    e4m3 codes decoded by the closed form of the format (written out below,
+    independent of the oracle's decoder) times the token's own fp32 scale,
+    on all 576 entries (one scale per token: latent and rope alike)."""
+    if w.kv_dtype == "bf16":
+        return [Decimal(_bf16(x)) for x in w.kv[page, row]]
+    sc = Decimal(float(w.kv_scale[page, row]))
+    return [Decimal(e4m3_closed_form(int(c))) * sc for c in w.kv[page, row]]
+
+
 def brute_force_row(w, b, i, h):
     """Attention for one query row in Decimal arithmetic, straight from the
     definition: exp of the scaled logits without subtracting a maximum,
@@ -47,8 +58,7 @@ def brute_force_row(w, b, i, h):
         if w.causal and t > L - w.q_len + i:
             continue
         page = int(w.block_table[b, t // 64])
-        row = w.kv[page, t % 64]
-        k = [Decimal(_bf16(x)) for x in row]
+        k = cache_row_decimal(w, page, t % 64)
         s = sum(qa * ka for qa, ka in zip(q, k)) * scale
         e = s.exp()
         den += e
@@ -74,6 +84,36 @@ def test_brute_force_matches_oracle(seed, lens, q_len, causal):
                 assert np.max(np.abs(bo - out[r])) <= 1e-12 * max(1e-3, np.max(np.abs(bo)))
 
 
+def spread_token_scales(w, seed):
+    """Multiply every token's scale of an fp8 cache by its own factor,
+    log-uniform over 2^-2 .. 2^2 and different for every row of a page, so
+    that a scale looked up by page, by the wrong row, or applied to only
+    part of a row changes the result."""
+    u = mi.uniform01(seed, 3, w.kv_scale.size).reshape(w.kv_scale.shape)
+    f = np.exp2(-2.0 + 4.0 * u) * (1.0 + (np.arange(64)[None, :] % 5) / 8.0)
+    w.kv_scale[...] = (w.kv_scale * f).astype(np.float32)
+    return w
+
+
+@pytest.mark.parametrize("seed,lens,q_len,causal", [(14, (1, 64), 1, False),
+                                                     (15, (65, 30), 1, False),
+                                                     (16, (20, 9), 2, True)])
+def test_brute_force_matches_oracle_fp8(seed, lens, q_len, causal):
+    """The fp8 gather: e4m3 code times the token's scale on every entry."""
+    w = spread_token_scales(small(seed, lens=lens, q_len=q_len, causal=causal,
+                                  kv_dtype="fp8", kv_sigma=1.0), seed)
+    assert len(np.unique(w.kv_scale[w.block_table[0, 0]])) > 32
+    out, lse = orc.attend(w, shard=-1)
+    H = w.num_heads
+    for b in range(w.batch):
+        for i in range(w.q_len):
+            for h in range(H):
+                r = (b * w.q_len + i) * H + h
+                bo, bl = brute_force_row(w, b, i, h)
+                assert abs(bl - lse[r]) <= 1e-12 * max(1.0, abs(bl))
+                assert np.max(np.abs(bo - out[r])) <= 1e-12 * max(1e-3, np.max(np.abs(bo)))
+
+
 # --------------------------------------------------------------- closed forms
 def test_single_token_returns_its_value():
     w = small(21, lens=(1, 1))
@@ -87,6 +127,46 @@ def test_single_token_returns_its_value():
             assert np.array_equal(out[r], v[:512])          # out = V_0 exactly
             s0 = float(np.dot(q, v)) / math.sqrt(192.0)
             assert abs(lse[r] - s0) <= 1e-12 * max(1.0, abs(s0))
+
+
+def test_fp8_single_token_returns_its_scaled_value():
+    """A one-token context of an fp8 cache returns that token's dequantised
+    latent, code by code times its own scale, and the lse is its logit."""
+    w = spread_token_scales(small(23, lens=(1, 1), kv_dtype="fp8", kv_sigma=1.0), 23)
+    out, lse = orc.attend(w, shard=-1)
+    for b in range(2):
+        page = int(w.block_table[b, 0])
+        sc = float(w.kv_scale[page, 0])
+        v = np.array([e4m3_closed_form(int(c)) for c in w.kv[page, 0]]) * sc
+        for h in range(2):
+            r = b * 2 + h
+            q = mi.bf16_bits_to_f32(w.q[b, 0, h]).astype(np.float64)
+            assert np.array_equal(out[r], v[:512])
+            s0 = float(np.dot(q, v)) / math.sqrt(192.0)
+            assert abs(lse[r] - s0) <= 1e-12 * max(1.0, abs(s0))
+
+
+def test_fp8_scale_belongs_to_its_token():
+    """Scaling one token's scale by 2^k scales its whole dequantised row:
+    the same result as a bf16-free fp64 recomputation with that row's
+    values multiplied by 2^k, and different from scaling a neighbour."""
+    w = spread_token_scales(small(24, B=1, lens=(3,), kv_dtype="fp8", kv_sigma=1.0), 24)
+    page = int(w.block_table[0, 0])
+    base, base_lse = orc.attend(w, shard=-1)
+    w.kv_scale[page, 1] *= 1.5
+    o1, l1 = orc.attend(w, shard=-1)
+    rows = [np.array([e4m3_closed_form(int(c)) for c in w.kv[page, t]]) * float(w.kv_scale[page, t])
+            for t in range(3)]
+    K = np.stack(rows)
+    for h in range(2):
+        q = mi.bf16_bits_to_f32(w.q[0, 0, h]).astype(np.float64)
+        s = K @ q / math.sqrt(192.0)
+        m = s.max()
+        p = np.exp(s - m)
+        want = p @ K[:, :512] / p.sum()
+        assert np.max(np.abs(o1[h] - want)) <= 1e-12 * max(1.0, np.max(np.abs(want)))
+        assert abs(l1[h] - (m + math.log(p.sum()))) <= 1e-12 * max(1.0, abs(m))
+    assert not np.allclose(o1, base)
 
 
 def test_identical_keys_return_mean_of_values():
