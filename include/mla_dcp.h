@@ -177,20 +177,31 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
  * Arguments, layouts, results and host-side errors are those of
  * mla_decode_partial.
  *
- * The first call on a device looks up the scratch's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls on a device share the one scratch buffer, so calls whose kernels
- * overlap on the GPU (different streams, or different host threads) race:
- * order them on one stream.  Nothing needs clearing between calls; each call
- * rebuilds what it reads.  Device-side error words (see
- * mla_get_device_error) are kept in the scratch and are not reported by this
- * call.
+ * The first call in a CUDA context (normally: on a device) looks up the
+ * scratch's device address (cudaGetSymbolAddress) and keeps it for that
+ * context; make that first call before any stream capture.  All calls on a
+ * device share the one scratch buffer, so calls whose kernels overlap on the
+ * GPU (different streams, or different host threads) race: order them on
+ * one stream.  Nothing needs clearing between calls; each call rebuilds what
+ * it reads.  Device-side errors (a bad block-table page, a wait that timed
+ * out) are kept in the scratch's error word: read them with
+ * mla_get_device_error_noalloc.
  */
 mla_status mla_decode_partial_noalloc(const void* q, const mla_kv_pages* kv,
                                       const int32_t* block_table, int max_pages_per_req,
                                       const int32_t* seq_lens, const mla_shape* shape,
                                       int shard_id, int num_shards, mla_layout layout,
                                       float* out_partial, float* lse_partial, void* stream);
+
+/*
+ * The device error word of mla_decode_partial_noalloc's scratch on the
+ * current device: synchronises `stream`, reads and clears it, with the
+ * results of mla_get_device_error.  Like the entry point it serves, this has
+ * no counterpart on the pages; it lets callers that cannot allocate see a
+ * bad block-table page or a timed-out wait.  It reads the state left by the
+ * last mla_decode_partial_noalloc on the device, whatever its stream.
+ */
+mla_status mla_get_device_error_noalloc(void* stream);
 
 /*
  * LSE combine of N shard partials ("Decode Context Parallelism", section 4.1:
@@ -216,6 +227,28 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
  * occurred, or MLA_ERR_CUDA.
  */
 mla_status mla_get_device_error(void* workspace, void* stream);
+
+/*
+ * Testing and diagnostic aid (not part of the method): sets the time limit,
+ * in nanoseconds, of every device-side wait of the partial-attention kernels
+ * launched from now on (process-wide, any thread).  A wait that runs out
+ * makes its kernel stop early, with MLA_ERR_TIMEOUT in the error word and
+ * its outputs undefined; the kernel still lets its own copies and tensor-core
+ * operations finish and releases its tensor memory, so later calls work
+ * normally.  0 restores the default of 2 s.  Always MLA_OK.
+ */
+mla_status mla_set_wait_budget_ns(unsigned long long ns);
+
+/*
+ * Testing aid (not part of the method): while `on` is non-zero, the
+ * partial-attention kernels of mla_decode_partial launched from now on never
+ * load the query rows of each CTA's first piece of work (process-wide).  The
+ * waits for those rows cannot succeed, so each CTA stops once its wait
+ * budget (mla_set_wait_budget_ns) runs out, and mla_get_device_error then
+ * reads MLA_ERR_TIMEOUT; outputs are undefined.  This exercises the
+ * time-out path without any fault.  0 turns it off.  Always MLA_OK.
+ */
+mla_status mla_set_withhold_query(int on);
 
 /*
  * Profiling aid (not part of the method): while set, every later

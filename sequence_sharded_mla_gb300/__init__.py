@@ -57,9 +57,10 @@ class gqa_kv_pages(ctypes.Structure):
 
 _LIB = None
 EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
-           "mla_workspace_size", "mla_get_device_error", "mla_set_profile_events",
-           "mla_status_string", "mla_version", "gqa_workspace_size", "gqa_decode_partial",
-           "gqa_shard_combine")
+           "mla_workspace_size", "mla_get_device_error", "mla_get_device_error_noalloc",
+           "mla_set_wait_budget_ns", "mla_set_withhold_query", "mla_set_profile_events",
+           "mla_status_string",
+           "mla_version", "gqa_workspace_size", "gqa_decode_partial", "gqa_shard_combine")
 
 
 def lib():
@@ -83,6 +84,12 @@ def lib():
         L.mla_workspace_size.restype = sz
         L.mla_get_device_error.argtypes = [vp, vp]
         L.mla_get_device_error.restype = i32
+        L.mla_get_device_error_noalloc.argtypes = [vp]
+        L.mla_get_device_error_noalloc.restype = i32
+        L.mla_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
+        L.mla_set_wait_budget_ns.restype = i32
+        L.mla_set_withhold_query.argtypes = [i32]
+        L.mla_set_withhold_query.restype = i32
         L.mla_set_profile_events.argtypes = [vp, vp]
         L.mla_set_profile_events.restype = i32
         L.mla_status_string.argtypes = [i32]
@@ -207,12 +214,25 @@ def mla_decode_partial_noalloc(q, kv, block_table, seq_lens, num_shards, layout=
     _check(q, "q", (torch.bfloat16,), 4)
     dev = q.device
     B, q_len, H, _ = q.shape
-    kv_dtype = KV_BF16 if kv.dtype == torch.bfloat16 else KV_FP8
+    if kv.dtype == torch.bfloat16:
+        kv_dtype = KV_BF16
+    elif kv.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        kv_dtype = KV_FP8
+        _check(kv_scale, "kv_scale", (torch.float32,), 2, dev)
+    else:
+        raise TypeError(f"kv dtype {kv.dtype} unsupported")
+    _check(kv, "kv", (kv.dtype,), 3, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
     n_out = num_shards if shard_id == ALL_SHARDS else 1
     if out_partial is None:
         out_partial = torch.empty((n_out, B, q_len, H, D_V), dtype=torch.float32, device=dev)
     if lse_partial is None:
         lse_partial = torch.empty((n_out, B, q_len, H), dtype=torch.float32, device=dev)
+    _check(out_partial, "out_partial", (torch.float32,), 5, dev)
+    _check(lse_partial, "lse_partial", (torch.float32,), 4, dev)
+    if q_lens is not None:
+        _check(q_lens, "q_lens", (torch.int32,), 1, dev)
     sh = _shape(B, q_len, H, causal, softmax_scale, q_lens)
     pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
                          kv_dtype, kv.shape[0], kv.shape[1])
@@ -255,6 +275,24 @@ def mla_shard_combine(partials, lses, w_uv=None, out=None, lse_out=None, stream=
 def mla_get_device_error(workspace, stream=None) -> int:
     """Sync the stream, read and clear the device error word; returns a status code."""
     return int(lib().mla_get_device_error(_ptr(workspace), _stream_ptr(stream)))
+
+
+def mla_get_device_error_noalloc(stream=None) -> int:
+    """Sync the stream, read and clear the error word of the fixed scratch
+    used by mla_decode_partial_noalloc; returns a status code."""
+    return int(lib().mla_get_device_error_noalloc(_stream_ptr(stream)))
+
+
+def mla_set_wait_budget_ns(ns: int) -> None:
+    """Testing aid: time limit (ns) of every device-side wait of later
+    partial-attention launches; 0 restores the default (2 s)."""
+    lib().mla_set_wait_budget_ns(int(ns))
+
+
+def mla_set_withhold_query(on: bool) -> None:
+    """Testing aid: while on, later partial-attention launches never load the
+    first piece's query rows, so their waits run out (MLA_ERR_TIMEOUT)."""
+    lib().mla_set_withhold_query(int(bool(on)))
 
 
 def mla_set_profile_events(before=None, after=None) -> None:

@@ -265,7 +265,8 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   p.q_one_box = q_one_box;
   p.kv_fp8 = nullptr;
   p.q = static_cast<const uint16_t*>(q);
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = host::wait_budget_ns(kTimeoutNs);
+  p.withhold_query = host::g_withhold_query.load();
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(pd, p.hdr, p.prefix, grid, kMinTilesPerCta, fp8 ? kUnitCostFp8 : kUnitCost,
@@ -291,7 +292,8 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
                              void* stream) {
   if (!partials || !lses || !out || !shape_ok(shape)) return MLA_ERR_INVALID;
   if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
-  if (!aligned16(partials) || !aligned16(out) || (w_uv && !aligned16(w_uv)))
+  if (!aligned16(partials) || !aligned16(out) || (w_uv && !aligned16(w_uv)) ||
+      !aligned4(lses) || (lse_out && !aligned4(lse_out)))
     return MLA_ERR_INVALID;
   const int rows = shape->batch * shape->q_len * shape->num_heads;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -312,6 +314,16 @@ mla_status mla_set_profile_events(void* before_partial, void* after_partial) {
   return MLA_OK;
 }
 
+mla_status mla_set_wait_budget_ns(unsigned long long ns) {
+  host::g_wait_budget_ns.store(ns);
+  return MLA_OK;
+}
+
+mla_status mla_set_withhold_query(int on) {
+  host::g_withhold_query.store(on != 0 ? 1 : 0);
+  return MLA_OK;
+}
+
 mla_status mla_get_device_error(void* workspace, void* stream) {
   if (workspace == nullptr) return MLA_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -320,8 +332,9 @@ mla_status mla_get_device_error(void* workspace, void* stream) {
     return MLA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
   if (err != 0) {
-    unsigned zero = 0;
-    if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    // cleared in stream order, behind everything already queued on `stream`
+    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
   if (err & kErrTimeout) return MLA_ERR_TIMEOUT;

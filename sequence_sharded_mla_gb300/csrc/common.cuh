@@ -20,6 +20,11 @@ constexpr int kTileBytes = kChunks * kChunkBytes;  // 73728
 constexpr int kCgChunks = 3;     // bf16 kernel: chunks per KV TMA box (one chunk group)
 constexpr int kMaxShards = 8;
 
+// Bound on the waits of a kernel's teardown after another wait gave up: the
+// MMAs and copies it still has in flight always complete, so this limit is
+// independent of the (possibly very short) budget of the ordinary waits.
+constexpr unsigned long long kDrainNs = 2000000000ull;
+
 // Error bits written to the workspace error word.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrBadPage = 2u;
@@ -80,6 +85,7 @@ struct PartialParams {
   int q_one_box;        // 1: tm_q loads all 9 chunks of a 64-row group per box
   const uint8_t* kv_fp8;  // fp8 caches: [num_pages, 64, 576] codes
   unsigned long long timeout_ns;
+  int withhold_query;   // testing aid: 1 = never load the first piece's query rows
 };
 
 // Geometry of one work unit u = ((b * n_out) + so) * G + g.

@@ -145,6 +145,7 @@ struct Misc {
   uint64_t s_full[kStages], s_empty[kStages];
   uint64_t p_full[kStages], pv_done[kStages];
   uint64_t q_full, q_empty, o_free;
+  uint64_t drain;  // teardown after a failure: MMAs in flight
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(&misc->q_full), 1);
     mbar_init(bar(&misc->q_empty), 1);
     mbar_init(bar(&misc->o_free), kSoftmaxWarps);
+    mbar_init(bar(&misc->drain), 2);  // the two MMA-issuing threads
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -529,15 +531,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    int never = 0;
-    for (int st = 0; st < kStages; ++st)
-      if (armed_kv[st] >= 0)
-        mbar_wait(bar(&misc->kv_full[st]), (armed_kv[st] / kStages) & 1, tmo, &never);
-    if (armed_q >= 0) mbar_wait(bar(&misc->q_full), armed_q & 1, tmo, &never);
-  }
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // after a failure, let this CTA's own MMAs and copies complete first
+    int never = 0;
+    if (lane == 0 && (warp == 1 || warp == 6)) {
+      mma_commit(bar(&misc->drain));
+      mbar_wait(bar(&misc->drain), 0, kDrainNs, &never);
+    }
+    if (warp == 0 && lane == 0) {
+      for (int st = 0; st < kStages; ++st)
+        if (armed_kv[st] >= 0)
+          mbar_wait(bar(&misc->kv_full[st]), (armed_kv[st] / kStages) & 1, kDrainNs, &never);
+      if (armed_q >= 0) mbar_wait(bar(&misc->q_full), armed_q & 1, kDrainNs, &never);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -772,20 +783,14 @@ mla_status gqa_decode_partial(const void* q, const gqa_kv_pages* kv, const int32
   p.prefix = reinterpret_cast<int*>(ws + wl.prefix);
   p.ws_o = reinterpret_cast<float*>(ws + wl.ws_o);
   p.ws_lse = reinterpret_cast<float*>(ws + wl.ws_lse);
-  p.timeout_ns = gqa::kTimeoutNs;
+  p.timeout_ns = host::wait_budget_ns(gqa::kTimeoutNs);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   gqa::gqa_plan_kernel<<<1, 1024, 0, st>>>(d, p.hdr, p.prefix, grid);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    if (cudaFuncSetAttribute(gqa::gqa_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gqa::kSmemBytes) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    configured_device = dev;
-  }
+  if (host::ensure_dynamic_smem(reinterpret_cast<const void*>(&gqa::gqa_partial_kernel),
+                                gqa::kSmemBytes) != cudaSuccess)
+    return MLA_ERR_CUDA;
   cudaLaunchAttribute attr = pdl_attribute();
   void* ev0 = host::g_ev_before.load();
   void* ev1 = host::g_ev_after.load();

@@ -12,9 +12,8 @@
 // the ordinary partial-attention path on it.  Nothing here allocates.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
+#include "host_util.h"
 #include "mla_dcp.h"
 
 namespace {
@@ -34,23 +33,20 @@ constexpr size_t kScratchBytes =
 // the process exits (about 40 MiB).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per
-// device.  The host-side symbol is only a stand-in; kernels must be given the
-// address returned by cudaGetSymbolAddress.
-void* scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = ptr;
-  }
-  return g_scratch_ptr[dev];
+// Device address of the scratch in the current context.  The host-side
+// symbol is only a stand-in; kernels must be given the address that
+// cudaGetSymbolAddress returns, looked up once per CUDA context (a new
+// context after cudaDeviceReset, or a driver-API context, holds its own copy
+// of the module and so its own scratch).
+void* scratch_for_current_context() {
+  static mla::host::PerContext<void*> table;
+  void* ptr = nullptr;
+  if (!table.get(reinterpret_cast<const void*>(&g_noalloc_scratch), ptr, [](void*& v) {
+        v = nullptr;
+        return cudaGetSymbolAddress(&v, g_noalloc_scratch) == cudaSuccess && v != nullptr;
+      }))
+    return nullptr;
+  return ptr;
 }
 
 }  // namespace
@@ -76,7 +72,7 @@ extern "C" mla_status mla_decode_partial_noalloc(const void* q, const mla_kv_pag
   const size_t need = mla_workspace_size(shape, num_shards, shard_id);
   if (need == 0) return MLA_ERR_INVALID;
   if (need > kScratchBytes) return MLA_ERR_UNSUPPORTED;  // cannot happen within the limits
-  void* scratch = scratch_for_current_device();
+  void* scratch = scratch_for_current_context();
   if (scratch == nullptr) return MLA_ERR_CUDA;
   // Everything the kernels read from the scratch is written earlier in the
   // same call (the planning kernel resets the error word and rebuilds the
@@ -84,4 +80,13 @@ extern "C" mla_status mla_decode_partial_noalloc(const void* q, const mla_kv_pag
   return mla_decode_partial(q, kv, block_table, max_pages_per_req, seq_lens, shape, shard_id,
                             num_shards, layout, out_partial, lse_partial, scratch, kScratchBytes,
                             stream);
+}
+
+// The error word of the scratch (its first four bytes, as in every
+// workspace), read and cleared on `stream` exactly as mla_get_device_error
+// does for a caller's workspace.
+extern "C" mla_status mla_get_device_error_noalloc(void* stream) {
+  void* scratch = scratch_for_current_context();
+  if (scratch == nullptr) return MLA_ERR_CUDA;
+  return mla_get_device_error(scratch, stream);
 }

@@ -53,6 +53,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "host_util.h"
 #include "ptx.cuh"
 
 namespace mla {
@@ -75,6 +76,7 @@ struct Misc {
   // single barrier could complete two phases between tests and alias parities
   uint64_t p_full[2], pv_done[2];
   uint64_t q_full, q_empty, o_free;
+  uint64_t drain;                         // teardown after a failure: MMAs in flight
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
@@ -162,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, kIssuers);
     mbar_init(b_o_free, kSoftmaxWarps);
+    mbar_init(smem_u32(&misc->drain), kIssuers + kPvIssuers);
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
             if (!ok) break;
           }
-          if (lane == 0) {
+          if (lane == 0 && !(p.withhold_query && pc == 0)) {
             mbar_arrive_expect_tx(b_q_full, kTileBytes);
             armed_q = pc;
             const int row0 = x.b * pd.R + x.g * kRows;
@@ -587,16 +590,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    // after a failure, let this CTA's own TMA copies land before it exits
-    int never = 0;
-    for (int st = 0; st < 2; ++st)
-      for (int cg = 0; cg < kCg && armed_kv[st] >= 0; ++cg)
-        mbar_wait(b_kv_full + 8 * (kCg * st + cg), (armed_kv[st] >> 1) & 1, tmo, &never);
-    if (armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, tmo, &never);
-  }
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // After a failure, let this CTA's own MMAs and TMA copies complete before
+    // TMEM is freed and the CTA exits.  A commit tracks every earlier MMA of
+    // its thread, so one commit per issuing thread drains them all.
+    int never = 0;
+    if (lane == 0 && (warp == 1 || warp == 6 || (warp >= 7 && warp <= 10))) {
+      mma_commit(smem_u32(&misc->drain));
+      mbar_wait(smem_u32(&misc->drain), 0, kDrainNs, &never);
+    }
+    if (warp == 0 && lane == 0) {
+      for (int st = 0; st < 2; ++st)
+        for (int cg = 0; cg < kCg && armed_kv[st] >= 0; ++cg)
+          mbar_wait(b_kv_full + 8 * (kCg * st + cg), (armed_kv[st] >> 1) & 1, kDrainNs, &never);
+      if (armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, kDrainNs, &never);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -609,15 +622,9 @@ template <bool kLocal>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                   cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel<kLocal>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  const cudaError_t e =
+      host::ensure_dynamic_smem(reinterpret_cast<const void*>(&mla_partial_kernel<kLocal>), kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

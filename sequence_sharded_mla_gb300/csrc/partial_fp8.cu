@@ -43,6 +43,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "host_util.h"
 #include "ptx.cuh"
 
 namespace mla {
@@ -76,6 +77,7 @@ struct Misc {
   uint64_t kv_full[kStages], kv_empty[kStages], prep[kStages];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
   uint64_t q_full, q_conv, q_empty, o_free;
+  uint64_t drain;       // teardown after a failure: MMAs in flight
   uint32_t tmem_base;
   int abort;
   float alpha[2][kRows];
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_q_conv, kConvThreads / 32);
     mbar_init(b_q_empty, 1);
     mbar_init(b_o_free, kSoftmaxWarps);
+    mbar_init(smem_u32(&misc->drain), 2);     // the two MMA-issuing threads
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every splitter reaches these barriers once per piece, failure or not
       if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
       Unit x = make_unit<kLocal>(pd, unit);
-      if (ct == 0) {
+      if (ct == 0 && !(p.withhold_query && pc == 0)) {
         mbar_arrive_expect_tx(b_q_full, kQBytes);
         armed_q = pc;
         tma_load_4d(sQ, &tm_q, b_q_full, 0, 0, 0, (x.b * pd.R + x.g * kRows) >> 3);
@@ -758,19 +761,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp == 7 && lane == 0 && *abort_flag && armed_q >= 0) {
-    int never = 0;
-    mbar_wait(b_q_full, armed_q & 1, tmo, &never);
-  }
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    // after a failure, let this CTA's own copies land before it exits
-    int never = 0;
-    for (int st = 0; st < kStages; ++st)
-      if (armed_kv[st] >= 0)
-        mbar_wait(b_kv_full + 8 * st, (armed_kv[st] >> 2) & 1, tmo, &never);
-  }
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // After a failure, let this CTA's own MMAs and copies complete before
+    // TMEM is freed and the CTA exits (one commit drains every earlier MMA
+    // of the issuing thread).
+    int never = 0;
+    if (lane == 0 && (warp == 1 || warp == 6)) {
+      mma_commit(smem_u32(&misc->drain));
+      mbar_wait(smem_u32(&misc->drain), 0, kDrainNs, &never);
+    }
+    if (warp == 7 && lane == 0 && armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, kDrainNs, &never);
+    if (warp == 0 && lane == 0) {
+      for (int st = 0; st < kStages; ++st)
+        if (armed_kv[st] >= 0)
+          mbar_wait(b_kv_full + 8 * st, (armed_kv[st] >> 2) & 1, kDrainNs, &never);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -780,15 +790,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kLocal>
 static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                            const PartialParams& p, int grid, cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(mla_partial_fp8_kernel<kLocal>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  const cudaError_t e = host::ensure_dynamic_smem(
+      reinterpret_cast<const void*>(&mla_partial_fp8_kernel<kLocal>), kSmemBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

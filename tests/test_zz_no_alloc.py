@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 
 import mla_inputs as mi
+import oracle
 from _helpers import REL_OUT, TOL_LSE, TOL_OUT, check_close, to_device
 
 pytestmark = pytest.mark.gpu
@@ -87,3 +88,70 @@ def test_noalloc_second_call_after_other_entry_points():
     for o, l in ((out1, lse1), (out2, lse2)):
         check_close(o.cpu().numpy(), ref.cpu().numpy(), TOL_OUT, "out", rel=REL_OUT)
         check_close(l.cpu().numpy(), ref_lse.cpu().numpy(), TOL_LSE, "lse")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_noalloc_matches_the_oracle(kv_dtype):
+    """Every shard's partial from the scratch-backed call against the fp64
+    oracle, bf16 and fp8 caches, with split work units (long contexts)."""
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    dev = torch.device("cuda:0")
+    w = mi.build_workload("noalloc-oracle", 3, 1, 32, [4100, 70, 9000], 4, "interleaved",
+                          kv_dtype, False, seed=902, poison=True, extra_pages=2,
+                          kv_sigma=1.0 if kv_dtype == "fp8" else 0.5)
+    t = to_device(w, dev)
+    rows = w.batch * w.q_len * w.num_heads
+    for call in range(2):
+        out, lse = mla.mla_decode_partial_noalloc(t["q"], t["kv"], t["block_table"],
+                                                  t["seq_lens"], 4, "interleaved",
+                                                  kv_scale=t["kv_scale"])
+        assert mla.mla_get_device_error_noalloc() == 0
+        got = out.cpu().numpy().reshape(4, rows, 512)
+        got_lse = lse.cpu().numpy().reshape(4, rows)
+        for s in range(4):
+            ro, rl = oracle.attend(w, shard=s, num_shards=4, layout="interleaved")
+            check_close(got[s], ro, TOL_OUT, f"call {call} shard {s}", rel=REL_OUT)
+            check_close(got_lse[s], rl, TOL_LSE, f"call {call} lse shard {s}")
+
+
+def test_noalloc_local_shard_cache_matches_the_oracle():
+    """The per-GPU call of a multi-GPU deployment (one shard, a cache that
+    holds only that shard's positions, causal verify rows) on the scratch."""
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    dev = torch.device("cuda:0")
+    lens = [1, 300, 5000]
+    w = mi.build_workload("noalloc-local", len(lens), 2, 32, lens, 3, "interleaved", "bf16",
+                          True, seed=903, poison=True)
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    rows = w.batch * w.q_len * w.num_heads
+    for s in range(3):
+        d = mi.local_shard_cache(w, 3, s, "interleaved", seed=s)
+        kv = torch.from_numpy(d["kv"].view(np.int16)).view(torch.bfloat16).to(dev)
+        bt = torch.from_numpy(d["block_table"]).to(dev)
+        out, lse = mla.mla_decode_partial_noalloc(q, kv, bt, sl, 3, "interleaved_local",
+                                                  shard_id=s, causal=True)
+        assert mla.mla_get_device_error_noalloc() == 0
+        ro, rl = oracle.attend(w, shard=s, num_shards=3, layout="interleaved")
+        check_close(out.cpu().numpy().reshape(rows, 512), ro, TOL_OUT, f"local shard {s}",
+                    rel=REL_OUT)
+        check_close(lse.cpu().numpy().reshape(rows), rl, TOL_LSE, f"local lse {s}")
+
+
+def test_noalloc_reports_a_bad_block_table_page():
+    """A block-table entry outside the page pool is read as zeros and
+    reported through the scratch's error word; reading clears it."""
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    dev = torch.device("cuda:0")
+    w = mi.build_workload("noalloc-bad", 2, 1, 16, [200, 64], 2, "interleaved", "bf16", False,
+                          seed=904)
+    w.block_table[0, 2] = w.num_pages + 100
+    t = to_device(w, dev)
+    out, lse = mla.mla_decode_partial_noalloc(t["q"], t["kv"], t["block_table"], t["seq_lens"],
+                                              2, "interleaved")
+    assert mla.mla_get_device_error_noalloc() == -5          # MLA_ERR_DEVICE_BOUNDS
+    assert mla.mla_get_device_error_noalloc() == 0
+    assert np.all(np.isfinite(out.cpu().numpy()))
