@@ -169,9 +169,18 @@ def rank_workload_params(config, rank, requests=0):
     return p
 
 
+_WORKLOADS = {}
+
+
 def rank_workload(config, rank, requests=0, pinned=True):
+    """The rank's workload, generated once per process (the shard-count sweep
+    runs one cache at several shard counts and layouts)."""
     import mla_inputs as mi
-    return mi.build_workload(pinned=pinned, **rank_workload_params(config, rank, requests))
+    key = (config, rank, requests, pinned)
+    if key not in _WORKLOADS:
+        _WORKLOADS[key] = mi.build_workload(pinned=pinned,
+                                            **rank_workload_params(config, rank, requests))
+    return _WORKLOADS[key]
 
 
 def reduce_over_ranks(dist, times, kv_bytes, device):
@@ -186,10 +195,12 @@ def reduce_over_ranks(dist, times, kv_bytes, device):
     return t.tolist(), b.item()
 
 
-def cpu_sample(w, budget_s, oracle):
+def cpu_sample(w, budget_s, oracle, threads=0):
     """Oracle on whole requests (all heads, unsharded, W_UV if present) until
-    about ``budget_s`` of CPU time; returns (KV bytes covered, seconds, desc)."""
+    about ``budget_s`` of CPU time; returns (KV bytes covered, seconds, desc).
+    ``threads`` > 0 runs the oracle on that many host threads."""
     import numpy as np
+    oracle.set_threads(threads)
     order = np.argsort(w.seq_lens)            # short to long, one of each band first
     picked, t_used, kv_bytes = [], 0.0, 0
     per = 1152 if w.kv_dtype == "bf16" else 580
@@ -210,10 +221,11 @@ def cpu_sample(w, budget_s, oracle):
     return kv_bytes, t_used, desc
 
 
-def gqa_cpu_sample(w, budget_s, oracle):
+def gqa_cpu_sample(w, budget_s, oracle, threads=0):
     """The GQA oracle on whole requests (all heads, unsharded) until about
     ``budget_s`` of CPU time; returns (K/V bytes covered, seconds, desc)."""
     import numpy as np
+    oracle.set_threads(threads)
     order = np.argsort(w.seq_lens)
     picked, t_used, kv_bytes = [], 0.0, 0
     per = 2 * w.num_kv_heads * w.head_dim * 2
@@ -277,7 +289,7 @@ class Case:
 
     def __init__(self, name, kv_bytes, config, pairs, outputs, workspace, step, dtype, kernel,
                  kernel_src, cpu, flops=0.0, combine_bytes=0.0, tensor_bound=False,
-                 tensor_fp8=False):
+                 tensor_fp8=False, launches_per_step=4, fused_step=False):
         self.name, self.kv_bytes, self.config = name, kv_bytes, config
         self.pairs = pairs            # [(pinned host tensor, device tensor)] copied per e2e step
         self.outputs = outputs        # [(device tensor, pinned host tensor)] read per e2e step
@@ -288,6 +300,10 @@ class Case:
         self.combine_bytes = combine_bytes   # bytes the combine kernel reads and writes
         self.tensor_bound = tensor_bound     # the dense contractions bound the partial kernel
         self.tensor_fp8 = tensor_fp8         # the contractions run on e4m3 operands
+        self.launches_per_step = launches_per_step
+        # fused_step: the step is one mla_decode_step call (plan, partial,
+        # combine); the combine is timed from the end of the partial kernel
+        self.fused_step = fused_step
 
 
 def visible_pairs(seq_lens, q_len, causal):
@@ -311,45 +327,50 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
     import mla_inputs as mi
     import sequence_sharded_mla_gb300 as mla
     w = rank_workload(args.config, rank, args.requests)
-    B, H, q_len, N = w.batch, w.num_heads, w.q_len, w.num_shards
-    q = _pinned_pair(torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16), dev)
-    if w.kv_dtype == "bf16":
-        kv = _pinned_pair(torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16), dev)
-        sc = None
-    else:
-        kv = _pinned_pair(torch.from_numpy(w.kv), dev)
-        sc = _pinned_pair(torch.from_numpy(w.kv_scale), dev)
-    bt = _pinned_pair(torch.from_numpy(w.block_table), dev)
-    sl = _pinned_pair(torch.from_numpy(w.seq_lens), dev)
+    B, H, q_len = w.batch, w.num_heads, w.q_len
+    N = args.num_shards or w.num_shards
+    layout = args.layout or w.layout
+    key = ("device", args.config, rank, args.requests)
+    if key not in _WORKLOADS:
+        q = _pinned_pair(torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16), dev)
+        if w.kv_dtype == "bf16":
+            kv = _pinned_pair(torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16), dev)
+            sc = None
+        else:
+            kv = _pinned_pair(torch.from_numpy(w.kv), dev)
+            sc = _pinned_pair(torch.from_numpy(w.kv_scale), dev)
+        bt = _pinned_pair(torch.from_numpy(w.block_table), dev)
+        sl = _pinned_pair(torch.from_numpy(w.seq_lens), dev)
+        _WORKLOADS[key] = (q, kv, sc, bt, sl)
+    q, kv, sc, bt, sl = _WORKLOADS[key]
     d_wuv = None
     if w.w_uv is not None:
         d_wuv = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16).to(dev)
-    part = torch.empty((N, B, q_len, H, 512), dtype=torch.float32, device=dev)
-    lsep = torch.empty((N, B, q_len, H), dtype=torch.float32, device=dev)
     out = torch.empty((B, q_len, H, 512 if d_wuv is None else 128), dtype=torch.bfloat16,
                       device=dev)
     lse = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
-    ws = torch.empty((mla.mla_workspace_size(B, q_len, H, N),), dtype=torch.uint8, device=dev)
+    ws = torch.empty((mla.mla_decode_step_workspace_size(B, q_len, H, N),), dtype=torch.uint8,
+                     device=dev)
 
     def step(i=None):
+        # one call: plan, partial kernel (events around it recorded by the
+        # library), then the combine that also merges split pieces
         if i is not None:
             ev_p[2 * i].record(stream)
             mla.mla_set_profile_events(ev_k[2 * i], ev_k[2 * i + 1])
-        mla.mla_decode_partial(q[1], kv[1], bt[1], sl[1], N, w.layout,
-                               kv_scale=None if sc is None else sc[1], causal=w.causal,
-                               out_partial=part, lse_partial=lsep, workspace=ws, stream=stream)
+        mla.mla_decode_step(q[1], kv[1], bt[1], sl[1], N, layout,
+                            kv_scale=None if sc is None else sc[1], causal=w.causal,
+                            w_uv=d_wuv, out=out, lse_out=lse, workspace=ws, stream=stream)
         if i is not None:
             mla.mla_set_profile_events(None, None)
-            ev_p[2 * i + 1].record(stream)
-        mla.mla_shard_combine(part, lsep, w_uv=d_wuv, out=out, lse_out=lse, stream=stream)
-        if i is not None:
             ev_c[i].record(stream)
 
     pairs = [q, kv, bt, sl] + ([sc] if sc is not None else [])
     outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
                (lse, torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))]
-    config = {"workload": mi.CONFIG_NAMES[args.config], "batch": B, "heads": H, "q_len": q_len,
-              "num_shards": N, "layout": w.layout, "kv_dtype": w.kv_dtype,
+    name = w.name + (f"-n{N}-{layout}" if args.config == 3 else "")
+    config = {"workload": name, "batch": B, "heads": H, "q_len": q_len,
+              "num_shards": N, "layout": layout, "kv_dtype": w.kv_dtype,
               "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
               "total_tokens_per_gpu": w.total_tokens}
     fp8 = w.kv_dtype == "fp8"
@@ -361,8 +382,9 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
         comb += d_wuv.numel() * 2
     return Case(config["workload"], w.kv_bytes(), config, pairs, outputs, ws, step,
                 "e4m3" if fp8 else "bf16", kernel, "partial_fp8.cu" if fp8 else "partial.cu",
-                lambda budget, orc: cpu_sample(w, budget, orc), flops=flops,
-                combine_bytes=comb, tensor_bound=q_len * H > 64, tensor_fp8=fp8)
+                lambda budget, orc, threads=0: cpu_sample(w, budget, orc, threads), flops=flops,
+                combine_bytes=comb, tensor_bound=q_len * H > 64, tensor_fp8=fp8,
+                launches_per_step=3, fused_step=True)
 
 
 def gqa_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
@@ -411,9 +433,141 @@ def gqa_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
     rows = B * q_len * H
     return Case(mi.GQA_CONFIG_NAME, w.kv_bytes(), config, [q, k, v, bt, sl], outputs, ws, step,
                 "bf16", "gqa_partial_kernel", "gqa.cu",
-                lambda budget, orc: gqa_cpu_sample(w, budget, orc),
+                lambda budget, orc, threads=0: gqa_cpu_sample(w, budget, orc, threads),
                 flops=2.0 * H * (D + D) * visible_pairs(w.seq_lens, q_len, w.causal),
                 combine_bytes=N * rows * (D * 4 + 4) + rows * (D * 2 + 4))
+
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(case, args):
+    """The oracle as it stands on a bounded sample of the workload: all host
+    cores, then one core (a smaller sample)."""
+    import oracle
+    kvb, dt, desc = case.cpu(args.cpu_seconds, oracle)
+    cores = oracle.num_threads()
+    kvb1, dt1, desc1 = case.cpu(args.cpu_seconds / 3.0, oracle, 1)
+    oracle.set_threads(0)
+    return {"value": kvb / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": desc, "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "one_core": {"value": kvb1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                         "sample": desc1}}
+
+
+def time_case(case, args, dev, stream, ev_p, ev_k, ev_c, barrier, flush):
+    """Warm-up, then args.steps timed steps.  Returns per-step times (ms) of
+    the whole step, the partial kernel alone, the calls before it and the
+    combine, and the clock record.
+
+    Inputs larger than L2 (flush is None): the timed steps run back to back
+    with one event before and one after them, nothing in between (an event
+    between two kernels keeps the second from launching early), and a second,
+    untimed pass of as many steps records the events inside every step for
+    the per-kernel breakdown.  Otherwise each step is timed between its own
+    events, with L2 flushed before it."""
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    for _ in range(args.warmup):
+        case.step()
+    assert mla.mla_get_device_error(case.workspace, stream) == 0
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    if flush is None:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            case.step()
+        t1.record(stream)
+        barrier()
+        total_ms = t0.elapsed_time(t1)
+        for i in range(args.steps):
+            case.step(i)
+    else:
+        for i in range(args.steps):
+            flush.zero_()          # evict the previous step's data from L2 (not timed)
+            case.step(i)
+    barrier()
+    clk = clocks.stop()
+    status = mla.mla_get_device_error(case.workspace, stream)
+    if status != 0:
+        raise RuntimeError(f"device error status {status}")
+    if flush is None:
+        step_ms = [total_ms / args.steps] * args.steps
+    else:
+        step_ms = [ev_p[2 * i].elapsed_time(ev_c[i]) for i in range(args.steps)]
+    kernel_ms = [ev_k[2 * i].elapsed_time(ev_k[2 * i + 1]) for i in range(args.steps)]
+    if case.fused_step:
+        before_ms = [ev_p[2 * i].elapsed_time(ev_k[2 * i + 1]) for i in range(args.steps)]
+        combine_ms = [ev_k[2 * i + 1].elapsed_time(ev_c[i]) for i in range(args.steps)]
+    else:
+        before_ms = [ev_p[2 * i].elapsed_time(ev_p[2 * i + 1]) for i in range(args.steps)]
+        combine_ms = [ev_p[2 * i + 1].elapsed_time(ev_c[i]) for i in range(args.steps)]
+    case.profiled_step_ms = statistics.mean(
+        ev_p[2 * i].elapsed_time(ev_c[i]) for i in range(args.steps))
+    return step_ms, kernel_ms, before_ms, combine_ms, clk
+
+
+def make_events(n):
+    import torch
+    return ([torch.cuda.Event(enable_timing=True) for _ in range(2 * n)],
+            [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)],
+            [torch.cuda.Event(enable_timing=True) for _ in range(n)])
+
+
+def run_sweep(args, dev, stream, barrier):
+    """Config 3's shard-count sweep: one seeded cache at N = 1, 2, 4, 8 in
+    both layouts; the partial kernel's and the combine's bandwidth per run."""
+    import torch
+    peak, peak_kind = load_peaks()
+    rows = []
+    for layout in ("interleaved", "contiguous"):
+        for N in (1, 2, 4, 8):
+            args.num_shards, args.layout = N, layout
+            ev_p, ev_k, ev_c = make_events(args.steps)
+            for ev in ev_p + ev_k + ev_c:
+                ev.record(stream)
+            case = mla_case(args, 0, dev, stream, ev_p, ev_k, ev_c)
+            step_ms, kernel_ms, _, combine_ms, clk = time_case(case, args, dev, stream, ev_p,
+                                                               ev_k, ev_c, barrier, None)
+            km, cm, sm = (statistics.mean(kernel_ms), statistics.mean(combine_ms),
+                          statistics.mean(step_ms))
+            rows.append({"num_shards": N, "layout": layout,
+                         "partial_kernel_ms": km,
+                         "partial_kernel_gbps": case.kv_bytes / km / 1e6,
+                         "partial_frac_of_peak": case.kv_bytes / km / 1e6 / peak,
+                         "combine_ms": cm,
+                         "combine_gbps": case.combine_bytes / cm / 1e6,
+                         "combine_bytes": case.combine_bytes,
+                         "step_ms": sm, "step_gbps": case.kv_bytes / sm / 1e6,
+                         "sm_mhz": clk["sm_mhz"], "reasons": clk["reasons"]})
+            del case
+            torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "shard-count-sweep", "peak_gbs": peak,
+                      "peak_source": f"{peak_kind} hbm_gbs", "steps": args.steps,
+                      "warmup": args.warmup, "runs": rows}), flush=True)
 
 
 def run_gpu(args, world, rank, local, dist):
@@ -425,48 +579,35 @@ def run_gpu(args, world, rank, local, dist):
     dev = torch.device("cuda", local)
     mla.lib()
     stream = torch.cuda.current_stream(dev)
-    # per timed step: events around the whole partial call (plan, partial
-    # kernel, merge) and, recorded by the library itself, around the partial
-    # kernel alone
-    ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    ev_k = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    ev_c = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for ev in ev_p + ev_k + ev_c:
-        ev.record(stream)
-    # each rank decodes its own batch of the same shape (independent requests)
-    make = gqa_case if args.config == GQA_CONFIG else mla_case
-    case = make(args, rank, dev, stream, ev_p, ev_k, ev_c)
-    kv_bytes = case.kv_bytes
-    ws = case.workspace
-    step = case.step
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        step()
-    assert mla.mla_get_device_error(ws, stream) == 0
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    t_end.record(stream)
-    barrier()
-    clk = clocks.stop()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    partial_ms = [ev_p[2 * i].elapsed_time(ev_p[2 * i + 1]) for i in range(args.steps)]
-    kernel_ms = [ev_k[2 * i].elapsed_time(ev_k[2 * i + 1]) for i in range(args.steps)]
-    combine_ms = [ev_p[2 * i + 1].elapsed_time(ev_c[i]) for i in range(args.steps)]
-    status = mla.mla_get_device_error(ws, stream)
-    if status != 0:
-        raise RuntimeError(f"device error status {status}")
+    if args.sweep:
+        if args.config != 3 or world != 1:
+            raise SystemExit("--sweep is the shard-count sweep of --config 3 on one GPU")
+        run_sweep(args, dev, stream, barrier)
+        return
+    # per timed step: events at its start, around the partial kernel
+    # (recorded by the library itself) and at its end
+    ev_p, ev_k, ev_c = make_events(args.steps)
+    for ev in ev_p + ev_k + ev_c:
+        ev.record(stream)
+    # each rank decodes its own batch of the same shape (independent requests)
+    make = gqa_case if args.config == GQA_CONFIG else mla_case
+    case = make(args, rank, dev, stream, ev_p, ev_k, ev_c)
+    kv_bytes = case.kv_bytes
+    step = case.step
+    # inputs not well above L2 (the tiny batch, the q_len-9 batch's 148 MB)
+    # are evicted by writing a buffer twice L2's size before every timed step
+    flush = None
+    if kv_bytes < 4 * L2_BYTES:
+        flush = torch.empty((2 * L2_BYTES // 4,), dtype=torch.float32, device=dev)
+    step_ms, kernel_ms, before_ms, combine_ms, clk = time_case(case, args, dev, stream, ev_p,
+                                                               ev_k, ev_c, barrier, flush)
+    elapsed = sum(step_ms) / 1e3
 
     # end to end through host buffers: copy the step's inputs in, read results out
     h2d = sum(h.numel() * h.element_size() for h, _ in case.pairs)
@@ -491,8 +632,8 @@ def run_gpu(args, world, rank, local, dist):
     barrier()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
 
-    (elapsed, e2e_per_step, partial_avg_ms, kernel_avg_ms, combine_avg_ms), total_kv = \
-        reduce_over_ranks(dist, [elapsed, e2e_elapsed / e2e_steps, statistics.mean(partial_ms),
+    (elapsed, e2e_per_step, before_avg_ms, kernel_avg_ms, combine_avg_ms), total_kv = \
+        reduce_over_ranks(dist, [elapsed, e2e_elapsed / e2e_steps, statistics.mean(before_ms),
                                  statistics.mean(kernel_ms), statistics.mean(combine_ms)],
                           kv_bytes, dev)
     if rank != 0:
@@ -521,12 +662,16 @@ def run_gpu(args, world, rank, local, dist):
     tensor_roof = {"kernel": case.kernel, "bound": "tensor", "achieved": tflops, "peak": tpeak,
                    "unit": "TFLOP/s", "frac": tflops / tpeak, "peak_source": tsrc,
                    "traffic": traffic}
+    if flush is not None:
+        l2 = (f"L2 flushed before every timed step (a {2 * L2_BYTES >> 20} MiB buffer written, "
+              f"outside the timed interval); {kv_bytes / 1e6:.1f} MB of KV per GPU")
+    else:
+        l2 = f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per GPU vs 129 MB)"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": case.dtype, "data": "synthetic",
-        "config": dict(case.config, kv_bytes_per_gpu=kv_bytes,
-                       l2=f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per GPU vs 129 MB)",
+        "config": dict(case.config, kv_bytes_per_gpu=kv_bytes, l2=l2,
                        parallelism=f"{world} GPU(s), independent batches; "
                                    f"{case.config['num_shards']} logical shards each"),
         "steps_per_s": args.steps / elapsed,
@@ -537,18 +682,16 @@ def run_gpu(args, world, rank, local, dist):
                     "gbps": case.combine_bytes / (combine_avg_ms / 1e3) / 1e9,
                     "bytes_per_step": case.combine_bytes},
         "partial_kernel_ms": kernel_avg_ms,
-        "partial_call_ms": partial_avg_ms,
+        "partial_call_ms": before_avg_ms,
+        "profiled_step_ms": case.profiled_step_ms,   # a step with events between its kernels
         "e2e": {"value": total_kv / e2e_per_step / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,   # plan, partial, merge, combine
+        "gpu_launches": case.launches_per_step * args.steps,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
-        import oracle
-        kvb, dt, desc = case.cpu(args.cpu_seconds, oracle)
-        line["cpu_baseline"] = {"value": kvb / dt / 1e9, "unit": "GB/s",
-                                "cores": oracle.num_threads(), "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = cpu_baseline(case, args)
     print(json.dumps(line), flush=True)
 
 
@@ -567,6 +710,13 @@ def main():
                          "or 6: the grouped-query batch")
     ap.add_argument("--requests", type=int, default=0,
                     help="profiling only: keep the first K requests of the workload")
+    ap.add_argument("--num-shards", type=int, default=0,
+                    help="override the configuration's logical shard count (1..8)")
+    ap.add_argument("--layout", default="", choices=["", "interleaved", "contiguous"],
+                    help="override the configuration's shard layout")
+    ap.add_argument("--sweep", action="store_true",
+                    help="with --config 3: the shard-count sweep, N = 1, 2, 4, 8 in both "
+                         "layouts over one seeded cache (one JSON line with a table)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

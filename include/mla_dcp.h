@@ -220,6 +220,32 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
                              void* stream);
 
 /*
+ * One whole decode step on one GPU: every shard's partial attention
+ * (mla_decode_partial with MLA_ALL_SHARDS) and their LSE combine
+ * (mla_shard_combine, optionally fused with W_UV) in one call, with the shard
+ * partials kept in the workspace instead of caller buffers.  The N shards are
+ * logical partitions of the cache ("Decode Context Parallelism", section 4.1:
+ * Compute, then the LSE reweighting of the partials into the true output).
+ * A shard's unit that the work split divides between several CTAs leaves one
+ * partial per CTA; these pieces are merged together with the other shards'
+ * partials in the combine itself (the LSE merge is associative), so no merged
+ * per-shard partial is written.
+ *
+ * Arguments as for mla_decode_partial and mla_shard_combine; layout must be
+ * MLA_LAYOUT_INTERLEAVED or MLA_LAYOUT_CONTIGUOUS.  out: bf16
+ * [B, q_len, H, 512], or [B, q_len, H, 128] with w_uv; lse_out: fp32
+ * [B, q_len, H] or NULL.  workspace_bytes must be at least
+ * mla_decode_step_workspace_size(shape, num_shards).  Device-side errors are
+ * read with mla_get_device_error(workspace, stream).
+ */
+size_t mla_decode_step_workspace_size(const mla_shape* shape, int num_shards);
+mla_status mla_decode_step(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                           int max_pages_per_req, const int32_t* seq_lens, const mla_shape* shape,
+                           int num_shards, mla_layout layout, const void* w_uv, void* out,
+                           float* lse_out, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * Synchronises `stream`, reads and clears the device error word kept in
  * `workspace` by the last mla_decode_partial on it.  Returns MLA_OK,
  * MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_RANGE or MLA_ERR_INVALID (a

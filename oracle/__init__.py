@@ -42,6 +42,8 @@ def lib():
         L.oracle_token_owner.restype = i32
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = i32
+        L.oracle_set_threads.argtypes = [i32]
+        L.oracle_set_threads.restype = None
         _LIB = L
     return _LIB
 
@@ -163,6 +165,11 @@ def token_owner(t, L, num_shards, layout):
 
 def num_threads():
     return int(lib().oracle_num_threads())
+
+
+def set_threads(n=0):
+    """Host threads of later oracle calls: n > 0 that many, 0 the default."""
+    lib().oracle_set_threads(int(n))
 
 
 def reference_step(w, rows=None):

@@ -365,3 +365,17 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads for later calls: n > 0 sets n, n == 0 restores the count the
+ * process started with (CPU timings at 1 core and at all cores). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  extern int omp_get_max_threads(void);
+  extern void omp_set_num_threads(int);
+  static int initial = 0;
+  if (initial == 0) initial = omp_get_max_threads();
+  omp_set_num_threads(n > 0 ? n : initial);
+#else
+  (void)n;
+#endif
+}

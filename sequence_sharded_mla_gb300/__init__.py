@@ -57,6 +57,7 @@ class gqa_kv_pages(ctypes.Structure):
 
 _LIB = None
 EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
+           "mla_decode_step", "mla_decode_step_workspace_size",
            "mla_workspace_size", "mla_get_device_error", "mla_get_device_error_noalloc",
            "mla_set_wait_budget_ns", "mla_set_withhold_query", "mla_set_profile_events",
            "mla_status_string",
@@ -80,6 +81,12 @@ def lib():
         L.mla_decode_partial_noalloc.restype = i32
         L.mla_shard_combine.argtypes = [vp, vp, i32, ctypes.POINTER(mla_shape), vp, vp, vp, vp]
         L.mla_shard_combine.restype = i32
+        L.mla_decode_step.argtypes = [vp, ctypes.POINTER(mla_kv_pages), vp, i32, vp,
+                                      ctypes.POINTER(mla_shape), i32, i32, vp, vp, vp, vp, sz,
+                                      vp]
+        L.mla_decode_step.restype = i32
+        L.mla_decode_step_workspace_size.argtypes = [ctypes.POINTER(mla_shape), i32]
+        L.mla_decode_step_workspace_size.restype = sz
         L.mla_workspace_size.argtypes = [ctypes.POINTER(mla_shape), i32, i32]
         L.mla_workspace_size.restype = sz
         L.mla_get_device_error.argtypes = [vp, vp]
@@ -198,6 +205,66 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
     if st != 0:
         raise MLAError(st, "mla_decode_partial")
     return out_partial, lse_partial, workspace
+
+
+def mla_decode_step_workspace_size(batch, q_len, num_heads, num_shards) -> int:
+    sh = _shape(batch, q_len, num_heads, False, DEFAULT_SCALE)
+    return int(lib().mla_decode_step_workspace_size(ctypes.byref(sh), int(num_shards)))
+
+
+def mla_decode_step(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
+                    kv_scale=None, causal=False, softmax_scale=DEFAULT_SCALE, w_uv=None,
+                    out=None, lse_out=None, workspace=None, stream=None, q_lens=None):
+    """One whole decode step on one GPU: all shards' partials and their LSE
+    combine (optionally fused with W_UV); returns (out, lse_out, workspace).
+
+    Inputs as for mla_decode_partial; w_uv: bf16 [H, 512, 128] or None.
+    out: bf16 [B, q_len, H, 512] (or [.., 128] with w_uv); lse_out: fp32 [B, q_len, H].
+    """
+    _check(q, "q", (torch.bfloat16,), 4)
+    dev = q.device
+    B, q_len, H, d = q.shape
+    if d != D_QK:
+        raise ValueError("q must be [B, q_len, H, 576]")
+    if kv.dtype == torch.bfloat16:
+        kv_dtype = KV_BF16
+        if kv_scale is not None:
+            raise ValueError("kv_scale is only for fp8 caches")
+    elif kv.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        kv_dtype = KV_FP8
+        if kv_scale is None:
+            raise ValueError("fp8 caches need kv_scale")
+        _check(kv_scale, "kv_scale", (torch.float32,), 2, dev)
+    else:
+        raise TypeError(f"kv dtype {kv.dtype} unsupported")
+    _check(kv, "kv", (kv.dtype,), 3, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
+    if w_uv is not None:
+        _check(w_uv, "w_uv", (torch.bfloat16,), 3, dev)
+    if q_lens is not None:
+        _check(q_lens, "q_lens", (torch.int32,), 1, dev)
+    width = D_UV if w_uv is not None else D_V
+    if out is None:
+        out = torch.empty((B, q_len, H, width), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, q_len, H), dtype=torch.float32, device=dev)
+    _check(out, "out", (torch.bfloat16,), 4, dev)
+    _check(lse_out, "lse_out", (torch.float32,), 3, dev)
+    sh = _shape(B, q_len, H, causal, softmax_scale, q_lens)
+    need = int(lib().mla_decode_step_workspace_size(ctypes.byref(sh), int(num_shards)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
+                         kv_dtype, kv.shape[0], kv.shape[1])
+    st = lib().mla_decode_step(_ptr(q), ctypes.byref(pages), _ptr(block_table),
+                               block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
+                               int(num_shards), LAYOUTS[layout], _ptr(w_uv), _ptr(out),
+                               _ptr(lse_out), _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "mla_decode_step")
+    return out, lse_out, workspace
 
 
 def mla_decode_partial_noalloc(q, kv, block_table, seq_lens, num_shards, layout="interleaved",

@@ -30,6 +30,10 @@ cudaError_t launch_combine(const float* partials, const float* lses, int num_sha
 cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
                                int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
                                float* lse_out, cudaStream_t stream);
+cudaError_t launch_step_combine(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
+                                const float* ws_o, const float* ws_lse, const float* part,
+                                const float* part_lse, const uint16_t* w_uv, uint16_t* out,
+                                float* lse_out, cudaStream_t stream);
 }  // namespace mla
 
 using namespace mla;
@@ -112,11 +116,30 @@ size_t mla_workspace_size(const mla_shape* shape, int num_shards, int shard_id) 
   return ws_layout(units_for(shape, num_shards, shard_id), grid).total;
 }
 
-mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
-                              int max_pages_per_req, const int32_t* seq_lens,
-                              const mla_shape* shape, int shard_id, int num_shards,
-                              mla_layout layout, float* out_partial, float* lse_partial,
-                              void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// What a partial-attention launch leaves for the kernel that completes it
+// (the merge of split pieces, or the combine of a whole decode step).
+struct Launched {
+  ProblemDesc pd;
+  WsHeader* hdr;
+  int* prefix;
+  float* ws_o;
+  float* ws_lse;
+  int num_units;
+};
+
+// Checks the arguments, encodes the tensor maps and launches the planning
+// and partial-attention kernels.  Units that one CTA computes whole are
+// written to out_partial / lse_partial; pieces of split units to the
+// workspace slots described by *L.
+mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                          int max_pages_per_req, const int32_t* seq_lens, const mla_shape* shape,
+                          int shard_id, int num_shards, mla_layout layout, float* out_partial,
+                          float* lse_partial, void* workspace, size_t workspace_bytes,
+                          void* stream, Launched* L) {
   if (!q || !kv || !block_table || !seq_lens || !out_partial || !lse_partial) return MLA_ERR_INVALID;
   if (!shape_ok(shape)) return MLA_ERR_INVALID;
   if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
@@ -281,8 +304,83 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (ev1 != nullptr && cudaEventRecord(static_cast<cudaEvent_t>(ev1), st) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (le != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_merge(pd, p.hdr, p.prefix, p.ws_o, p.ws_lse, out_partial, lse_partial, U, st) !=
-      cudaSuccess)
+  L->pd = pd;
+  L->hdr = p.hdr;
+  L->prefix = p.prefix;
+  L->ws_o = p.ws_o;
+  L->ws_lse = p.ws_lse;
+  L->num_units = U;
+  return MLA_OK;
+}
+
+// Workspace of a whole decode step: the partial-attention workspace, then
+// the shard partials [N, B, R, 512] and their LSEs [N, B, R].
+struct StepLayout {
+  size_t partial_ws, part, part_lse, total;
+};
+
+StepLayout step_layout(const mla_shape* shape, int num_shards) {
+  auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  StepLayout s;
+  s.partial_ws = up(mla_workspace_size(shape, num_shards, MLA_ALL_SHARDS));
+  const size_t rows = (size_t)num_shards * shape->batch * shape->q_len * shape->num_heads;
+  s.part = s.partial_ws;
+  s.part_lse = s.part + up(rows * kDv * sizeof(float));
+  s.total = s.part_lse + up(rows * sizeof(float));
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                              int max_pages_per_req, const int32_t* seq_lens,
+                              const mla_shape* shape, int shard_id, int num_shards,
+                              mla_layout layout, float* out_partial, float* lse_partial,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  Launched L;
+  const mla_status st = partial_launch(q, kv, block_table, max_pages_per_req, seq_lens, shape,
+                                       shard_id, num_shards, layout, out_partial, lse_partial,
+                                       workspace, workspace_bytes, stream, &L);
+  if (st != MLA_OK) return st;
+  if (launch_merge(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, out_partial, lse_partial,
+                   L.num_units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+size_t mla_decode_step_workspace_size(const mla_shape* shape, int num_shards) {
+  if (mla_workspace_size(shape, num_shards, MLA_ALL_SHARDS) == 0) return 0;
+  return step_layout(shape, num_shards).total;
+}
+
+mla_status mla_decode_step(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
+                           int max_pages_per_req, const int32_t* seq_lens, const mla_shape* shape,
+                           int num_shards, mla_layout layout, const void* w_uv, void* out,
+                           float* lse_out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (out == nullptr || !aligned16(out) || (w_uv != nullptr && !aligned16(w_uv)) ||
+      (lse_out != nullptr && !aligned4(lse_out)))
+    return MLA_ERR_INVALID;
+  if (!shape_ok(shape) || num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
+  if (layout != MLA_LAYOUT_INTERLEAVED && layout != MLA_LAYOUT_CONTIGUOUS) return MLA_ERR_INVALID;
+  if (workspace == nullptr || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
+  const size_t need_partial = mla_workspace_size(shape, num_shards, MLA_ALL_SHARDS);
+  if (need_partial == 0) return MLA_ERR_INVALID;
+  const StepLayout sl = step_layout(shape, num_shards);
+  if (workspace_bytes < sl.total) return MLA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* part = reinterpret_cast<float*>(ws + sl.part);
+  float* part_lse = reinterpret_cast<float*>(ws + sl.part_lse);
+  Launched L;
+  const mla_status st = partial_launch(q, kv, block_table, max_pages_per_req, seq_lens, shape,
+                                       MLA_ALL_SHARDS, num_shards, layout, part, part_lse,
+                                       workspace, sl.partial_ws, stream, &L);
+  if (st != MLA_OK) return st;
+  if (launch_step_combine(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, part, part_lse,
+                          static_cast<const uint16_t*>(w_uv), static_cast<uint16_t*>(out),
+                          lse_out, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

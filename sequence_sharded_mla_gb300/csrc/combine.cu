@@ -5,14 +5,25 @@
 // DSL Decode on NVIDIA GB300", section 1: a fused kernel combines the partial
 // results with v-proj).
 //
-//   M = max_s lse_s,  w_s = exp(lse_s - M),  lse = M + ln sum_s w_s
-//   out = sum_s w_s o_s / sum_s w_s                      -> bf16 [rows, 512]
+//   M = max_k lse_k,  w_k = exp(lse_k - M),  lse = M + ln sum_k w_k
+//   out = sum_k w_k o_k / sum_k w_k                      -> bf16 [rows, 512]
 //   y   = out . W_UV[h]   (fp32 out, bf16 weights)       -> bf16 [rows, 128]
+//
+// The k run over the "pieces" of a row: its N shard partials
+// (mla_shard_combine), or, inside a whole decode step, every piece of every
+// shard -- a shard's unit computed by one CTA is one piece, a unit split
+// across CTAs contributes each CTA's piece.  The merge is associative, so
+// merging all pieces of all shards at once equals merging the pieces of each
+// shard first and the shards afterwards; no merged per-shard partial is ever
+// written back.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace mla {
 
@@ -23,189 +34,368 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-}  // namespace
-
-// Merges one row of the N shard partials by their LSEs into acc (unscaled)
-// and returns M = max lse and wsum = sum of exp(lse - M).  Each lane owns 16
-// of the 512 dims (four float4 at dims 4*lane + 128*k).  The rows of up to
-// four shards and all the LSEs are loaded together, before the weights are
-// known, so their latencies overlap; the sum runs over s = 0..N-1 in order.
-__device__ __forceinline__ void merge_row(const float* __restrict__ partials,
-                                          const float* __restrict__ lses, int num_shards,
-                                          int rows, int row, int lane, float4 (&acc)[4], float& M,
-                                          float& wsum) {
-  float4 ob[4][4];
-  auto load4 = [&](int s0) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (s0 + j < num_shards) {
-        const float4* src =
-            reinterpret_cast<const float4*>(partials + ((size_t)(s0 + j) * rows + row) * kDv);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ob[j][k] = __ldg(src + lane + 32 * k);
-      }
+// Pieces of a row when the N shard partials are stacked shard-major:
+// partials [N, rows, 512], lses [N, rows].
+struct StackedRows {
+  const float* partials;
+  const float* lses;
+  int num_shards, rows;
+  struct Ctx {
+    int row, count;
   };
-  load4(0);
-  float l[kMaxShards];
-  M = -CUDART_INF_F;
-#pragma unroll
-  for (int s = 0; s < kMaxShards; ++s) {
-    l[s] = s < num_shards ? __ldg(lses + (size_t)s * rows + row) : -CUDART_INF_F;
-    M = fmaxf(M, l[s]);
+  __device__ Ctx prepare(int row, int /*lane*/) const { return Ctx{row, num_shards}; }
+  // Called by every lane of the warp (k may differ per lane, 0 <= k < count).
+  __device__ void piece(const Ctx& c, int k, const float*& src, float& lse) const {
+    const size_t i = (size_t)k * rows + c.row;
+    src = partials + i * kDv;
+    lse = __ldg(lses + i);
   }
+};
+
+// Pieces of a row of a whole decode step (every shard computed by one
+// launch): unit u = (b N + s) G + g of shard s is empty (no piece), written
+// whole by one CTA to the step's partial buffer [N, B, R, 512] (one piece),
+// or split across CTAs c0..c1 whose pieces are in the workspace slots.
+struct StepRows {
+  ProblemDesc pd;
+  const WsHeader* hdr;
+  const int* prefix;
+  const float* ws_o;
+  const float* ws_lse;
+  const float* part;      // [N, B, R, 512]: units written whole
+  const float* part_lse;  // [N, B, R]
+  struct Ctx {
+    int b, rr, r;            // request, row within the request, row within its group
+    int count;               // pieces over all shards (warp-uniform)
+    int excl, c0, ps, whole; // lane s < N: shard s's first piece index, first CTA,
+                             // first work position, whether it is one whole piece
+  };
+  __device__ Ctx prepare(int row, int lane) const {
+    Ctx c;
+    c.b = row / pd.R;
+    c.rr = row - c.b * pd.R;
+    const int g = c.rr / kRows;
+    c.r = c.rr - g * kRows;
+    const int per = hdr->per_cta;
+    int np = 0;
+    c.c0 = 0;
+    c.ps = 0;
+    c.whole = 0;
+    if (lane < pd.num_shards) {
+      const int u = (c.b * pd.num_shards + lane) * pd.G + g;
+      const Unit x = make_unit(pd, u);
+      const int ps = prefix[u], ue = prefix[u + 1];
+      const int us = unit_tile_start(prefix, u, hdr->unit_cost);
+      // no token to see: an empty shard, or a padding row of a request with
+      // fewer query tokens
+      if (us < ue && c.r < x.rows) {
+        const int c0 = us / per, c1 = (ue - 1) / per;
+        c.c0 = c0;
+        c.ps = ps;
+        c.whole = c0 == c1;
+        np = c0 == c1 ? 1 : c1 - c0 + 1;
+      }
+    }
+    int incl = np;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  wsum = 0.f;
-  if (M == -CUDART_INF_F) return;
+    for (int off = 1; off < kMaxShards; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    c.excl = incl - np;
+    c.count = __shfl_sync(0xffffffffu, incl, kMaxShards - 1);
+    return c;
+  }
+  __device__ void piece(const Ctx& c, int k, const float*& src, float& lse) const {
+    int s = 0;
 #pragma unroll
-  for (int s0 = 0; s0 < kMaxShards; s0 += 4) {
-    if (s0 >= num_shards) break;
-    if (s0 > 0) load4(s0);
+    for (int t = 1; t < kMaxShards; ++t)
+      if (t < pd.num_shards && k >= __shfl_sync(0xffffffffu, c.excl, t)) s = t;
+    const int ex = __shfl_sync(0xffffffffu, c.excl, s);
+    const int c0 = __shfl_sync(0xffffffffu, c.c0, s);
+    const int ps = __shfl_sync(0xffffffffu, c.ps, s);
+    const int whole = __shfl_sync(0xffffffffu, c.whole, s);
+    if (whole) {
+      const size_t i = ((size_t)s * pd.B + c.b) * pd.R + c.rr;
+      src = part + i * kDv;
+      lse = part_lse[i];
+    } else {
+      // a CTA writes its first piece to slot 0 and its last to slot 1; the
+      // unit's first CTA had an earlier piece iff its range starts before
+      // the unit's positions
+      const int cc = c0 + (k - ex);
+      const int per = hdr->per_cta;
+      const size_t slot = (cc == c0 && c0 * per < ps) ? 2 * (size_t)cc + 1 : 2 * (size_t)cc;
+      src = ws_o + (slot * kRows + c.r) * kDv;
+      lse = ws_lse[slot * kRows + c.r];
+    }
+  }
+};
+
+// Merges pieces [kbeg, kend) of one row's T pieces (all of them by
+// default), a warp at a time, over part of the row: lane `lane` owns the
+// float4 columns q0 + lane + 32 v (v < kVec).  The merge is online, batch by
+// batch in piece order: a batch's data loads are issued together with its
+// LSE loads (the piece addresses need no memory access), the running maximum
+// M is raised to the batch's largest LSE and the sums so far are rescaled
+// by exp(M_old - M_new).  A typical row is thus two memory round trips (the
+// unit lookup, then one batch), and a long request's row -- dozens of
+// pieces, every shard's unit split across CTAs -- one round trip per kB
+// pieces.  Returns the unnormalised sum acc, M and wsum = sum of
+// exp(lse - M) over the warp's pieces (the same value in every lane).
+template <int kVec, int kB, class Src>
+__device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, int q0,
+                                             float4 (&acc)[kVec], float& M, float& wsum,
+                                             int part = 0, int nparts = 1) {
+  const typename Src::Ctx ctx = src.prepare(row, lane);
+  const int T = ctx.count;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (s0 + j < num_shards) {
-        const float w = __expf(l[s0 + j] - M);
-        wsum += w;
+  for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  M = -CUDART_INF_F;
+  float ws = 0.f;
+  const int kbeg = (int)((long long)T * part / nparts);
+  const int kend = (int)((long long)T * (part + 1) / nparts);
+  for (int k0 = kbeg; k0 < kend; k0 += 32) {
+    const float* p;
+    float l;
+    src.piece(ctx, min(k0 + lane, kend - 1), p, l);
+    if (k0 + lane >= kend) l = -CUDART_INF_F;
+    const unsigned long long pa = reinterpret_cast<unsigned long long>(p);
+    const int n = min(32, kend - k0);
+    for (int j = 0; j < n; j += kB) {
+      float4 ob[kB][kVec];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[k].x += w * ob[j][k].x;
-          acc[k].y += w * ob[j][k].y;
-          acc[k].z += w * ob[j][k].z;
-          acc[k].w += w * ob[j][k].w;
+      for (int jj = 0; jj < kB; ++jj) {
+        const float4* s4 = reinterpret_cast<const float4*>(__shfl_sync(0xffffffffu, pa, j + jj));
+        if (j + jj < n) {
+#pragma unroll
+          for (int v = 0; v < kVec; ++v) ob[jj][v] = s4[q0 + lane + 32 * v];
+        }
+      }
+      float mb = (lane >= j && lane < j + kB) ? l : -CUDART_INF_F;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+      if (mb > M) {
+        const float sc = M == -CUDART_INF_F ? 0.f : __expf(M - mb);
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+          acc[v].x *= sc;
+          acc[v].y *= sc;
+          acc[v].z *= sc;
+          acc[v].w *= sc;
+        }
+        ws *= sc;
+        M = mb;
+      }
+      if (M == -CUDART_INF_F) continue;   // nothing seen yet: every lse so far is -inf
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj) {
+        const float w = __expf(__shfl_sync(0xffffffffu, l, j + jj) - M);
+        if (j + jj < n) {
+          ws += w;
+#pragma unroll
+          for (int v = 0; v < kVec; ++v) {
+            acc[v].x = fmaf(w, ob[jj][v].x, acc[v].x);
+            acc[v].y = fmaf(w, ob[jj][v].y, acc[v].y);
+            acc[v].z = fmaf(w, ob[jj][v].z, acc[v].z);
+            acc[v].w = fmaf(w, ob[jj][v].w, acc[v].w);
+          }
         }
       }
     }
   }
+  wsum = ws;
 }
 
-// One warp per query row; each lane owns 16 of the 512 latent dims
-// (four float4 at dims 4*lane + 128*k), so every load instruction of the warp
-// reads 512 contiguous bytes.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const float* __restrict__ partials,
-                                                          const float* __restrict__ lses,
-                                                          int num_shards, int rows,
-                                                          uint16_t* __restrict__ out,
-                                                          float* __restrict__ lse_out) {
+// Two warps per query row, one per 256-wide half of the 512 latent dims (a
+// lane owns two float4 of its half, so each load instruction of a warp reads
+// 512 contiguous bytes), eight pieces in flight per batch; a block of 256
+// threads handles four rows.
+template <class Src>
+__global__ void __launch_bounds__(256, 2) mla_combine_kernel(Src src, int rows,
+                                                             uint16_t* __restrict__ out,
+                                                             float* __restrict__ lse_out) {
   griddep_wait();                // the partials
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + (warp >> 1), half = warp & 1;
   if (row >= rows) return;
-  float4 acc[4];
+  float4 acc[2];
   float M, wsum;
-  merge_row(partials, lses, num_shards, rows, row, lane, acc, M, wsum);
+  merge_pieces<2, 8>(src, row, lane, 64 * half, acc, M, wsum);
   const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
   uint2* dst = reinterpret_cast<uint2*>(out + (size_t)row * kDv);
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    dst[lane + 32 * k] = make_uint2(pack2(acc[k].x * inv, acc[k].y * inv),
-                                    pack2(acc[k].z * inv, acc[k].w * inv));
-  if (lse_out != nullptr && lane == 0)
-    lse_out[row] = M > -CUDART_INF_F ? M + __logf(wsum) : -CUDART_INF_F;
+  for (int v = 0; v < 2; ++v)
+    dst[64 * half + lane + 32 * v] = make_uint2(pack2(acc[v].x * inv, acc[v].y * inv),
+                                                pack2(acc[v].z * inv, acc[v].w * inv));
+  if (lse_out != nullptr && half == 0 && lane == 0)
+    lse_out[row] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
 }
 
-// Fused combine + W_UV.  Block (h, jb) handles head h and output columns
-// [16*jb, 16*jb + 16) for every (b, i) row of that head, 8 rows at a time:
-// it merges the shard partials of those rows into shared memory (fp32, one
-// warp per row), then 256 threads (16 columns x 16 slices; slice s takes the
-// latent dims c = s mod 16) accumulate out . W_UV[h][:, col] and reduce the
-// slices.  128 / 16 column blocks per head keep 8 x H blocks in flight: at
-// small batches the projection is latency-bound, not bandwidth-bound.  The
-// block's W_UV columns (512 x 16 bf16) do not depend on the partials, so they
-// are staged in shared memory before the wait on the preceding kernel.
-constexpr int kWuvRowsPerPass = 8;
-constexpr int kWuvCols = 16;                  // output columns per block
-constexpr int kWuvSlices = 256 / kWuvCols;    // 16 slices of 32 latent dims
+// Fused combine + W_UV, as a cluster of four CTAs that split the 512 latent
+// dims.  Cluster (h, rb) handles head h and the query rows (b, i) of block rb
+// (kWuvRows of them); CTA q of the cluster merges the dims [128 q, 128 q + 128)
+// of those rows (one warp per row, one float4 per lane), multiplies them by
+// W_UV[h][128 q .. 128 q + 127][:] (32 KB, staged in shared memory before the
+// wait on the preceding kernel), and the four partial projections are summed
+// through distributed shared memory, in the fixed order q = 0..3, by CTA q
+// for output columns [32 q, 32 q + 32).  Every latent value is merged once
+// and W_UV is read once per row block.
+constexpr int kWuvRows = 8;            // query rows per cluster (one warp each)
+constexpr int kWuvSplit = 4;           // CTAs per cluster
+constexpr int kWuvDims = kDv / kWuvSplit;   // 128 latent dims per CTA
 
-__global__ void __launch_bounds__(256) mla_combine_wuv_kernel(
-    const float* __restrict__ partials, const float* __restrict__ lses, int num_shards,
-    int rows_per_head_group /* B*q_len */, int H, const uint16_t* __restrict__ w_uv,
-    uint16_t* __restrict__ y, float* __restrict__ lse_out) {
-  __shared__ float so[kWuvRowsPerPass][kDv];
-  __shared__ float red[kWuvSlices][kWuvRowsPerPass][kWuvCols];
-  __shared__ __align__(16) uint16_t wsm[kDv][kWuvCols];
-  const int h = blockIdx.x, jb = blockIdx.y;
-  const int tid = threadIdx.x;
+template <class Src>
+__global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
+    mla_combine_wuv_kernel(Src src, int rows_per_head /* B*q_len */, int H,
+                           const uint16_t* __restrict__ w_uv, uint16_t* __restrict__ y,
+                           float* __restrict__ lse_out) {
+  __shared__ __align__(16) uint16_t wsm[kWuvDims][kDuv];   // 32 KB
+  __shared__ __align__(16) float so[kWuvRows][kWuvDims];   // merged latent slice
+  __shared__ __align__(16) float yp[kWuvRows][kDuv];       // this CTA's partial projection
+  __shared__ __align__(16) float red[8][kWuvDims];         // per-warp sums of a row's pieces
+  __shared__ float rsum[8], rmax[8];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int q = (int)cluster.block_rank();
+  const int h = blockIdx.x / kWuvSplit;
+  const int rb = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
-    // 512 rows x 32 bytes: two 16-byte pieces per row
-    const uint16_t* wblk = w_uv + (size_t)h * kDv * kDuv + kWuvCols * jb;
-    for (int i = tid; i < kDv * 2; i += blockDim.x) {
-      const int c = i >> 1, half = i & 1;
-      *reinterpret_cast<uint4*>(&wsm[c][8 * half]) =
-          __ldg(reinterpret_cast<const uint4*>(wblk + (size_t)c * kDuv + 8 * half));
-    }
+    const uint4* wsrc =
+        reinterpret_cast<const uint4*>(w_uv + ((size_t)h * kDv + (size_t)kWuvDims * q) * kDuv);
+    uint4* wdst = reinterpret_cast<uint4*>(&wsm[0][0]);
+    for (int i = tid; i < kWuvDims * kDuv / 8; i += 256) wdst[i] = __ldg(wsrc + i);
   }
   griddep_wait();                // the partials
-  const int rows = rows_per_head_group * H;
-  const int col = tid & (kWuvCols - 1), slice = tid / kWuvCols;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int base = 0; base < rows_per_head_group; base += kWuvRowsPerPass) {
-    const int nr = min(kWuvRowsPerPass, rows_per_head_group - base);
-    // merge: warp w handles row w of this pass
-    if (warp < nr) {
-      const int row = (base + warp) * H + h;
-      float4 acc[4];
-      float M, wsum;
-      merge_row(partials, lses, num_shards, rows, row, lane, acc, M, wsum);
-      const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<float4*>(&so[warp][4 * (lane + 32 * k)]) = v;
+  const int bi0 = rb * kWuvRows;
+  const int nr = min(kWuvRows, rows_per_head - bi0);
+  // warps per row: with fewer rows than warps, a row's pieces are divided
+  // between several warps, whose sums are added in a fixed order below
+  const int wpr = nr > 4 ? 1 : nr > 2 ? 2 : nr > 1 ? 4 : 8;
+  {
+    const int r = warp / wpr, part = warp % wpr;
+    float4 acc[1] = {make_float4(0.f, 0.f, 0.f, 0.f)};
+    float M = -CUDART_INF_F, wsum = 0.f;
+    if (r < nr)
+      merge_pieces<1, 16>(src, (bi0 + r) * H + h, lane, kWuvDims / 4 * q, acc, M, wsum, part,
+                          wpr);
+    *reinterpret_cast<float4*>(&red[warp][4 * lane]) = acc[0];
+    if (lane == 0) {
+      rsum[warp] = wsum;
+      rmax[warp] = M;
+    }
+  }
+  __syncthreads();
+  {
+    // row r's merged slice: its warps' parts brought to the row's largest
+    // maximum and added in order, normalised
+    const int r = warp;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nr) {
+      float M = -CUDART_INF_F;
+      for (int pp = 0; pp < wpr; ++pp) M = fmaxf(M, rmax[r * wpr + pp]);
+      float ws = 0.f;
+      if (M > -CUDART_INF_F) {
+        for (int pp = 0; pp < wpr; ++pp) {
+          const float mp = rmax[r * wpr + pp];
+          const float sc = mp == -CUDART_INF_F ? 0.f : __expf(mp - M);
+          const float4 a = *reinterpret_cast<const float4*>(&red[r * wpr + pp][4 * lane]);
+          v.x = fmaf(sc, a.x, v.x);
+          v.y = fmaf(sc, a.y, v.y);
+          v.z = fmaf(sc, a.z, v.z);
+          v.w = fmaf(sc, a.w, v.w);
+          ws = fmaf(sc, rsum[r * wpr + pp], ws);
+        }
       }
-      if (lse_out != nullptr && jb == 0 && lane == 0)
-        lse_out[row] = M > -CUDART_INF_F ? M + __logf(wsum) : -CUDART_INF_F;
+      const float inv = ws > 0.f ? 1.0f / ws : 0.f;
+      v = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+      if (lse_out != nullptr && q == 0 && lane == 0)
+        lse_out[(bi0 + r) * H + h] = ws > 0.f ? M + __logf(ws) : -CUDART_INF_F;
     }
-    __syncthreads();
-    float acc[kWuvRowsPerPass];
-#pragma unroll
-    for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] = 0.f;
+    *reinterpret_cast<float4*>(&so[r][4 * lane]) = v;
+  }
+  __syncthreads();
+  {
+    // thread (rh, c): output column c, rows 4 rh .. 4 rh + 3
+    const int c = tid & (kDuv - 1), rh = tid >> 7;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-    for (int c = slice; c < kDv; c += kWuvSlices) {
-      const float w = __uint_as_float(((uint32_t)wsm[c][col]) << 16);
+    for (int d = 0; d < kWuvDims; ++d) {
+      const float w = __uint_as_float(((uint32_t)wsm[d][c]) << 16);
 #pragma unroll
-      for (int r = 0; r < kWuvRowsPerPass; ++r) acc[r] += so[r][c] * w;
+      for (int r = 0; r < 4; ++r) a[r] = fmaf(so[4 * rh + r][d], w, a[r]);
     }
 #pragma unroll
-    for (int r = 0; r < kWuvRowsPerPass; ++r) red[slice][r][col] = acc[r];
-    __syncthreads();
-    if (tid < nr * kWuvCols) {
-      const int r = tid / kWuvCols, c = tid % kWuvCols;
+    for (int r = 0; r < 4; ++r) yp[4 * rh + r][c] = a[r];
+  }
+  cluster.sync();                // every CTA's partial projection is complete
+  {
+    // CTA q finalises columns [32 q, 32 q + 32) of the block's rows
+    const int r = tid >> 5, c = 32 * q + lane;
+    if (r < nr) {
       float v = 0.f;
 #pragma unroll
-      for (int sl = 0; sl < kWuvSlices; ++sl) v += red[sl][r][c];
-      const int row = (base + r) * H + h;
+      for (int qq = 0; qq < kWuvSplit; ++qq) {
+        const float* peer = cluster.map_shared_rank(&yp[0][0], qq);
+        v += peer[r * kDuv + c];
+      }
       __nv_bfloat16 b = __float2bfloat16_rn(v);
-      y[(size_t)row * kDuv + kWuvCols * jb + c] = *reinterpret_cast<uint16_t*>(&b);
+      y[((size_t)(bi0 + r) * H + h) * kDuv + c] = *reinterpret_cast<uint16_t*>(&b);
     }
-    __syncthreads();
   }
+  cluster.sync();                // peers' shared memory stays alive until read
 }
 
-cudaError_t launch_combine(const float* partials, const float* lses, int num_shards, int rows,
-                           uint16_t* out, float* lse_out, cudaStream_t stream) {
+template <class Src>
+cudaError_t launch_combine_impl(const Src& src, int rows, uint16_t* out, float* lse_out,
+                                cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ceil_div(rows, 8));
+  cfg.gridDim = dim3(ceil_div(rows, 4));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, partials, lses, num_shards, rows, out,
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src>, src, rows, out, lse_out);
+}
+
+template <class Src>
+cudaError_t launch_combine_wuv_impl(const Src& src, int rows_per_head, int H,
+                                    const uint16_t* w_uv, uint16_t* y, float* lse_out,
+                                    cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H * kWuvSplit, ceil_div(rows_per_head, kWuvRows));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr = pdl_attribute();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_wuv_kernel<Src>, src, rows_per_head, H, w_uv, y,
                             lse_out);
 }
 
+}  // namespace
+
+cudaError_t launch_combine(const float* partials, const float* lses, int num_shards, int rows,
+                           uint16_t* out, float* lse_out, cudaStream_t stream) {
+  return launch_combine_impl(StackedRows{partials, lses, num_shards, rows}, rows, out, lse_out,
+                             stream);
+}
+
 cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
-                               int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
+                               int rows_per_head, int H, const uint16_t* w_uv, uint16_t* y,
                                float* lse_out, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(H, kDuv / kWuvCols);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr = pdl_attribute();
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_wuv_kernel, partials, lses, num_shards,
-                            rows_per_head_group, H, w_uv, y, lse_out);
+  return launch_combine_wuv_impl(StackedRows{partials, lses, num_shards, rows_per_head * H},
+                                 rows_per_head, H, w_uv, y, lse_out, stream);
+}
+
+cudaError_t launch_step_combine(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
+                                const float* ws_o, const float* ws_lse, const float* part,
+                                const float* part_lse, const uint16_t* w_uv, uint16_t* out,
+                                float* lse_out, cudaStream_t stream) {
+  const StepRows src{pd, hdr, prefix, ws_o, ws_lse, part, part_lse};
+  if (w_uv == nullptr) return launch_combine_impl(src, pd.B * pd.R, out, lse_out, stream);
+  return launch_combine_wuv_impl(src, pd.B * pd.q_len, pd.H, w_uv, out, lse_out, stream);
 }
 
 }  // namespace mla
