@@ -13,32 +13,44 @@
 //   - the query: per row a power-of-two scale s_r puts max|q| in [128, 256);
 //     q*s_r = hi + lo with hi = e4m3(q*s_r), lo = e4m3(q*s_r - hi).  That is
 //     exact for every component with |q*s_r| >= 2^-2 and within 2^-10 (in
-//     scaled units) below; S = (Q_hi + Q_lo) K^T is two accumulating MMAs.
+//     scaled units) below.  Q_hi and Q_lo are the 128 rows of one M=128 MMA
+//     (row 2k: Q_hi of query row k, row 2k+1: its Q_lo), so S_hi and S_lo of
+//     a query row land in adjacent TMEM lanes and the two threads reading
+//     them exchange halves by shuffle; an M=64 MMA would cost the tensor core
+//     as much as an M=128 one.
 //   - the probabilities: with sigma_t = mant_t * 2^E_t (mant in [0.5, 1)),
 //     the softmax keeps its running max over b_t = a_t + E_t, where a_t is
-//     the log2-domain logit; e_t = 2^(b_t - m) is at most 2^8, P'_t = e_t *
-//     mant_t = 2^(a_t - m) * sigma_t carries the value scale, and the
-//     normaliser sums e_t * 2^-E_t = 2^(a_t - m).  P' = hi + lo as above
+//     the log2-domain logit, so that P'_t = 2^(a_t - m) * sigma_t =
+//     2^(b_t - m) * mant_t is at most 2^8; P'_t carries the value scale, and
+//     the normaliser sums u_t = 2^(a_t - m).  P' = hi + lo as above
 //     (relative error about 2^-8, like a bf16 P), and O^T += V^T P'^T is two
 //     accumulating MMAs per 32-token step.
 // The tensor cores accumulate in fp32.
 //
 // Shared memory (1024-byte aligned base):
-//   Q            72 KB      per 8-row group rg, 9216 bytes: Q_hi then Q_lo, each
+//   Q            72 KB      the MMA's 128 rows (Q_hi, Q_lo of query rows 4G..4G+3
+//                           interleaved) in 16 groups of 8, 4608 bytes each:
 //                           [chunk c][8 rows][64 codes] with 64-byte swizzle; the
-//                           piece's bf16 rows land here by TMA first, in the same
-//                           9216 bytes per row group, and are split in place
+//                           piece's bf16 rows land here by TMA first (9216 bytes
+//                           per 8 query rows, the same bytes as their two groups)
+//                           and are split in place
 //   stages       4 x 36 KB  group-major: slot a's 64-code chunk c at
 //                           (a/8)*4608 + c*512 + (a%8)*64 (swizzled), one TMA box per page
 //   P_lo         4 KB       [8-row group][8 rows][64 tokens]; P_hi goes into the
 //                           stage's rope atoms once QK^T has read them
-//   misc         barriers, token scales and their exponent split, softmax exchange
+//   misc         barriers, token scales and their exponents, the softmax groups' exchange
 //
-// Warps: 0 producer (block table, TMA of the codes, cp.async of the scales);
-// 1 issues QK^T (per pair of adjacent stages as one N=128 chain, else per
-// tile); 6 issues P.V; 2..5 softmax and epilogue (two threads per query row);
-// 7..10 load each piece's query by TMA and split it into Q_hi/Q_lo in place,
-// and warp 7 also splits every tile's token scales.
+// Warps: 0 producer (block table, TMA of the codes, cp.async of the scales,
+// L2 prefetch of the next tiles); 1 issues QK^T (per pair of adjacent stages
+// as one N=128 chain, else per tile) and then splits the unit's token scales
+// into mantissa and exponent; 6 and 7 issue P.V, two latent blocks each
+// (P_lo terms first, so the one P_lo buffer is freed early); 2..5 and 8..11
+// are two softmax groups, two warps per SM sub-partition: group k takes
+// tokens [32 k, 32 k + 32) of every tile (two threads per query row, 16
+// tokens each), the groups exchange each row's tile maximum through shared
+// memory,
+// and group 1 also loads each piece's query by TMA and splits it into
+// Q_hi / Q_lo in place.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -50,13 +62,15 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
+constexpr int kPvIssuers = 2;              // P.V-issuing warps (6, 7), two latent blocks each
 constexpr int kStages = 4;
 constexpr int kStageBytes = kTile * kDqk;        // 36864: codes of one 64-token tile
 constexpr int kAtom = 512;                       // 8 rows x 64 bytes
 constexpr int kGroupBytes = kChunks * kAtom;     // 4608: one 8-slot group, nine chunks
 constexpr int kRopeAtom = 8 * kAtom;             // rope chunk of a group (P_hi after QK^T)
-constexpr int kQGroupBytes = 2 * kChunks * kAtom;  // 9216: Q_hi + Q_lo of 8 rows (= their bf16)
+constexpr int kQGroupBytes = 2 * kChunks * kAtom;  // 9216: bf16 of 8 query rows (= 2 MMA row groups)
+constexpr int kQAGroupBytes = kChunks * kAtom;     // 4608: one 8-row group of the MMA's 128 rows
 constexpr int kQBytes = 8 * kQGroupBytes;          // 73728
 constexpr int kSmemQ = 0;
 constexpr int kSmemKV = kQBytes;                                 // 73728
@@ -66,55 +80,45 @@ constexpr int kMiscBytes = 6144;
 constexpr int kSmemBytes = kSmemMisc + kMiscBytes + 1024;        // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr int kSoftmaxThreads = 128;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kConvThreads = 128;
-constexpr uint32_t kBarSoftmax = 1;
-constexpr uint32_t kBarConv = 2;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: e_t <= 2^8 keeps P' inside e4m3
+constexpr int kSoftmaxThreads = 256;        // both groups
+constexpr int kSoftmaxWarps = 8;
+constexpr int kConvThreads = 128;           // softmax group 1 splits the query
+constexpr uint32_t kBarSoftmax = 1;         // all softmax threads
+constexpr uint32_t kBarGroup0 = 2;          // group k: kBarGroup0 + k
+constexpr uint32_t kBarConv = 4;            // the query split (group 1)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: 2^(b_t - m) <= 2^8 keeps P' inside e4m3
+constexpr int kPrefetch = 2;               // tiles of a piece prefetched into L2 ahead of the loads
 
 struct Misc {
   uint64_t kv_full[kStages], kv_empty[kStages], prep[kStages];
   uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t plo_free[2];  // the P_lo terms of a tile's P.V have completed (P_lo may be rewritten)
   uint64_t q_full, q_conv, q_empty, o_free;
   uint64_t drain;       // teardown after a failure: MMAs in flight
   uint32_t tmem_base;
   int abort;
-  float alpha[2][kRows];
+  float alpha[2][kRows];        // per softmax group: the rescale factor of each row
   alignas(16) float inv_l[kRows];
-  float qsc[kRows];     // splitters: the row's power-of-two scale (0: padding row)
+  float qinv[kRows];            // 1 / the row's power-of-two query scale (split by group 1)
+  float qsc[kRows];             // the row's power-of-two query scale s_r (0: padding row)
+  float xmax[2][2][kRows];      // by tile parity and group: the row's max over the group's tokens
+  float xl[2][kRows];           // per group: the row's sum over the group's tokens (epilogue)
   // per stage and token slot: the scale (cp.async target, then sanitised in
-  // place), E + 1 as a float, 2^-(E+1), and sigma * 2^-(E+1)
+  // place) and the exponent E of its mantissa-exponent split, as a float
   alignas(16) float sigma[kStages][kTile];
   alignas(16) float lge[kStages][kTile];
-  alignas(16) float il[kStages][kTile];
-  alignas(16) float mant[kStages][kTile];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc block");
 
-// TMEM: two S buffers of 128 columns (M=64: a QK^T unit of one or two tiles,
-// tile g at columns 64 (g & 1)), then the four 128-dim blocks of O^T (M=128,
-// 64 columns each).
+// TMEM: two S buffers of 128 columns (M=128, lane 2k = S_hi of query row k,
+// lane 2k + 1 = its S_lo: a QK^T unit of one or two tiles, tile g at columns
+// 64 (g & 1)), then the four 128-dim blocks of O^T (M=128, 64 columns each).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0, kColO = 256;
 
 __device__ __forceinline__ void set_error(PartialParams& p, Misc* misc, unsigned bits) {
   atomicOr(&p.hdr->err, bits);
   if (bits & kErrTimeout) *(volatile int*)&misc->abort = 1;
-}
-
-// Largest |q| of a row half as a bf16 magnitude pattern (monotonic in |q|;
-// NaN sorts above inf), over 288 values from 36 16-byte loads.
-__device__ __forceinline__ uint32_t half_row_max(const uint4* src) {
-  uint32_t m = 0;
-#pragma unroll 12
-  for (int i = 0; i < 36; ++i) {
-    const uint4 v = __ldg(src + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-  }
-  return m;
 }
 
 // Biased exponent that fixes a row's power-of-two query scale: s_r =
@@ -162,20 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(b_kv_full + 8 * st, 1 + 32);   // expect_tx arrival + one cp.async arrival per lane
-      mbar_init(b_kv_empty + 8 * st, 1);
+      mbar_init(b_kv_empty + 8 * st, kPvIssuers);
       mbar_init(b_prep + 8 * st, 1);
     }
     for (int sb = 0; sb < 2; ++sb) {
       mbar_init(b_s_full + 8 * sb, 1);
       mbar_init(b_s_empty + 8 * sb, kSoftmaxWarps);
       mbar_init(b_p_full + 8 * sb, kSoftmaxWarps);
-      mbar_init(b_pv_done + 8 * sb, 1);
+      mbar_init(b_pv_done + 8 * sb, kPvIssuers);
+      mbar_init(smem_u32(&misc->plo_free[sb]), kPvIssuers);
     }
     mbar_init(b_q_full, 1);
     mbar_init(b_q_conv, kConvThreads / 32);
     mbar_init(b_q_empty, 1);
     mbar_init(b_o_free, kSoftmaxWarps);
-    mbar_init(smem_u32(&misc->drain), 2);     // the two MMA-issuing threads
+    mbar_init(smem_u32(&misc->drain), 1 + kPvIssuers);   // the MMA-issuing threads
     misc->abort = 0;
     fence_mbar_init();
   }
@@ -216,8 +221,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
       const int res = nv > 1 ? x.s : 0;
       int win_base = -1, win_val = -1;
+      int pwin_base = -1, pwin_val = -1;   // block-table window of the L2 prefetches
       for (int j = t0; j < t1 && ok; ++j, ++gt) {
         const int st = gt & (kStages - 1);
+        // L2 prefetch of the piece's tiles up to kPrefetch ahead (this shard's
+        // rows of each page, and the lines of the page's token scales), so
+        // that a stage load mostly reads L2
+        for (int jp = (j == t0 ? j + 1 : j + kPrefetch); jp <= j + kPrefetch && jp < t1; ++jp) {
+          const int fs = nv > 1 ? jp * nv : (kLocal || pd.layout == kInterleaved ? jp : x.p0 + jp);
+          const int pwb = fs & ~31;
+          if (pwb != pwin_base && fs < npages_b) {
+            pwin_base = pwb;
+            const int e = pwb + lane;
+            pwin_val = (e < npages_b && e < pd.max_pages) ? __ldg(bt + e) : -1;
+          }
+          const int pidx = fs + lane;
+          const int pg = __shfl_sync(0xffffffffu, pwin_val, pidx & 31);
+          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages) {
+            tma_prefetch_l2_5d(&tm_kv, 0, 0, 0, 0, pg * kPage + res);
+            prefetch_l2(p.kv_scale + (size_t)pg * kPage);
+            prefetch_l2(p.kv_scale + (size_t)pg * kPage + 32);
+          }
+        }
         const int first_slot = nv > 1 ? j * nv : (kLocal || pd.layout == kInterleaved ? j : x.p0 + j);
         const int wb = first_slot & ~31;
         if (wb != win_base && first_slot < npages_b) {
@@ -270,11 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and one N=128 MMA chain covers them), else per single tile (N=64).
     // Unit u accumulates into S buffer u & 1 (128 columns); tile g's logits
     // are its columns 64 (g & 1) ..
-    const uint32_t id_qk1 = idesc_e4m3_f32(64, 64, false, false);
-    const uint32_t id_qk2 = idesc_e4m3_f32(64, 128, false, false);
-    // Q (A, K-major): 8-row groups 9216 bytes apart, chunks 512 (Q_lo 4608
-    // further); K (B, K-major): 8-slot groups 4608 apart
-    const uint64_t dq0 = sw64_desc(sQ, 16, kQGroupBytes);
+    const uint32_t id_qk1 = idesc_e4m3_f32(128, 64, false, false);
+    const uint32_t id_qk2 = idesc_e4m3_f32(128, 128, false, false);
+    // Q (A, K-major, 128 rows: Q_hi and Q_lo interleaved): 8-row groups 4608
+    // bytes apart, chunks 512; K (B, K-major): 8-slot groups 4608 apart
+    const uint64_t dq0 = sw64_desc(sQ, 16, kQAGroupBytes);
     const uint64_t dk0 = sw64_desc(sKV, 16, kGroupBytes);
     int gbase = 0, pc = 0, qu = 0;
     bool ok = true;
@@ -301,11 +326,36 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t aq = dq0 + (uint32_t)((c * kAtom + 32 * k) >> 4);
               const uint64_t bk = dk0 + st_off + (uint32_t)((c * kAtom + 32 * k) >> 4);
               mma_e4m3_ss(d, aq, bk, id, (c != 0 || k != 0) ? 1u : 0u);
-              mma_e4m3_ss(d, aq + (uint32_t)((kChunks * kAtom) >> 4), bk, id, 1u);
             }
           }
           mma_commit(b_s_full + 8 * sb);
           if (j + (pair ? 2 : 1) >= t1) mma_commit(b_q_empty);
+        }
+        // while the MMAs run: the unit's token scales, which have landed with
+        // its stages -- sanitised in place, and the exponent E of
+        // sigma = mant * 2^E (mant in [0.5, 1)) as a float
+        for (int tt = 0; tt < (pair ? 2 : 1); ++tt) {
+          const int sst = (g + tt) & (kStages - 1);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int a = lane + 32 * h;
+            float sg = misc->sigma[sst][a];
+            uint32_t bits = __float_as_uint(sg);
+            uint32_t eb = (bits >> 23) & 0xFFu;
+            if (eb < 27u) {
+              // zero, subnormal or below 2^-100: as 2^-60 (its values are
+              // negligible next to any normal token's, its logit ~0)
+              sg = copysignf(8.6736174e-19f, sg);
+              bits = __float_as_uint(sg);
+              eb = (bits >> 23) & 0xFFu;
+            }
+            // inf, NaN or >= 2^126: exponent 0 and the value itself as the
+            // scale, which propagates as the dequantised values would
+            misc->sigma[sst][a] = sg;
+            misc->lge[sst][a] = eb >= 253u ? 0.0f : (float)((int)eb - 126);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_prep + 8 * sst);
         }
         __syncwarp();
         ++qu;
@@ -315,11 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (warp == 6) {
+  } else if (warp == 6 || warp == 7) {
     // ------------------------------------------------------------ P.V issue
     // O^T (4 blocks of 128 dims) += V^T P'^T per tile: V^T (A, MN-major)
     // 64-dim blocks 512 bytes apart, 8-token groups 4608; P_hi in the
-    // groups' rope atoms, P_lo in its buffer (B, K-major)
+    // groups' rope atoms, P_lo in its buffer (B, K-major).  Warp 6 issues
+    // latent blocks 0, 1 and warp 7 blocks 2, 3; each issues its P_lo terms
+    // first and commits them to plo_free, so the softmax may write the next
+    // tile's P_lo (one buffer) while the P_hi terms still run.
+    const int blk0 = warp == 6 ? 0 : 2;
     const uint64_t dv0 = sw64_desc(sKV, kAtom, kGroupBytes);
     const uint64_t dph0 = sw64_desc(sKV + kRopeAtom, 16, kGroupBytes);
     const uint64_t dpl = sw64_desc(sPlo, 16, kAtom);
@@ -340,16 +394,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = g & (kStages - 1);
           const uint32_t st_off = (uint32_t)(st * kStageBytes) >> 4;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
+          for (int term = 1; term >= 0; --term) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const uint64_t a =
-                  dv0 + st_off + (uint32_t)((2 * blk * kAtom + kk * 4 * kGroupBytes) >> 4);
-              const uint32_t d = tmem + kColO + 64 * blk;
-              mma_e4m3_ss(d, a, dph0 + st_off + (uint32_t)((32 * kk) >> 4), id_pv,
-                          (j == t0 && kk == 0) ? 0u : 1u);
-              mma_e4m3_ss(d, a, dpl + (uint32_t)((32 * kk) >> 4), id_pv, 1u);
+            for (int b = 0; b < 2; ++b) {
+              const int blk = blk0 + b;
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t a =
+                    dv0 + st_off + (uint32_t)((2 * blk * kAtom + kk * 4 * kGroupBytes) >> 4);
+                const uint32_t d = tmem + kColO + 64 * blk;
+                const uint64_t pb = term ? dpl + (uint32_t)((32 * kk) >> 4)
+                                         : dph0 + st_off + (uint32_t)((32 * kk) >> 4);
+                // the piece's first tile starts the accumulator with its P_lo term
+                mma_e4m3_ss(d, a, pb, id_pv, (j == t0 && term == 1 && kk == 0) ? 0u : 1u);
+              }
             }
+            if (term == 1) mma_commit(smem_u32(&misc->plo_free[g & 1]));
           }
           mma_commit(b_kv_empty + 8 * st);
           mma_commit(b_pv_done + 8 * (g & 1));
@@ -360,155 +420,137 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (warp >= 7) {
-    // ------------------------------------------------------------ splitters
-    // Per piece: thread ct = 0 loads the 64 bf16 query rows by TMA (8 rows x
-    // 9 chunks per row group, 128-byte swizzle); thread (r, hh) = (ct / 2,
-    // ct % 2) takes row r's largest |q| over half of its 16-byte units; then,
-    // two row groups at a time, every thread reads 9 units into registers and,
-    // after a barrier, writes their Q_hi / Q_lo codes over the same row groups.
-    const int ct = threadIdx.x - 7 * 32;
-    const int r = ct >> 1, hh = ct & 1;
-    int gt = 0, pc = 0;
-    bool ok = true;
-    while (it.next(unit, t0, t1, whole, slot)) {
-      if (pc >= 1 && ok)
-        ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
-      // every splitter reaches these barriers once per piece, failure or not
-      if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
-      Unit x = make_unit<kLocal>(pd, unit);
-      if (ct == 0 && !(p.withhold_query && pc == 0)) {
-        mbar_arrive_expect_tx(b_q_full, kQBytes);
-        armed_q = pc;
-        tma_load_4d(sQ, &tm_q, b_q_full, 0, 0, 0, (x.b * pd.R + x.g * kRows) >> 3);
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
-      if (named_bar_or(kBarConv, kConvThreads, !ok)) { ok = false; break; }
-      uint8_t* q8 = smem + kSmemQ;
-      {
-        const int rg = r >> 3, rr = r & 7;
-        const uint8_t* row = q8 + rg * kQGroupBytes + rr * 128;
-        uint32_t mx = 0;
-#pragma unroll 12
-        for (int v = 0; v < 36; ++v) {
-          const int w = 36 * hh + v;   // 16-byte unit of the row: chunk w / 8, unit w % 8
-          const uint4 t = *reinterpret_cast<const uint4*>(row + (w >> 3) * 1024 + (w & 7) * 16);
-          const uint32_t ww[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx = max(mx, max(ww[k] & 0x7FFFu, (ww[k] >> 16) & 0x7FFFu));
-        }
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        const bool live = r < x.rows;
-        if (live && (mx >> 7) == 255u) atomicOr(&p.hdr->err, kErrQRange);   // inf or NaN
-        if (hh == 0) misc->qsc[r] = live ? __uint_as_float((261u - row_scale_exp(mx)) << 23) : 0.0f;
-      }
-      named_bar_sync(kBarConv, kConvThreads);
-#pragma unroll 1
-      for (int pr = 0; pr < 4; ++pr) {
-        uint4 in[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-          const int i = ct + kConvThreads * k;   // 16-byte unit of row groups 2 pr, 2 pr + 1
-          in[k] = *reinterpret_cast<const uint4*>(q8 + 2 * pr * kQGroupBytes + i * 16);
-        }
-        named_bar_sync(kBarConv, kConvThreads);   // the pair's bf16 has been read
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-          const int i = ct + kConvThreads * k;
-          const int rg = 2 * pr + i / 576, rem = i % 576;
-          const int c = rem >> 6, rr = (rem >> 3) & 7, u = (rem & 7) ^ rr;   // u: dims 8u.. of chunk c
-          const float sc = misc->qsc[rg * 8 + rr];
-          uint32_t whi = 0, wlo = 0, whi2 = 0, wlo2 = 0;
-          if (sc != 0.0f) {
-            const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
-            uint32_t sp[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              sp[e] = split_e4m3x2(__uint_as_float(w[e] << 16) * sc,
-                                   __uint_as_float(w[e] & 0xFFFF0000u) * sc);
-            whi = (sp[0] & 0xFFFFu) | (sp[1] << 16);
-            wlo = (sp[0] >> 16) | (sp[1] & 0xFFFF0000u);
-            whi2 = (sp[2] & 0xFFFFu) | (sp[3] << 16);
-            wlo2 = (sp[2] >> 16) | (sp[3] & 0xFFFF0000u);
-          }
-          uint8_t* dst = q8 + rg * kQGroupBytes + c * kAtom + rr * 64 +
-                         (((u >> 1) ^ (rr >> 1)) << 4) + (u & 1) * 8;
-          *reinterpret_cast<uint2*>(dst) = make_uint2(whi, whi2);
-          *reinterpret_cast<uint2*>(dst + kChunks * kAtom) = make_uint2(wlo, wlo2);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_q_conv);
-      if (warp == 7) {
-        for (int j = t0; j < t1; ++j, ++gt) {
-          const int st = gt & (kStages - 1);
-          if (ok) ok = __all_sync(0xffffffffu,
-                                  mbar_wait(b_kv_full + 8 * st, (gt >> 2) & 1, tmo, abort_flag));
-          if (!ok) continue;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int a = lane + 32 * h;
-            float sg = misc->sigma[st][a];
-            uint32_t bits = __float_as_uint(sg);
-            uint32_t eb = (bits >> 23) & 0xFFu;
-            if (eb < 27u) {
-              // zero, subnormal or below 2^-100: as 2^-60 (its values are
-              // negligible next to any normal token's, its logit ~0)
-              sg = copysignf(8.6736174e-19f, sg);
-              bits = __float_as_uint(sg);
-              eb = (bits >> 23) & 0xFFu;
-            }
-            float lg, inv, mt;
-            if (eb >= 253u) {   // inf, NaN or >= 2^126: propagate, as the dequantised values would
-              lg = 0.0f;
-              inv = sg;
-              mt = sg;
-            } else {
-              lg = (float)((int)eb - 126);
-              inv = __uint_as_float((253u - eb) << 23);
-              mt = __uint_as_float((bits & 0x807FFFFFu) | (126u << 23));
-            }
-            misc->sigma[st][a] = sg;
-            misc->lge[st][a] = lg;
-            misc->il[st][a] = inv;
-            misc->mant[st][a] = mt;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_prep + 8 * st);
-        }
-      } else {
-        gt += t1 - t0;
-      }
-      ++pc;
-    }
-    if (!ok && ct == 0) set_error(p, misc, kErrTimeout);
   } else {
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3;
-    const int tid = threadIdx.x - 64;    // 0..127
-    const int half = lane >> 4;
-    const int r = 16 * quad + (lane & 15);
+    // Group grp (warps 2..5: 0, warps 8..11: 1) takes tokens
+    // [32 grp, 32 grp + 32) of every tile.  Thread (quadrant, lane) reads
+    // TMEM lane 32 quadrant + lane, i.e. S_hi (even lane) or S_lo (odd lane)
+    // of query row r = 16 quadrant + lane / 2, for the group's 32 tokens; the
+    // two threads of a row swap halves, so each ends with S = S_hi + S_lo of
+    // 16 tokens: the even one tokens 32 grp .. + 15, the odd one the rest.
+    const int grp = warp >= 8 ? 1 : 0;
+    const int quad = warp & 3;           // TMEM lane quadrant this warp may access
+    const int gtid = threadIdx.x - (grp ? 256 : 64);   // 0..127 in the group
+    const int tid = gtid + 128 * grp;    // 0..255 over both groups
+    const int half = lane & 1;           // the term this thread's TMEM lane holds
+    const int r = 16 * quad + (lane >> 1);
+    const int tok0 = 32 * grp + 16 * half;   // this thread's first token of a tile
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     uint8_t* plo_row = smem + kSmemPlo + (r >> 3) * kAtom + (r & 7) * 64;   // P_lo row r
+    const int sw = (r & 7) >> 1;                                             // 64-byte swizzle
     int gt = 0, pc = 0, qu = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
+      if (grp == 1) {
+        // ---------------------------------------------------- query split
+        // Thread ct = 0 loads the piece's 64 bf16 query rows by TMA (8 rows
+        // x 9 chunks per row group, 128-byte swizzle); thread (qr, hh) =
+        // (ct / 2, ct % 2) takes row qr's largest |q| over half of its
+        // 16-byte units; then, two row groups at a time, every thread reads
+        // 9 units into registers and, after a barrier, writes their Q_hi /
+        // Q_lo codes over the same row groups.  Decisions that end the split
+        // early are taken by barrier reductions, so all 128 threads take the
+        // same path; a failure leaves ok false and the first reduction of the
+        // tile loop ends the piece for both groups.
+        const int ct = gtid;
+        const int qr = ct >> 1, hh = ct & 1;
+        if (pc >= 1 && ok)
+          ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
+        if (named_bar_or(kBarConv, kConvThreads, !ok)) {
+          ok = false;
+          if (ct == 0) set_error(p, misc, kErrTimeout);
+        }
+        if (ok) {
+          if (ct == 0 && !(p.withhold_query && pc == 0)) {
+            mbar_arrive_expect_tx(b_q_full, kQBytes);
+            armed_q = pc;
+            tma_load_4d(sQ, &tm_q, b_q_full, 0, 0, 0, (x.b * pd.R + x.g * kRows) >> 3);
+          }
+          ok = __all_sync(0xffffffffu, mbar_wait(b_q_full, pc & 1, tmo, abort_flag));
+          if (named_bar_or(kBarConv, kConvThreads, !ok)) {
+            ok = false;
+            if (ct == 0) set_error(p, misc, kErrTimeout);
+          }
+        }
+        if (ok) {
+          uint8_t* q8 = smem + kSmemQ;
+          {
+            const int rg = qr >> 3, rr = qr & 7;
+            const uint8_t* row = q8 + rg * kQGroupBytes + rr * 128;
+            uint32_t mx = 0;
+#pragma unroll 12
+            for (int v = 0; v < 36; ++v) {
+              const int w = 36 * hh + v;   // 16-byte unit of the row: chunk w / 8, unit w % 8
+              const uint4 t = *reinterpret_cast<const uint4*>(row + (w >> 3) * 1024 + (w & 7) * 16);
+              const uint32_t ww[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mx = max(mx, max(ww[k] & 0x7FFFu, (ww[k] >> 16) & 0x7FFFu));
+            }
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            const bool live = qr < x.rows;
+            if (live && (mx >> 7) == 255u) atomicOr(&p.hdr->err, kErrQRange);   // inf or NaN
+            if (hh == 0) {
+              // s_r = 2^(134 - e) puts max|q| in [128, 256); the softmax
+              // divides it out again with 1 / s_r = 2^(e - 134)
+              const uint32_t e = row_scale_exp(mx);
+              misc->qinv[qr] = __uint_as_float((e - 7u) << 23);
+              misc->qsc[qr] = live ? __uint_as_float((261u - e) << 23) : 0.0f;
+            }
+          }
+          named_bar_sync(kBarConv, kConvThreads);
+#pragma unroll 1
+          for (int pr = 0; pr < 4; ++pr) {
+            uint4 in[9];
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+              const int i = ct + kConvThreads * k;   // 16-byte unit of row groups 2 pr, 2 pr + 1
+              in[k] = *reinterpret_cast<const uint4*>(q8 + 2 * pr * kQGroupBytes + i * 16);
+            }
+            named_bar_sync(kBarConv, kConvThreads);   // the pair's bf16 has been read
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+              const int i = ct + kConvThreads * k;
+              const int rg = 2 * pr + i / 576, rem = i % 576;
+              const int c = rem >> 6, rr = (rem >> 3) & 7, u = (rem & 7) ^ rr;   // u: dims 8u.. of chunk c
+              const float sc = misc->qsc[rg * 8 + rr];   // s_r, 0 for a padding row
+              uint32_t whi = 0, wlo = 0, whi2 = 0, wlo2 = 0;
+              if (sc != 0.0f) {
+                const uint32_t w[4] = {in[k].x, in[k].y, in[k].z, in[k].w};
+                uint32_t sp[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  sp[e] = split_e4m3x2(__uint_as_float(w[e] << 16) * sc,
+                                       __uint_as_float(w[e] & 0xFFFF0000u) * sc);
+                whi = (sp[0] & 0xFFFFu) | (sp[1] << 16);
+                wlo = (sp[0] >> 16) | (sp[1] & 0xFFFF0000u);
+                whi2 = (sp[2] & 0xFFFFu) | (sp[3] << 16);
+                wlo2 = (sp[2] >> 16) | (sp[3] & 0xFFFF0000u);
+              }
+              // query row 8 rg + rr is MMA row i = 2 (rr % 4) (+1 for Q_lo)
+              // of group 2 rg + rr / 4; the swizzle term (i / 2) % 4 is rr % 4
+              // for both terms
+              uint8_t* dst = q8 + rg * kQGroupBytes + (rr >> 2) * kQAGroupBytes + c * kAtom +
+                             (rr & 3) * 128 + (((u >> 1) ^ (rr & 3)) << 4) + (u & 1) * 8;
+              *reinterpret_cast<uint2*>(dst) = make_uint2(whi, whi2);
+              *reinterpret_cast<uint2*>(dst + 64) = make_uint2(wlo, wlo2);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_q_conv);
+        }
+      } else {
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(b_q_conv, pc & 1, tmo, abort_flag));
+      }
       const bool owner = r < x.rows;
-      int unit_left = 0;   // tiles of the current QK^T unit still to read
       const int i_row = (x.g * kRows + r) / pd.H;
       const int vis_limit = x.L - x.qn + i_row;
-      // the row's query scale, computed exactly as the splitters do
-      float qs;
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + ((size_t)x.b * pd.R + (size_t)x.g * kRows + r) * kDqk + 288 * half);
-        uint32_t mx = owner ? half_row_max(src) : 0u;
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        qs = __uint_as_float((row_scale_exp(mx) - 7u) << 23) * pd.scale_log2;
-      }
-      float m_run = -CUDART_INF_F, l_run = 0.0f;
+      // the row's query scale and the softmax scale, in log2 units
+      const float qs = misc->qinv[r] * pd.scale_log2;
+      int unit_left = 0;   // tiles of the current QK^T unit still to read
+      float m_run = -CUDART_INF_F, l_run = 0.0f;   // l_run: sum of u_t over this thread's tokens
       for (int j = t0; j < t1; ++j, ++gt) {
         const int sb = qu & 1, st = gt & (kStages - 1);
         bool ok_s = ok;
@@ -520,13 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok_s = __all_sync(0xffffffffu,
                           ok_s && mbar_wait(b_prep + 8 * st, (gt >> 2) & 1, tmo, abort_flag));
-        bool resc = false;
-        uint32_t phi[8], plo[8];
         const bool full = tile_full<kLocal>(pd, x, j);
+        float a[16], sg[16];
+        uint32_t vis_mask = 0xFFFFu;
+        float mx = -CUDART_INF_F;
         if (ok_s) {
           tc_fence_after();
           uint32_t sr[32];
-          tmem_ld16x2_32(tmem + lane_off + kColS0 + 128 * sb + 64 * (gt & 1), sr);
+          tmem_ld32(tmem + lane_off + kColS0 + 128 * sb + 64 * (gt & 1) + 32 * grp, sr);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
@@ -534,102 +577,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(b_s_empty + 8 * sb);
             ++qu;
           }
-          // this tile's value factors, loaded early so their latency hides
-          // behind the logits and the max
-          float4 mtv[8], ilv[8];
-          {
-            const float4* mt4 = reinterpret_cast<const float4*>(&misc->mant[st][32 * half]);
-            const float4* il4 = reinterpret_cast<const float4*>(&misc->il[st][32 * half]);
+          // keep 16 tokens, send the partner the other term of its 16
+          float sv[16];
 #pragma unroll
-            for (int a4 = 0; a4 < 8; ++a4) {
-              mtv[a4] = mt4[a4];
-              ilv[a4] = il4[a4];
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float give = __uint_as_float(half ? sr[i] : sr[16 + i]);
+            const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+            sv[i] = __uint_as_float(half ? sr[16 + i] : sr[i]) + got;
           }
-          // b_t = S_t sigma_t / s_r * scale * log2(e) + E_t + 1
-          float b[32];
-          {
-            const float4* sg4 = reinterpret_cast<const float4*>(&misc->sigma[st][32 * half]);
-            const float4* lg4 = reinterpret_cast<const float4*>(&misc->lge[st][32 * half]);
+          // a_t = S_t sigma_t / s_r * scale * log2(e); b_t = a_t + E_t
+          const float4* sg4 = reinterpret_cast<const float4*>(&misc->sigma[st][tok0]);
+          const float4* lg4 = reinterpret_cast<const float4*>(&misc->lge[st][tok0]);
+          float b[16];
 #pragma unroll
-            for (int a4 = 0; a4 < 8; ++a4) {
-              const float4 sg = sg4[a4], lg = lg4[a4];
-              const float s0 = __uint_as_float(sr[4 * a4]);
-              const float s1 = __uint_as_float(sr[4 * a4 + 1]);
-              const float s2 = __uint_as_float(sr[4 * a4 + 2]);
-              const float s3 = __uint_as_float(sr[4 * a4 + 3]);
-              b[4 * a4] = fmaf(s0 * sg.x, qs, lg.x);
-              b[4 * a4 + 1] = fmaf(s1 * sg.y, qs, lg.y);
-              b[4 * a4 + 2] = fmaf(s2 * sg.z, qs, lg.z);
-              b[4 * a4 + 3] = fmaf(s3 * sg.w, qs, lg.w);
-            }
+          for (int a4 = 0; a4 < 4; ++a4) {
+            const float4 g = sg4[a4], l = lg4[a4];
+            sg[4 * a4] = g.x;
+            sg[4 * a4 + 1] = g.y;
+            sg[4 * a4 + 2] = g.z;
+            sg[4 * a4 + 3] = g.w;
+            a[4 * a4] = sv[4 * a4] * g.x * qs;
+            a[4 * a4 + 1] = sv[4 * a4 + 1] * g.y * qs;
+            a[4 * a4 + 2] = sv[4 * a4 + 2] * g.z * qs;
+            a[4 * a4 + 3] = sv[4 * a4 + 3] * g.w * qs;
+            b[4 * a4] = a[4 * a4] + l.x;
+            b[4 * a4 + 1] = a[4 * a4 + 1] + l.y;
+            b[4 * a4 + 2] = a[4 * a4 + 2] + l.z;
+            b[4 * a4 + 3] = a[4 * a4 + 3] + l.w;
           }
-          uint32_t vis_mask = 0xFFFFFFFFu;
           if (!full) {
 #pragma unroll
-            for (int a = 0; a < 32; ++a) {
-              int t = slot_token<kLocal>(pd, x, j, 32 * half + a);
-              bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
+            for (int i = 0; i < 16; ++i) {
+              const int t = slot_token<kLocal>(pd, x, j, tok0 + i);
+              const bool vis = slot_valid(pd, x, t) && (!pd.causal || t <= vis_limit);
               if (!vis) {
-                b[a] = -CUDART_INF_F;
-                vis_mask &= ~(1u << a);
+                a[i] = -CUDART_INF_F;
+                b[i] = -CUDART_INF_F;
+                vis_mask &= ~(1u << i);
               }
             }
           }
           float m4[4] = {b[0], b[1], b[2], b[3]};
 #pragma unroll
-          for (int a = 4; a < 32; a += 4) {
-            m4[0] = fmaxf(m4[0], b[a]);
-            m4[1] = fmaxf(m4[1], b[a + 1]);
-            m4[2] = fmaxf(m4[2], b[a + 2]);
-            m4[3] = fmaxf(m4[3], b[a + 3]);
+          for (int i = 4; i < 16; i += 4) {
+            m4[0] = fmaxf(m4[0], b[i]);
+            m4[1] = fmaxf(m4[1], b[i + 1]);
+            m4[2] = fmaxf(m4[2], b[i + 2]);
+            m4[3] = fmaxf(m4[3], b[i + 3]);
           }
-          float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_new = fmaxf(m_run, mx);
-          float alpha = 1.0f;
-          if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
-            alpha = (m_run == -CUDART_INF_F) ? 0.0f : ex2_approx(m_run - m_new);
-            l_run *= alpha;
-            m_run = m_new;
-            resc = owner && (j != t0);
-          }
-          if (owner && half == 0) misc->alpha[gt & 1][r] = alpha;
-          const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-          // e_t = 2^(b_t - m); P'_t = e_t mant_t; l += e_t 2^-(E_t+1)
-          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int a4 = 0; a4 < 8; ++a4) {
-            float4 mt = mtv[a4], iv = ilv[a4];
-            // a masked slot's scale may be garbage (even NaN): select, no branch
-            const uint32_t vm = vis_mask >> (4 * a4);
-            mt.x = (vm & 1u) ? mt.x : 0.0f;
-            iv.x = (vm & 1u) ? iv.x : 0.0f;
-            mt.y = (vm & 2u) ? mt.y : 0.0f;
-            iv.y = (vm & 2u) ? iv.y : 0.0f;
-            mt.z = (vm & 4u) ? mt.z : 0.0f;
-            iv.z = (vm & 4u) ? iv.z : 0.0f;
-            mt.w = (vm & 8u) ? mt.w : 0.0f;
-            iv.w = (vm & 8u) ? iv.w : 0.0f;
-            const float e0 = ex2_approx(b[4 * a4] - m_use);
-            const float e1 = ex2_approx(b[4 * a4 + 1] - m_use);
-            const float e2 = ex2_approx(b[4 * a4 + 2] - m_use);
-            const float e3 = ex2_approx(b[4 * a4 + 3] - m_use);
-            ls4[0] = fmaf(e0, iv.x, ls4[0]);
-            ls4[1] = fmaf(e1, iv.y, ls4[1]);
-            ls4[2] = fmaf(e2, iv.z, ls4[2]);
-            ls4[3] = fmaf(e3, iv.w, ls4[3]);
-            const uint32_t s01 = split_e4m3x2(e0 * mt.x, e1 * mt.y);
-            const uint32_t s23 = split_e4m3x2(e2 * mt.z, e3 * mt.w);
-            phi[a4] = (s01 & 0xFFFFu) | (s23 << 16);
-            plo[a4] = (s01 >> 16) | (s23 & 0xFFFF0000u);
-          }
-          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          if (half == 0) misc->xmax[gt & 1][grp][r] = mx;
         }
+        // both groups reach this reduction every tile: it publishes the
+        // groups' row maxima and ends the piece for all of them if any
+        // thread's wait failed
+        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
+        const float m_tile = fmaxf(mx, misc->xmax[gt & 1][grp ^ 1][r]);
+        const float m_new = fmaxf(m_run, m_tile);
+        float alpha = 1.0f;
+        bool resc = false;
+        if (m_new > m_run + kRescaleThreshold || (j == t0 && m_new > -CUDART_INF_F)) {
+          alpha = (m_run == -CUDART_INF_F) ? 0.0f : ex2_approx(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+          resc = owner && (j != t0);
+        }
+        if (owner && half == 0) misc->alpha[grp][r] = alpha;
         bool waited_pv = false;
-        if (named_bar_or(kBarSoftmax, kSoftmaxThreads, resc || !ok_s)) {
-          if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_s)) { ok = false; break; }
-          // some row's running max grew: rescale O^T once the previous P.V landed
+        // both groups see the same maxima, so they take the same decision
+        if (named_bar_or(kBarGroup0 + grp, 128, resc)) {
+          // some row's running max grew: rescale this group's half of O^T
+          // (latent blocks 2 grp, 2 grp + 1) once the previous P.V landed
           const bool ok_pv = __all_sync(
               0xffffffffu, (gt == 0) || mbar_wait(b_pv_done + 8 * ((gt - 1) & 1),
                                                   ((gt - 1) >> 1) & 1, tmo, abort_flag));
@@ -638,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok_pv) continue;  // caught by the next reduction (or the epilogue's)
           tc_fence_after();
 #pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
+          for (int blk = 2 * grp; blk < 2 * grp + 2; ++blk) {
 #pragma unroll 1
             for (int h2 = 0; h2 < 2; ++h2) {
               uint32_t v[32];
@@ -647,41 +666,60 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < 32; ++c)
-                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[gt & 1][32 * h2 + c]);
+                v[c] = __float_as_uint(__uint_as_float(v[c]) * misc->alpha[grp][32 * h2 + c]);
               tmem_st32(ta, v);
             }
           }
           tmem_wait_st();
         }
-        // P_lo has one buffer: the previous tile's P.V must have read it
+        // u_t = 2^(a_t - m); P'_t = u_t sigma_t (a masked slot's scale may be
+        // garbage, even NaN: select, no branch)
+        const float m_use = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+        uint32_t phi[4], plo[4];
+        {
+          float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            float pv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i = 4 * i4 + k;
+              const float u = ex2_approx(a[i] - m_use);
+              ls4[k] += u;
+              pv[k] = ((vis_mask >> i) & 1u) ? u * sg[i] : 0.0f;
+            }
+            const uint32_t s01 = split_e4m3x2(pv[0], pv[1]);
+            const uint32_t s23 = split_e4m3x2(pv[2], pv[3]);
+            phi[i4] = (s01 & 0xFFFFu) | (s23 << 16);
+            plo[i4] = (s01 >> 16) | (s23 & 0xFFFF0000u);
+          }
+          l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+        }
+        // P_lo has one buffer: the previous tile's P_lo terms must have run
         if (!waited_pv && gt > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(b_pv_done + 8 * ((gt - 1) & 1),
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&misc->plo_free[(gt - 1) & 1]),
                                                  ((gt - 1) >> 1) & 1, tmo, abort_flag));
           if (!ok) continue;
         }
         uint8_t* stage = smem + kSmemKV + st * kStageBytes;
         if (owner) {
-          // this thread's 32 tokens are 16-byte units 2 half, 2 half + 1 of the row
+          // this thread's 16 tokens are 16-byte unit tok0 / 16 of the row
+          const int u = tok0 >> 4;
           uint8_t* hrow = stage + (r >> 3) * kGroupBytes + kRopeAtom + (r & 7) * 64;
-          const int sw = (r & 7) >> 1;
-          *reinterpret_cast<uint4*>(hrow + (((2 * half) ^ sw) << 4)) =
+          *reinterpret_cast<uint4*>(hrow + ((u ^ sw) << 4)) =
               make_uint4(phi[0], phi[1], phi[2], phi[3]);
-          *reinterpret_cast<uint4*>(hrow + (((2 * half + 1) ^ sw) << 4)) =
-              make_uint4(phi[4], phi[5], phi[6], phi[7]);
-          *reinterpret_cast<uint4*>(plo_row + (((2 * half) ^ sw) << 4)) =
+          *reinterpret_cast<uint4*>(plo_row + ((u ^ sw) << 4)) =
               make_uint4(plo[0], plo[1], plo[2], plo[3]);
-          *reinterpret_cast<uint4*>(plo_row + (((2 * half + 1) ^ sw) << 4)) =
-              make_uint4(plo[4], plo[5], plo[6], plo[7]);
         }
         if (!full) {
           // zero the value codes of slots that hold no valid token of this
           // shard, so that garbage (even NaN codes) cannot reach O
           for (int e = tid; e < kTile * 32; e += kSoftmaxThreads) {
-            const int a = e >> 5, c = (e >> 2) & 7, u = e & 3;
-            const int t = slot_token<kLocal>(pd, x, j, a);
+            const int a2 = e >> 5, c = (e >> 2) & 7, u = e & 3;
+            const int t = slot_token<kLocal>(pd, x, j, a2);
             if (!slot_valid(pd, x, t))
-              *reinterpret_cast<uint4*>(stage + (a >> 3) * kGroupBytes + c * kAtom + (a & 7) * 64 +
-                                        u * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(stage + (a2 >> 3) * kGroupBytes + c * kAtom +
+                                        (a2 & 7) * 64 + u * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
@@ -693,6 +731,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok_e = __all_sync(
           0xffffffffu, ok && mbar_wait(b_pv_done + 8 * ((gt - 1) & 1), ((gt - 1) >> 1) & 1, tmo,
                                        abort_flag));
+      {
+        const float l_grp = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+        if (half == 0) misc->xl[grp][r] = l_grp;
+      }
       if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_e)) { ok = false; break; }
       tc_fence_after();
       float* dst_o;
@@ -706,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         dst_o = p.ws_o + sl * kRows * kDv;
         dst_lse = p.ws_lse + sl * kRows;
       }
-      const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
-      if (owner && half == 0) {
+      if (grp == 0 && owner && half == 0) {
+        const float l_tot = misc->xl[0][r] + misc->xl[1][r];
         float lse = (l_tot > 0.0f) ? (m_run + __log2f(l_tot)) * 0.69314718055994530942f
                                    : -CUDART_INF_F;
         misc->inv_l[r] = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
@@ -721,9 +763,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       {
-        const uint32_t o_base = tmem + lane_off + kColO;
+        // this group's latent blocks 2 grp, 2 grp + 1: block k / 2, rows
+        // 32 (k % 2) .. of this thread's latent dim, two TMEM loads in flight
+        const uint32_t o_base = tmem + lane_off + kColO + 128 * grp;
         auto store32 = [&](int k, const uint32_t (&v)[32]) {
-          const int dim = 128 * (k >> 1) + 32 * quad + lane;
+          const int dim = 128 * (2 * grp + (k >> 1)) + 32 * quad + lane;
           float il[32];
           const float4* il4 = reinterpret_cast<const float4*>(misc->inv_l + 32 * (k & 1));
 #pragma unroll
@@ -743,18 +787,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t va[32], vb[32];
         tmem_ld32(o_base, va);
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
+        for (int k = 0; k < 4; k += 2) {
           tmem_ld32(o_base + 32 * (k + 1), vb);
           tmem_wait_ld();
           store32(k, va);
-          if (k + 2 < 8) tmem_ld32(o_base + 32 * (k + 2), va);
+          if (k + 2 < 4) tmem_ld32(o_base + 32 * (k + 2), va);
           store32(k + 1, vb);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_o_free);
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // inv_l reused by the next piece
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // inv_l and xl reused by the next piece
       ++pc;
     }
     if (!ok && tid == 0) set_error(p, misc, kErrTimeout);
@@ -768,11 +812,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM is freed and the CTA exits (one commit drains every earlier MMA
     // of the issuing thread).
     int never = 0;
-    if (lane == 0 && (warp == 1 || warp == 6)) {
+    if (lane == 0 && (warp == 1 || warp == 6 || warp == 7)) {
       mma_commit(smem_u32(&misc->drain));
       mbar_wait(smem_u32(&misc->drain), 0, kDrainNs, &never);
     }
-    if (warp == 7 && lane == 0 && armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, kDrainNs, &never);
+    // the query copy is issued by thread 0 of softmax group 1 (warp 8, lane 0)
+    if (warp == 8 && lane == 0 && armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, kDrainNs, &never);
     if (warp == 0 && lane == 0) {
       for (int st = 0; st < kStages; ++st)
         if (armed_kv[st] >= 0)
