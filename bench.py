@@ -18,6 +18,13 @@ read of its outputs inside the timed region).
 
 --impl reference times the fp64 CPU oracle (the reference arm of this
 build) on a bounded sample of the same workload.
+
+With --gpus N > 1 (one process per GPU under torchrun) the step is the
+multi-GPU DCP step over one global batch ("Decode Context Parallelism",
+section 4.1): rank r holds shard r of every request's cache and query heads
+[r H/N, (r + 1) H/N); query all-gather, partial, head-sliced all-to-all of
+the partials, combine (strong scaling).  --independent runs N independent
+batches instead.
 """
 import argparse
 import hashlib
@@ -570,6 +577,151 @@ def run_sweep(args, dev, stream, barrier):
                       "warmup": args.warmup, "runs": rows}), flush=True)
 
 
+def dcp_rank_inputs(w, world, rank, device):
+    """Rank ``rank``'s inputs of a multi-GPU DCP step over the global workload
+    ``w``: its query heads [B, q_len, H/N, 576], the cache slice holding only
+    its shard's positions (the *_LOCAL layout), that slice's block table,
+    the global lengths and its heads' W_UV."""
+    import numpy as np
+    import torch
+    import mla_inputs as mi
+    H = w.num_heads
+    if H % world != 0:
+        raise ValueError(f"{H} heads do not split over {world} ranks")
+    Hl = H // world
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
+    d = mi.local_shard_cache(w, world, rank, w.layout, seed=rank)
+    if w.kv_dtype == "bf16":
+        kv = torch.from_numpy(d["kv"].view(np.int16)).view(torch.bfloat16)
+        sc = None
+    else:
+        kv = torch.from_numpy(d["kv"])
+        sc = torch.from_numpy(d["kv_scale"]).to(device)
+    w_uv = None
+    if w.w_uv is not None:
+        w_uv = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16)[
+            rank * Hl:(rank + 1) * Hl].contiguous().to(device)
+    return dict(q_local=q[:, :, rank * Hl:(rank + 1) * Hl].contiguous().to(device),
+                kv=kv.to(device), kv_scale=sc,
+                block_table=torch.from_numpy(d["block_table"]).to(device),
+                seq_lens=torch.from_numpy(w.seq_lens).to(device), w_uv_local=w_uv,
+                local_tokens=int(d["local_lens"].sum()))
+
+
+def dcp_exchange_bytes(w, world):
+    """Bytes one rank sends per DCP step: its query heads to every peer (the
+    all-gather) and, to every peer, that peer's head slice of its shard
+    partial (the all-to-all: 512 fp32 values and one LSE per row)."""
+    rows_l = w.batch * w.q_len * (w.num_heads // world)
+    return {"q_allgather_bytes_per_rank": (world - 1) * rows_l * 576 * 2,
+            "partial_alltoall_bytes_per_rank": (world - 1) * rows_l * (512 + 1) * 4}
+
+
+def run_dcp(args, world, rank, dist, device, workload=None, partial_fn=None, combine_fn=None):
+    """The multi-GPU DCP step ("Decode Context Parallelism", section 4.1) on
+    ``world`` ranks, one per GPU: rank r holds query heads
+    [r H/N, (r + 1) H/N) and shard r of every request's cache; a step is the
+    query all-gather, the rank's partial over its shard, the head-sliced
+    all-to-all of the partials and the combine of its heads.  The total work
+    is one global batch (strong scaling): value = the batch's KV bytes / the
+    step time (max over ranks).  Returns the JSON line on rank 0 (None
+    elsewhere).  ``workload``, ``partial_fn``, ``combine_fn`` and a CPU
+    ``device`` are for tests of this host logic on gloo ranks."""
+    import torch
+    from sequence_sharded_mla_gb300 import dcp
+    import mla_inputs as mi
+    w = workload if workload is not None else rank_workload(args.config, 0, args.requests)
+    w.layout = args.layout or w.layout
+    inp = dcp_rank_inputs(w, world, rank, device)
+    cuda = device.type == "cuda"
+
+    def step():
+        return dcp.dcp_decode_step(inp["q_local"], inp["kv"], inp["block_table"],
+                                   inp["seq_lens"], layout=w.layout, kv_scale=inp["kv_scale"],
+                                   causal=w.causal, softmax_scale=w.softmax_scale,
+                                   w_uv_local=inp["w_uv_local"], partial_fn=partial_fn,
+                                   combine_fn=combine_fn, chunks=args.dcp_chunks)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        if cuda:
+            torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        result = step()
+    clk = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    clocks = ClockSampler(device.index) if cuda else None
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    if cuda:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            result = step()
+        t1.record()
+        barrier()
+        elapsed = t0.elapsed_time(t1) / 1e3
+    else:
+        c0 = time.perf_counter()
+        for _ in range(args.steps):
+            result = step()
+        barrier()
+        elapsed = time.perf_counter() - c0
+    if clocks is not None:
+        clk = clocks.stop()
+    # the rank's partial kernel alone, from an untimed profiled step
+    kernel_ms = None
+    if cuda and partial_fn is None:
+        import sequence_sharded_mla_gb300 as mla
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        mla.mla_set_profile_events(e0, e1)
+        step()
+        mla.mla_set_profile_events(None, None)
+        barrier()
+        kernel_ms = e0.elapsed_time(e1)
+    local_kv = inp["local_tokens"] * (1152 if w.kv_dtype == "bf16" else 580)
+    (elapsed, kms), _ = reduce_over_ranks(dist, [elapsed, kernel_ms or 0.0], 0,
+                                          device if cuda else torch.device("cpu"))
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    ms = elapsed / args.steps * 1e3
+    name = f"{w.name}-dcp{world}-{w.layout}"
+    line = {
+        "metric": METRIC, "value": w.kv_bytes() * args.steps / elapsed / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
+        "config": {"workload": name, "batch": w.batch, "heads": w.num_heads, "q_len": w.q_len,
+                   "num_shards": world, "layout": w.layout, "kv_dtype": w.kv_dtype,
+                   "total_kv_bytes": w.kv_bytes(), "kv_bytes_rank0": local_kv,
+                   "l2": "inputs larger than L2" if w.kv_bytes() > 4 * L2_BYTES else
+                         "inputs not flushed from L2",
+                   "parallelism": f"dcp{world}: one sequence shard per GPU, query all-gather, "
+                                  "head-sliced all-to-all of the partials, combine per head "
+                                  f"slice; {args.dcp_chunks} request group(s) whose exchange "
+                                  "overlaps the next group's partial"},
+        "exchange": dict(dcp_exchange_bytes(w, world), chunks=args.dcp_chunks,
+                         step_ms=ms, partial_kernel_ms_max=kms if kernel_ms is not None else None,
+                         outside_partial_kernel_ms=(ms - kms) if kernel_ms is not None else None),
+        "clocks": clk,
+    }
+    if kernel_ms is not None:
+        achieved = local_kv / (kms / 1e3) / 1e9
+        line["roofline"] = {"kernel": "mla_partial_kernel<true>" if w.kv_dtype == "bf16"
+                            else "mla_partial_fp8_kernel<true>", "bound": "hbm",
+                            "achieved": achieved, "peak": peak, "unit": "GB/s",
+                            "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                            "traffic": None}
+    line["gpu_launches"] = 4 * args.dcp_chunks * args.steps   # plan, partial, merge, combine
+    return line
+
+
 def run_gpu(args, world, rank, local, dist):
     import torch
 
@@ -589,6 +741,13 @@ def run_gpu(args, world, rank, local, dist):
         if args.config != 3 or world != 1:
             raise SystemExit("--sweep is the shard-count sweep of --config 3 on one GPU")
         run_sweep(args, dev, stream, barrier)
+        return
+    if (world > 1 and not args.independent) or args.dcp:
+        if args.config == GQA_CONFIG:
+            raise SystemExit("the DCP step runs the MLA configurations")
+        line = run_dcp(args, world, rank, dist, dev)
+        if line is not None:
+            print(json.dumps(line), flush=True)
         return
     # per timed step: events at its start, around the partial kernel
     # (recorded by the library itself) and at its end
@@ -714,6 +873,14 @@ def main():
                     help="override the configuration's logical shard count (1..8)")
     ap.add_argument("--layout", default="", choices=["", "interleaved", "contiguous"],
                     help="override the configuration's shard layout")
+    ap.add_argument("--independent", action="store_true",
+                    help="with --gpus N > 1: N independent batches (no exchange) instead of "
+                         "the DCP step over one global batch")
+    ap.add_argument("--dcp", action="store_true",
+                    help="run the DCP step also at --gpus 1 (an exchange-free check of its path)")
+    ap.add_argument("--dcp-chunks", type=int, default=2,
+                    help="DCP step: request groups whose exchange overlaps the next group's "
+                         "partial attention")
     ap.add_argument("--sweep", action="store_true",
                     help="with --config 3: the shard-count sweep, N = 1, 2, 4, 8 in both "
                          "layouts over one seeded cache (one JSON line with a table)")
