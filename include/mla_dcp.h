@@ -62,7 +62,7 @@ typedef enum mla_status {
 
 /* Which token positions of a request belong to shard s of N
  * ("Decode Context Parallelism", section 4):
- *   INTERLEAVED  t mod N == s                  (N must divide 64)
+ *   INTERLEAVED  t mod N == s                  (any N <= 8)
  *   CONTIGUOUS   s*c <= t < min((s+1)*c, L),   c = ceil(L / N)
  * The section's worked example (a 200K-token request on 4 GPUs holding
  * 0-50K, 50K-100K, 100K-150K, 150K-200K) is the CONTIGUOUS layout.

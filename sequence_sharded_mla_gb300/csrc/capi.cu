@@ -159,7 +159,6 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
     return MLA_ERR_INVALID;
   }
   if (shape->num_heads % 16 != 0) return MLA_ERR_UNSUPPORTED;
-  if (layout == MLA_LAYOUT_INTERLEAVED && kPage % num_shards != 0) return MLA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kv->data) || !aligned16(out_partial) ||
       !aligned16(lse_partial) || !aligned4(block_table) || !aligned4(seq_lens) ||
       !aligned4(shape->q_lens))
@@ -188,6 +187,21 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
                   ? kInterleaved
                   : kContiguous;
   pd.local = local ? 1 : 0;
+  // interleaved shards of a whole-request cache: pages per tile and slots
+  // per page (padded when N does not divide 64)
+  pd.ppt = 1;
+  pd.spp_log2 = 6;
+  pd.pad = 0;
+  if (layout == MLA_LAYOUT_INTERLEAVED) {
+    if (kPage % num_shards == 0) {
+      pd.ppt = num_shards;
+      pd.spp_log2 = num_shards == 1 ? 6 : num_shards == 2 ? 5 : num_shards == 4 ? 4 : 3;
+    } else {
+      pd.pad = 1;
+      pd.ppt = num_shards == 3 ? 2 : 4;
+      pd.spp_log2 = num_shards == 3 ? 5 : 4;
+    }
+  }
   pd.causal = shape->causal;
   pd.num_pages = kv->num_pages;
   pd.max_pages = max_pages_per_req;
@@ -226,7 +240,8 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
   // and lands the residue's 64/nv rows of a page in the kernels'
   // shared-memory layouts: all 9 chunks of each 8-slot group in one box
   // (fp8), or three chunks per box, one box per chunk group (bf16).
-  const int nv = (pd.layout == kInterleaved && !pd.local) ? num_shards : 1;
+  // nv pages per tile, 64 / nv slots per page (padded for N not dividing 64)
+  const int nv = pd.ppt;
   const bool fp8 = kv->dtype == MLA_KV_FP8_E4M3;
   CUtensorMap tm_q8;
   if (fp8) {
@@ -246,16 +261,34 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
     // all nine chunks, in the group-major layout of the fp8 kernel.  No L2
     // promotion: a 576-byte row is 18 whole sectors, and promotion to 128
     // bytes would fetch 640
-    cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
-                          (cuuint64_t)kv->num_pages * kPage};
-    cuuint64_t strides[4] = {(cuuint64_t)kDqk * nv, 64, (cuuint64_t)kDqk * 8 * nv,
-                             (cuuint64_t)kDqk};
-    cuuint32_t box[5] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kPage / 8 / nv), 1};
-    cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MLA_ERR_CUDA;
+    if (pd.pad) {
+      // N does not divide 64: view (64 codes, row in page, chunk, page) with
+      // strides (-, 576, 64, 36864); a box of 8 N rows traversed with stride
+      // N lands one 8-slot group (4608 bytes), and rows past the page's end
+      // are outside the view and fill zeros
+      cuuint64_t pdims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)kChunks,
+                             (cuuint64_t)kv->num_pages};
+      cuuint64_t pstrides[3] = {(cuuint64_t)kDqk, 64, (cuuint64_t)kDqk * kPage};
+      cuuint32_t pbox[4] = {64, (cuuint32_t)(8 * num_shards), (cuuint32_t)kChunks, 1};
+      cuuint32_t pes[4] = {1, (cuuint32_t)num_shards, 1, 1};
+      if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(kv->data), pdims,
+                 pstrides, pbox, pes, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_CUDA;
+    } else {
+      cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
+                            (cuuint64_t)kv->num_pages * kPage};
+      cuuint64_t strides[4] = {(cuuint64_t)kDqk * nv, 64, (cuuint64_t)kDqk * 8 * nv,
+                               (cuuint64_t)kDqk};
+      cuuint32_t box[5] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kPage / 8 / nv), 1};
+      cuuint32_t es[5] = {1, 1, 1, 1, 1};
+      if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(kv->data), dims,
+                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_CUDA;
+    }
   } else {
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)(kPage / 8 / nv),
                           (cuuint64_t)kv->num_pages * kPage};
@@ -263,10 +296,27 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
                              (cuuint64_t)kDqk * 2};
     cuuint32_t box[5] = {64, 8, (cuuint32_t)kCgChunks, (cuuint32_t)(kPage / 8 / nv), 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (pd.pad) {
+      // N does not divide 64: view (64 dims, row in page, chunk, page) with
+      // strides (-, 1152, 128, 73728); a box of 8 N rows traversed with
+      // stride N and three chunks lands one 8-slot group of a chunk group
+      // (3072 bytes), and rows past the page's end fill zeros
+      cuuint64_t pdims[4] = {64, (cuuint64_t)kPage, (cuuint64_t)kChunks,
+                             (cuuint64_t)kv->num_pages};
+      cuuint64_t pstrides[3] = {(cuuint64_t)kDqk * 2, 128, (cuuint64_t)kDqk * 2 * kPage};
+      cuuint32_t pbox[4] = {64, (cuuint32_t)(8 * num_shards), (cuuint32_t)kCgChunks, 1};
+      cuuint32_t pes[4] = {1, (cuuint32_t)num_shards, 1, 1};
+      if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv->data),
+                 pdims, pstrides, pbox, pes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MLA_ERR_CUDA;
+    } else if (encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data),
+                      dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
       return MLA_ERR_CUDA;
+    }
     // the same view with all nine chunks in one box, for the L2 prefetch
     box[2] = (cuuint32_t)kChunks;
     if (encode(&tm_kv_pf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv->data), dims,

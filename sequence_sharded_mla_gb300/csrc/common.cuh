@@ -66,6 +66,15 @@ struct ProblemDesc {
   int causal;
   int num_pages;
   int max_pages;
+  // Interleaved shards of a whole-request cache: a tile of shard s covers
+  // ppt consecutive pages of the request, and page k's rows of the shard
+  // (r_k, r_k + N, ..., r_k = (s - 64 k) mod N) take 2^spp_log2 slots.  When
+  // N divides 64, ppt = N and 2^spp_log2 = 64 / N exactly; otherwise (pad = 1)
+  // the slots per page are padded (N = 3: 32 slots, 22 rows; N = 5..7: 16
+  // slots, 13..10 rows) and slots past a page's rows hold no token.
+  int ppt;
+  int spp_log2;
+  int pad;
   float scale_log2;    // softmax scale * log2(e)
   const int32_t* block_table;  // [B, max_pages]
   const int32_t* seq_lens;     // [B]
@@ -203,11 +212,17 @@ inline cudaLaunchAttribute pdl_attribute() {
   return a;
 }
 
-// kLocal: whether the cache is a local slice (pd.local), fixed at compile time
-// (0 or 1) in the partial kernel, read at run time (-1) elsewhere.
+// kLocal: the cache kind, fixed at compile time in the partial kernels --
+// 0: whole requests, 1: a local slice (pd.local), 2: whole requests with
+// interleaved shards whose count does not divide the page (pd.pad) -- and
+// read at run time (-1) elsewhere.
 template <int kLocal>
 __device__ __forceinline__ bool is_local(const ProblemDesc& pd) {
-  return kLocal < 0 ? pd.local != 0 : kLocal != 0;
+  return kLocal < 0 ? pd.local != 0 : kLocal == 1;
+}
+template <int kLocal>
+__device__ __forceinline__ bool is_pad(const ProblemDesc& pd) {
+  return kLocal < 0 ? pd.pad != 0 : kLocal == 2;
 }
 
 template <int kLocal = -1>
@@ -230,7 +245,12 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
   if (x.rows == 0) L = 0;   // only padding rows: nothing to attend
   if (pd.layout == kInterleaved) {
     int n_local = L > x.s ? (L - 1 - x.s) / pd.num_shards + 1 : 0;
-    x.tiles = ceil_div(n_local, kTile);
+    if (is_pad<kLocal>(pd)) {
+      // tiles up to the page of the shard's last position
+      x.tiles = n_local > 0 ? ((x.s + pd.num_shards * (n_local - 1)) / kPage) / pd.ppt + 1 : 0;
+    } else {
+      x.tiles = ceil_div(n_local, kTile);
+    }
   } else {
     int c = ceil_div(L, pd.num_shards);
     x.tstart = x.s * c;
@@ -251,9 +271,27 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
 // shards: tile j holds the shard's positions 64j..64j+63 (in a local cache,
 // exactly local page j).  Contiguous shards: tile j is global page p0 + j, or
 // local page j of a local cache.
+// The first row of shard s in page `page` of an interleaved whole-request
+// cache: (s - 64 page) mod N.
+__host__ __device__ __forceinline__ int shard_row0(int s, int page, int n) {
+  const int v = (s - (kPage % n) * (page % n)) % n;
+  return v < 0 ? v + n : v;
+}
+
+// A position past every context: the slot holds no token.
+constexpr int kNoToken = 0x3fffffff;
+
 template <int kLocal = -1>
 __device__ __forceinline__ int slot_token(const ProblemDesc& pd, const Unit& x, int j, int a) {
-  if (pd.layout == kInterleaved) return (j * kTile + a) * pd.num_shards + x.s;
+  if (pd.layout == kInterleaved) {
+    if (is_pad<kLocal>(pd)) {
+      const int page = pd.ppt * j + (a >> pd.spp_log2);
+      const int row = shard_row0(x.s, page, pd.num_shards) +
+                      pd.num_shards * (a & ((1 << pd.spp_log2) - 1));
+      return row < kPage ? page * kPage + row : kNoToken;
+    }
+    return (j * kTile + a) * pd.num_shards + x.s;
+  }
   if (is_local<kLocal>(pd)) return x.tstart + j * kTile + a;
   return (x.p0 + j) * kPage + a;
 }

@@ -118,7 +118,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-template <bool kLocal>
+template <int kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv,
@@ -194,15 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     // Lane k < nv issues the boxes of page k of the tile; lane 0 arms each
     // group barrier with the group's whole byte count first.
-    // page boxes per tile: N pages' residue rows for interleaved shards of a
-    // global cache, otherwise one whole page
-    const int nv = (pd.layout == kInterleaved && !kLocal) ? pd.num_shards : 1;
+    // page boxes per tile: the shard's rows of ppt pages for interleaved
+    // shards of a global cache (ppt = N when N divides 64), otherwise one
+    // whole page
+    const int nv = (pd.layout == kInterleaved && kLocal != 1) ? pd.ppt : 1;
     const int box_bytes = kCgBytes / nv;     // one chunk group of one page's slots
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
-      const int npages_b = kLocal ? x.tiles : ceil_div(x.L, kPage);   // block-table entries
+      const int npages_b = kLocal == 1 ? x.tiles : ceil_div(x.L, kPage);   // block-table entries
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
       const int res = nv > 1 ? x.s : 0;
       int win_base = -1, win_val = -1;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stages, an SM's own loads keep too few bytes in flight to cover
         // the DRAM latency; a stage load then reads L2
         for (int jp = (j == t0 ? j + 1 : j + kPrefetch); jp <= j + kPrefetch && jp < t1; ++jp) {
-          const int fs = nv > 1 ? jp * nv : (kLocal || pd.layout == kInterleaved ? jp : x.p0 + jp);
+          const int fs = nv > 1 ? jp * nv : (kLocal == 1 || pd.layout == kInterleaved ? jp : x.p0 + jp);
           const int pwb = fs & ~31;
           if (pwb != pwin_base && fs < npages_b) {
             pwin_base = pwb;
@@ -224,12 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pg = __shfl_sync(0xffffffffu, pwin_val, pidx & 31);
           // one box per page: the prefetch needs no chunk-group barriers,
           // and every TMA box costs issue throughput
-          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages)
+          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages && kLocal != 2)
             tma_prefetch_l2_5d(&tm_kv_pf, 0, 0, 0, 0, pg * kPage + res);
         }
         // page slot of this lane's box; nv divides 32, so a tile never
         // straddles two 32-entry windows of the block table
-        const int first_slot = nv > 1 ? j * nv : (kLocal || pd.layout == kInterleaved ? j : x.p0 + j);
+        const int first_slot = nv > 1 ? j * nv : (kLocal == 1 || pd.layout == kInterleaved ? j : x.p0 + j);
         const int wb = first_slot & ~31;
         if (wb != win_base && first_slot < npages_b) {
           win_base = wb;
@@ -255,7 +256,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed_kv[st] = gt;
         }
         __syncwarp();
-        if (lane < nv) {
+        if (kLocal == 2) {
+          // N does not divide 64: lane k*gpp + g (gpp = 8-slot groups per
+          // page) loads group g of page k of the tile, rows r_k + 8 N g +
+          // N i (i < 8) of the (64 dims, row in page, chunk, page) view with
+          // traversal stride N along the rows, so rows past the page's end
+          // are out of the view and fill zeros.  One box is one 8-slot group
+          // of a chunk group (3072 bytes).
+          const int gpp_log2 = pd.spp_log2 - 3;
+          const int k = lane >> gpp_log2, g = lane & ((1 << gpp_log2) - 1);
+          const int pgk = __shfl_sync(0xffffffffu, page, k & 31);
+          if (lane < 8) {
+            const int r0 = shard_row0(x.s, first_slot + k, pd.num_shards) + 8 * pd.num_shards * g;
+#pragma unroll
+            for (int cg = 0; cg < kCg; ++cg)
+              tma_load_4d(sKV + st * kTileBytes + cg * kCgBytes + lane * kGroupBytes, &tm_kv,
+                          full + 8 * cg, 0, r0, kCgChunks * cg, pgk);
+          }
+        } else if (lane < nv) {
           // cache row page*64 + res of the (row-in-group, chunk, group, row)
           // view; a page of num_pages is out of range and fills zeros.  The
           // chunk groups go out in order, each on its own barrier, so QK^T
@@ -618,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-template <bool kLocal>
+template <int kLocal>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                   cudaStream_t stream) {
@@ -636,13 +654,15 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
   return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, tm_kv_pf, p);
 }
 
-// The cache kind (local slice or whole requests) is a template parameter:
-// branching on it at run time cost about 2% on the bimodal batch.
+// The cache kind (whole requests, a local slice, or whole requests with
+// interleaved shards whose count does not divide the page) is a template
+// parameter: branching on it at run time cost about 2% on the bimodal batch.
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                 cudaStream_t stream) {
-  return p.pd.local ? launch_partial<true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
-                    : launch_partial<false>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
+  return p.pd.local ? launch_partial<1>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
+         : p.pd.pad   ? launch_partial<2>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
+                      : launch_partial<0>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
 }
 
 }  // namespace mla

@@ -130,7 +130,7 @@ __device__ __forceinline__ uint32_t row_scale_exp(uint32_t max_bits) {
 
 }  // namespace
 
-template <bool kLocal>
+template <int kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_fp8_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_kv, PartialParams p) {
@@ -207,17 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // nv page boxes per tile: N pages' residue rows for interleaved shards of
-    // a global cache, otherwise one whole page.  Lane k < nv issues box k;
-    // every lane copies the scales of token slots lane and lane + 32.
-    const int nv = (pd.layout == kInterleaved && !kLocal) ? pd.num_shards : 1;
-    const int lg_rows = 6 - (nv == 1 ? 0 : nv == 2 ? 1 : nv == 4 ? 2 : 3);   // log2(64 / nv)
+    // nv page boxes per tile: the shard's rows of ppt pages for interleaved
+    // shards of a global cache (ppt = N when N divides 64), otherwise one
+    // whole page.  Lane k < nv issues box k; every lane copies the scales of
+    // token slots lane and lane + 32.
+    const bool shard_rows = pd.layout == kInterleaved && kLocal != 1;
+    const int nv = shard_rows ? pd.ppt : 1;
+    const int lg_rows = shard_rows ? pd.spp_log2 : 6;   // log2(slots per page)
+    const int rstride = shard_rows ? pd.num_shards : 1;  // cache rows between slots
     const int box_bytes = kStageBytes / nv;
     int gt = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
       Unit x = make_unit<kLocal>(pd, unit);
-      const int npages_b = kLocal ? x.tiles : ceil_div(x.L, kPage);
+      const int npages_b = kLocal == 1 ? x.tiles : ceil_div(x.L, kPage);
       const int32_t* bt = pd.block_table + (size_t)x.b * pd.max_pages;
       const int res = nv > 1 ? x.s : 0;
       int win_base = -1, win_val = -1;
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows of each page, and the lines of the page's token scales), so
         // that a stage load mostly reads L2
         for (int jp = (j == t0 ? j + 1 : j + kPrefetch); jp <= j + kPrefetch && jp < t1; ++jp) {
-          const int fs = nv > 1 ? jp * nv : (kLocal || pd.layout == kInterleaved ? jp : x.p0 + jp);
+          const int fs = nv > 1 ? jp * nv : (kLocal == 1 || pd.layout == kInterleaved ? jp : x.p0 + jp);
           const int pwb = fs & ~31;
           if (pwb != pwin_base && fs < npages_b) {
             pwin_base = pwb;
@@ -237,13 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int pidx = fs + lane;
           const int pg = __shfl_sync(0xffffffffu, pwin_val, pidx & 31);
-          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages) {
+          if (lane < nv && pidx < npages_b && pg >= 0 && pg < pd.num_pages && kLocal != 2) {
             tma_prefetch_l2_5d(&tm_kv, 0, 0, 0, 0, pg * kPage + res);
             prefetch_l2(p.kv_scale + (size_t)pg * kPage);
             prefetch_l2(p.kv_scale + (size_t)pg * kPage + 32);
           }
         }
-        const int first_slot = nv > 1 ? j * nv : (kLocal || pd.layout == kInterleaved ? j : x.p0 + j);
+        const int first_slot = nv > 1 ? j * nv : (kLocal == 1 || pd.layout == kInterleaved ? j : x.p0 + j);
         const int wb = first_slot & ~31;
         if (wb != win_base && first_slot < npages_b) {
           win_base = wb;
@@ -263,9 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int a = lane + 32 * h;
           const int k = a >> lg_rows;
           const int pg = __shfl_sync(0xffffffffu, page, k);
-          const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages;
-          scale_src[h] = p.kv_scale +
-                         (okpg ? (size_t)pg * kPage + (a & ((1 << lg_rows) - 1)) * nv + res : 0);
+          const int row = (kLocal == 2 ? shard_row0(x.s, first_slot + k, pd.num_shards) : res) +
+                          (a & ((1 << lg_rows) - 1)) * rstride;
+          // a slot past its page's rows holds no token: any valid address
+          const bool okpg = first_slot + k < npages_b && pg >= 0 && pg < pd.num_pages &&
+                            row < kPage;
+          scale_src[h] = p.kv_scale + (okpg ? (size_t)pg * kPage + row : 0);
         }
         if (gt >= kStages) {
           ok = __all_sync(0xffffffffu, mbar_wait(b_kv_empty + 8 * st, ((gt >> 2) - 1) & 1, tmo,
@@ -278,9 +284,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed_kv[st] = gt;
         }
         __syncwarp();
-        if (lane < nv)
+        if (kLocal == 2) {
+          // N does not divide 64: lane k*gpp + g loads 8-slot group g of
+          // page k, rows r_k + 8 N g + N i of the (64 codes, row in page,
+          // chunk, page) view with traversal stride N along the rows: rows
+          // past the page's end are out of the view and fill zeros
+          const int gpp_log2 = pd.spp_log2 - 3;
+          const int k = lane >> gpp_log2, g = lane & ((1 << gpp_log2) - 1);
+          const int pgk = __shfl_sync(0xffffffffu, page, k & 31);
+          if (lane < 8)
+            tma_load_4d(sKV + st * kStageBytes + lane * kGroupBytes, &tm_kv, full, 0,
+                        shard_row0(x.s, first_slot + k, pd.num_shards) + 8 * pd.num_shards * g,
+                        0, pgk);
+        } else if (lane < nv) {
           tma_load_5d(sKV + st * kStageBytes + lane * box_bytes, &tm_kv, full, 0, 0, 0, 0,
                       page * kPage + res);
+        }
         cp_async_4(smem_u32(&misc->sigma[st][lane]), scale_src[0]);
         cp_async_4(smem_u32(&misc->sigma[st][lane + 32]), scale_src[1]);
         cp_async_mbar_arrive_noinc(full);
@@ -832,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kLocal>
+template <int kLocal>
 static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                            const PartialParams& p, int grid, cudaStream_t stream) {
   const cudaError_t e = host::ensure_dynamic_smem(
@@ -851,8 +870,9 @@ static cudaError_t launch_partial_fp8_impl(const CUtensorMap& tm_q, const CUtens
 
 cudaError_t launch_partial_fp8(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                const PartialParams& p, int grid, cudaStream_t stream) {
-  return p.pd.local ? launch_partial_fp8_impl<true>(tm_q, tm_kv, p, grid, stream)
-                    : launch_partial_fp8_impl<false>(tm_q, tm_kv, p, grid, stream);
+  return p.pd.local ? launch_partial_fp8_impl<1>(tm_q, tm_kv, p, grid, stream)
+         : p.pd.pad   ? launch_partial_fp8_impl<2>(tm_q, tm_kv, p, grid, stream)
+                      : launch_partial_fp8_impl<0>(tm_q, tm_kv, p, grid, stream);
 }
 
 }  // namespace mla

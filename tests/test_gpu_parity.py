@@ -52,20 +52,40 @@ def test_ragged_lengths(dev, H, layout):
     compare_all(w, dev)
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("layout", ["interleaved", "contiguous"])
 def test_shard_counts(dev, N, layout):
+    """Every shard count, both layouts.  Interleaved shard counts that do not
+    divide the page size (3, 5, 6, 7) take each page's rows of a shard as a
+    padded run of slots, loaded 8 rows at a time with the rows past the
+    page's end outside the load."""
     lens = [5, 700, 2049, 130]
     w = mi.build_workload("shards", len(lens), 1, 32, lens, N, layout, "bf16", False,
-                          seed=200 + N)
-    if layout == "interleaved" and 64 % N != 0:
-        # a whole-request cache interleaved over N shards needs N | 64 (one
-        # TMA box per page); such calls are refused before any launch
-        import sequence_sharded_mla_gb300 as mla
-        with pytest.raises(mla.MLAError) as e:
-            run_gpu(w, dev)
-        assert e.value.status == -2
-        return
+                          seed=200 + N, poison=True, extra_pages=2)
+    compare_all(w, dev)
+
+
+@pytest.mark.parametrize("N", [3, 5, 6, 7])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_interleaved_shard_counts_not_dividing_the_page(dev, N, kv_dtype):
+    """Long contexts (split units), causal verify rows, a context that ends
+    in the pool's last page, and NaN-poisoned rows everywhere outside the
+    contexts: interleaved shards whose count does not divide 64."""
+    lens = [1, 64, 65, 4000, 9001]
+    w = mi.build_workload("padded", len(lens), 2, 16, lens, N, "interleaved", kv_dtype, True,
+                          seed=260 + N, poison=True, kv_sigma=1.0 if kv_dtype == "fp8" else 0.5)
+    # make the last request's last page the pool's last page: swap the two
+    # physical pages' contents (poison included) along with their entries
+    last = w.kv.shape[0] - 1
+    b, k = len(lens) - 1, (lens[-1] - 1) // 64
+    other = int(w.block_table[b, k])
+    if other != last:
+        j = tuple(np.argwhere(w.block_table == last)[0])
+        w.block_table[j], w.block_table[b, k] = other, last
+        w.kv[[other, last]] = w.kv[[last, other]]
+        if w.kv_scale is not None:
+            w.kv_scale[[other, last]] = w.kv_scale[[last, other]]
+    assert int(w.block_table[b, k]) == last
     compare_all(w, dev)
 
 
@@ -146,9 +166,6 @@ def test_invalid_arguments_rejected_before_launch(dev):
     with pytest.raises(mla.MLAError) as e:
         mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 9)
     assert e.value.status == -1
-    with pytest.raises(mla.MLAError) as e:
-        mla.mla_decode_partial(t["q"], t["kv"], t["block_table"], t["seq_lens"], 3, "interleaved")
-    assert e.value.status == -2          # interleaved needs N | 64
     q20 = torch.zeros((1, 1, 20, 576), dtype=torch.bfloat16, device=dev)
     with pytest.raises(mla.MLAError) as e:
         mla.mla_decode_partial(q20, t["kv"], t["block_table"], t["seq_lens"], 2)
