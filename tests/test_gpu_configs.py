@@ -1,8 +1,11 @@
 """GPU parity at the full benchmark sizes, in the launch configuration the
 benchmark times.  The oracle computes sampled query rows one by one: the
 longest and shortest requests plus seeded random ones, every query position
-of the causal verify step at its ends, and the per-shard partials of those
-rows for every shard.
+of the causal verify step at its ends, one row of every work unit that the
+device's own work plan (read back from the workspace) splits across CTAs --
+so every split piece, boundary pieces included, is checked -- and the
+per-shard partials of those rows for every shard.  The whole decode step
+(mla_decode_step, the call the benchmark times) is checked on the same rows.
 """
 import numpy as np
 import pytest
@@ -32,6 +35,64 @@ def sample_rows(w, n_random=10, seed=0):
         for i in i_list:
             rows.append((b * q + i) * H + h)
     return np.unique(np.array(rows, dtype=np.int64))
+
+
+def split_unit_rows(w, workspace, n_out, seed=0):
+    """One seeded row of every work unit the device's plan splits across
+    CTAs.  The workspace starts with the plan's header (error word, total
+    positions, positions per CTA, grid, units, positions charged per unit)
+    and, 256 bytes in, the exclusive prefix of work positions over units."""
+    ws = workspace.cpu().numpy()
+    hdr = ws[:256].view(np.int32)
+    per, U, cost = int(hdr[2]), int(hdr[4]), int(hdr[5])
+    prefix = ws[256:256 + 4 * (U + 1)].view(np.int32)
+    R = w.q_len * w.num_heads
+    G = (R + 63) // 64
+    u64 = mi.u64(2000 + seed, 78, U)
+    rows = []
+    for u in range(U):
+        if prefix[u + 1] == prefix[u]:
+            continue
+        us, ue = prefix[u] + cost, prefix[u + 1]
+        if us // per == (ue - 1) // per:
+            continue
+        g = u % G
+        b = u // (G * n_out)
+        nrow = min(64, R - 64 * g)
+        rows.append(b * R + 64 * g + int(u64[u] % nrow))
+    return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def run_step(w, dev):
+    import torch
+    import sequence_sharded_mla_gb300 as mla
+    from _helpers import to_device
+    t = to_device(w, dev)
+    out, lse, ws = mla.mla_decode_step(t["q"], t["kv"], t["block_table"], t["seq_lens"],
+                                       w.num_shards, w.layout, kv_scale=t["kv_scale"],
+                                       causal=w.causal, softmax_scale=w.softmax_scale,
+                                       w_uv=t["w_uv"])
+    torch.cuda.synchronize()
+    assert mla.mla_get_device_error(ws) == 0
+    return out, lse, ws
+
+
+def check_step(w, dev, rows):
+    """The whole decode step on the sampled rows and one row of every unit
+    its own plan splits."""
+    out, lse, ws = run_step(w, dev)
+    rows = np.union1d(rows, split_unit_rows(w, ws, w.num_shards, seed=7))
+    R = w.batch * w.q_len * w.num_heads
+    ref, ref_lse = oracle.attend(w, shard=-1, rows=rows)
+    check_close(lse.cpu().numpy().reshape(R)[rows], ref_lse, TOL_LSE, "step lse")
+    if w.w_uv is not None:
+        ref_y = oracle.project_wuv(ref, (rows % w.num_heads).astype(np.int32), w.w_uv)
+        check_close(bf16_to_np(out).reshape(R, 128)[rows], ref_y, TOL_OUT, "step y",
+                    rel=REL_OUT)
+    else:
+        check_close(bf16_to_np(out).reshape(R, 512)[rows], ref, TOL_OUT, "step out",
+                    rel=REL_OUT)
+    return len(rows)
 
 
 def check_sampled(w, res, rows, N, layout):
@@ -65,7 +126,16 @@ def test_config2_bimodal_agentic(dev):
     w = mi.config_workload(2)
     res = run_gpu(w, dev)
     assert res["status"] == 0
-    check_sampled(w, res, sample_rows(w, seed=2), w.num_shards, w.layout)
+    rows = np.union1d(sample_rows(w, seed=2),
+                      split_unit_rows(w, res["workspace"], w.num_shards, seed=2))
+    check_sampled(w, res, rows, w.num_shards, w.layout)
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 5])
+def test_decode_step_full_size(dev, cfg):
+    w = mi.config_workload(cfg)
+    n = check_step(w, dev, sample_rows(w, n_random=6, seed=20 + cfg))
+    assert n >= 8
 
 
 @pytest.fixture(scope="module")
@@ -92,4 +162,6 @@ def test_config5_longtail_fp8_fused_wuv(dev):
     w = mi.config_workload(5)
     res = run_gpu(w, dev)
     assert res["status"] == 0
-    check_sampled(w, res, sample_rows(w, n_random=6, seed=5), w.num_shards, w.layout)
+    rows = np.union1d(sample_rows(w, n_random=6, seed=5),
+                      split_unit_rows(w, res["workspace"], w.num_shards, seed=5))
+    check_sampled(w, res, rows, w.num_shards, w.layout)
