@@ -21,6 +21,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "host_util.h"
 #include "ptx.cuh"
 
 namespace cg = cooperative_groups;
@@ -144,17 +145,13 @@ struct StepRows {
 // pieces.  Returns the unnormalised sum acc, M and wsum = sum of
 // exp(lse - M) over the warp's pieces (the same value in every lane).
 template <int kVec, int kB, class Src>
-__device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, int q0,
-                                             float4 (&acc)[kVec], float& M, float& wsum,
-                                             int part = 0, int nparts = 1) {
-  const typename Src::Ctx ctx = src.prepare(row, lane);
-  const int T = ctx.count;
+__device__ __forceinline__ void merge_pieces_ctx(const Src& src, const typename Src::Ctx& ctx,
+                                                 int lane, int q0, float4 (&acc)[kVec], float& M,
+                                                 float& wsum, int kbeg, int kend) {
 #pragma unroll
   for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   M = -CUDART_INF_F;
   float ws = 0.f;
-  const int kbeg = (int)((long long)T * part / nparts);
-  const int kend = (int)((long long)T * (part + 1) / nparts);
   for (int k0 = kbeg; k0 < kend; k0 += 32) {
     const float* p;
     float l;
@@ -207,6 +204,13 @@ __device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, 
   wsum = ws;
 }
 
+template <int kVec, int kB, class Src>
+__device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, int q0,
+                                             float4 (&acc)[kVec], float& M, float& wsum) {
+  const typename Src::Ctx ctx = src.prepare(row, lane);
+  merge_pieces_ctx<kVec, kB>(src, ctx, lane, q0, acc, M, wsum, 0, ctx.count);
+}
+
 // Two warps per query row, one per 256-wide half of the 512 latent dims (a
 // lane owns two float4 of its half, so each load instruction of a warp reads
 // 512 contiguous bytes), eight pieces in flight per batch; a block of 256
@@ -245,16 +249,25 @@ constexpr int kWuvRows = 8;            // query rows per cluster (one warp each)
 constexpr int kWuvSplit = 4;           // CTAs per cluster
 constexpr int kWuvDims = kDv / kWuvSplit;   // 128 latent dims per CTA
 
+// Dynamic shared memory of the W_UV combine kernel.
+template <class Src>
+struct WuvSmem {
+  uint16_t wsm[kWuvDims][kDuv];               // this CTA's 128 rows of W_UV[h] (32 KB)
+  float so[kWuvRows][kWuvDims];               // merged latent slice of each row
+  float yp[kWuvRows][kDuv];                   // this CTA's partial projection
+  float red[8][kWuvRows][kWuvDims];           // per warp and row: sum over its pieces
+  float rmax[8][kWuvRows], rsum[8][kWuvRows];
+  typename Src::Ctx ctx[kWuvRows][32];        // per row and lane: where its pieces live
+  int cnt[kWuvRows];                          // pieces of each row
+};
+
 template <class Src>
 __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
     mla_combine_wuv_kernel(Src src, int rows_per_head /* B*q_len */, int H,
                            const uint16_t* __restrict__ w_uv, uint16_t* __restrict__ y,
                            float* __restrict__ lse_out) {
-  __shared__ __align__(16) uint16_t wsm[kWuvDims][kDuv];   // 32 KB
-  __shared__ __align__(16) float so[kWuvRows][kWuvDims];   // merged latent slice
-  __shared__ __align__(16) float yp[kWuvRows][kDuv];       // this CTA's partial projection
-  __shared__ __align__(16) float red[8][kWuvDims];         // per-warp sums of a row's pieces
-  __shared__ float rsum[8], rmax[8];
+  extern __shared__ __align__(16) uint8_t wuv_smem_raw[];
+  WuvSmem<Src>& sm = *reinterpret_cast<WuvSmem<Src>*>(wuv_smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
   const int q = (int)cluster.block_rank();
   const int h = blockIdx.x / kWuvSplit;
@@ -263,48 +276,64 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
   {
     const uint4* wsrc =
         reinterpret_cast<const uint4*>(w_uv + ((size_t)h * kDv + (size_t)kWuvDims * q) * kDuv);
-    uint4* wdst = reinterpret_cast<uint4*>(&wsm[0][0]);
+    uint4* wdst = reinterpret_cast<uint4*>(&sm.wsm[0][0]);
     for (int i = tid; i < kWuvDims * kDuv / 8; i += 256) wdst[i] = __ldg(wsrc + i);
   }
   griddep_wait();                // the partials
   const int bi0 = rb * kWuvRows;
   const int nr = min(kWuvRows, rows_per_head - bi0);
-  // warps per row: with fewer rows than warps, a row's pieces are divided
-  // between several warps, whose sums are added in a fixed order below
-  const int wpr = nr > 4 ? 1 : nr > 2 ? 2 : nr > 1 ? 4 : 8;
+  // where every row's pieces live, one row per warp
+  if (warp < nr) {
+    sm.ctx[warp][lane] = src.prepare((bi0 + warp) * H + h, lane);
+    if (lane == 0) sm.cnt[warp] = sm.ctx[warp][lane].count;
+  }
+  __syncthreads();
   {
-    const int r = warp / wpr, part = warp % wpr;
-    float4 acc[1] = {make_float4(0.f, 0.f, 0.f, 0.f)};
-    float M = -CUDART_INF_F, wsum = 0.f;
-    if (r < nr)
-      merge_pieces<1, 16>(src, (bi0 + r) * H + h, lane, kWuvDims / 4 * q, acc, M, wsum, part,
-                          wpr);
-    *reinterpret_cast<float4*>(&red[warp][4 * lane]) = acc[0];
-    if (lane == 0) {
-      rsum[warp] = wsum;
-      rmax[warp] = M;
+    // The rows' pieces, concatenated in row order, are divided evenly over
+    // the 8 warps: a long request's row (dozens of pieces) is merged by
+    // several warps at once instead of one round trip after another.
+    int total = 0;
+    for (int r = 0; r < nr; ++r) total += sm.cnt[r];
+    const int lo = (int)((long long)total * warp / 8), hi = (int)((long long)total * (warp + 1) / 8);
+    int base = 0;
+    for (int r = 0; r < kWuvRows; ++r) {
+      const int c = r < nr ? sm.cnt[r] : 0;
+      const int k0 = max(lo, base) - base, k1 = min(hi, base + c) - base;
+      float M = -CUDART_INF_F, wsum = 0.f;
+      float4 acc[1] = {make_float4(0.f, 0.f, 0.f, 0.f)};
+      if (k0 < k1) {
+        const typename Src::Ctx ctx = sm.ctx[r][lane];
+        merge_pieces_ctx<1, 8>(src, ctx, lane, kWuvDims / 4 * q, acc, M, wsum, k0, k1);
+      }
+      *reinterpret_cast<float4*>(&sm.red[warp][r][4 * lane]) = acc[0];
+      if (lane == 0) {
+        sm.rmax[warp][r] = M;
+        sm.rsum[warp][r] = wsum;
+      }
+      base += c;
     }
   }
   __syncthreads();
   {
-    // row r's merged slice: its warps' parts brought to the row's largest
-    // maximum and added in order, normalised
+    // row r's merged slice: the warps' parts brought to the row's largest
+    // maximum and added in warp order, normalised
     const int r = warp;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r < nr) {
       float M = -CUDART_INF_F;
-      for (int pp = 0; pp < wpr; ++pp) M = fmaxf(M, rmax[r * wpr + pp]);
+      for (int w = 0; w < 8; ++w) M = fmaxf(M, sm.rmax[w][r]);
       float ws = 0.f;
       if (M > -CUDART_INF_F) {
-        for (int pp = 0; pp < wpr; ++pp) {
-          const float mp = rmax[r * wpr + pp];
-          const float sc = mp == -CUDART_INF_F ? 0.f : __expf(mp - M);
-          const float4 a = *reinterpret_cast<const float4*>(&red[r * wpr + pp][4 * lane]);
+        for (int w = 0; w < 8; ++w) {
+          const float mp = sm.rmax[w][r];
+          if (mp == -CUDART_INF_F) continue;
+          const float sc = __expf(mp - M);
+          const float4 a = *reinterpret_cast<const float4*>(&sm.red[w][r][4 * lane]);
           v.x = fmaf(sc, a.x, v.x);
           v.y = fmaf(sc, a.y, v.y);
           v.z = fmaf(sc, a.z, v.z);
           v.w = fmaf(sc, a.w, v.w);
-          ws = fmaf(sc, rsum[r * wpr + pp], ws);
+          ws = fmaf(sc, sm.rsum[w][r], ws);
         }
       }
       const float inv = ws > 0.f ? 1.0f / ws : 0.f;
@@ -312,7 +341,7 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
       if (lse_out != nullptr && q == 0 && lane == 0)
         lse_out[(bi0 + r) * H + h] = ws > 0.f ? M + __logf(ws) : -CUDART_INF_F;
     }
-    *reinterpret_cast<float4*>(&so[r][4 * lane]) = v;
+    *reinterpret_cast<float4*>(&sm.so[r][4 * lane]) = v;
   }
   __syncthreads();
   {
@@ -321,12 +350,12 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
     float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int d = 0; d < kWuvDims; ++d) {
-      const float w = __uint_as_float(((uint32_t)wsm[d][c]) << 16);
+      const float w = __uint_as_float(((uint32_t)sm.wsm[d][c]) << 16);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = fmaf(so[4 * rh + r][d], w, a[r]);
+      for (int r = 0; r < 4; ++r) a[r] = fmaf(sm.so[4 * rh + r][d], w, a[r]);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) yp[4 * rh + r][c] = a[r];
+    for (int r = 0; r < 4; ++r) sm.yp[4 * rh + r][c] = a[r];
   }
   cluster.sync();                // every CTA's partial projection is complete
   {
@@ -336,7 +365,7 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
       float v = 0.f;
 #pragma unroll
       for (int qq = 0; qq < kWuvSplit; ++qq) {
-        const float* peer = cluster.map_shared_rank(&yp[0][0], qq);
+        const float* peer = cluster.map_shared_rank(&sm.yp[0][0], qq);
         v += peer[r * kDuv + c];
       }
       __nv_bfloat16 b = __float2bfloat16_rn(v);
@@ -363,9 +392,14 @@ template <class Src>
 cudaError_t launch_combine_wuv_impl(const Src& src, int rows_per_head, int H,
                                     const uint16_t* w_uv, uint16_t* y, float* lse_out,
                                     cudaStream_t stream) {
+  const int smem = (int)sizeof(WuvSmem<Src>);
+  const cudaError_t e = host::ensure_dynamic_smem(
+      reinterpret_cast<const void*>(&mla_combine_wuv_kernel<Src>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(H * kWuvSplit, ceil_div(rows_per_head, kWuvRows));
   cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
