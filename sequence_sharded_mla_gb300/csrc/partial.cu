@@ -8,11 +8,12 @@
 // each rank attends over its local latent slice; partial outputs and LSEs are
 // merged afterwards).
 //
-// Data flow per persistent CTA (one per SM, 352 threads):
+// Data flow per persistent CTA (one per SM, 256 threads):
 //   warp 0      producer: block-table lookups; TMA loads of the query group
 //               (64 rows x 576, once per piece) and of 64-token KV tiles
 //               (one box per page and chunk group, 128-byte swizzle) into
-//               two stages; a stage is refilled as soon as its P.V is done.
+//               two stages; each chunk group of a stage is refilled as soon
+//               as the P.V blocks that read it are done.
 //               The next tile of the piece is prefetched into L2 (TMA
 //               prefetch, no shared memory) when a tile's load is issued:
 //               the two stages alone keep too few bytes in flight to cover
@@ -34,10 +35,11 @@
 //               chunk group at a time as each lands.  One thread issues a
 //               tcgen05.mma about every 40 cycles, so these small MMAs need
 //               several issuing warps.
-//   warps 7..10 P.V issuers: warp 7 + b issues latent block b of O^T += V^T P^T
+//   warp 7      P.V issuer: latent blocks 0..3 of O^T += V^T P^T in order
 //               (M=128 latent dims, N=rows, K=64 tokens) the moment the
 //               tile's probabilities are ready, into a TMEM accumulator of
-//               4 x 64 columns; the stage is free when all four are done.
+//               4 x 64 columns; chunk group c of the stage is free once
+//               block c + 1 is done.
 //   warps 2..5  softmax: two threads per query row (32 logits each) read S
 //               from TMEM, mask, keep the running max / sum and write bf16
 //               probabilities into the tile's own rope-chunk slot (free once
@@ -60,9 +62,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 256;
 constexpr int kIssuers = 2;                // QK^T-issuing warps (1 and 6)
-constexpr int kPvIssuers = 4;              // P.V-issuing warps (7..10), one latent block each
+constexpr int kPvIssuers = 1;              // P.V-issuing warp (7): the four latent blocks in order
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kBarSoftmax = 1;        // named barrier id for the softmax warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -70,7 +72,7 @@ constexpr int kSoftmaxWarps = 4;
 constexpr int kPrefetch = 1;               // tiles of a piece prefetched into L2 ahead of the stage loads
 
 struct Misc {
-  uint64_t kv_full[2 * 3], kv_empty[2];   // kv_full: per stage, one per chunk group
+  uint64_t kv_full[2 * 3], kv_empty[2 * 3];   // per stage, one per chunk group
   uint64_t s_full[2], s_empty[2];
   // per-stage barriers: the softmax may run up to two tiles ahead of P.V, so a
   // single barrier could complete two phases between tests and alias parities
@@ -154,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < 2; ++st) {
-      for (int cg = 0; cg < kCg; ++cg) mbar_init(b_kv_full + 8 * (kCg * st + cg), 1);
-      mbar_init(b_kv_empty + 8 * st, kPvIssuers);
+      for (int cg = 0; cg < kCg; ++cg) {
+        mbar_init(b_kv_full + 8 * (kCg * st + cg), 1);
+        mbar_init(b_kv_empty + 8 * (kCg * st + cg), 1);
+      }
       mbar_init(b_s_full + 8 * st, kIssuers);
       mbar_init(b_s_empty + 8 * st, kSoftmaxWarps);
       mbar_init(b_p_full + 8 * st, kSoftmaxWarps);
@@ -186,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   PieceIter it;
   it.init(p.prefix, U, lo, hi, p.hdr->unit_cost);
-  int armed_kv[2] = {-1, -1}, armed_q = -1;  // producer: last armed phase per barrier
+  // producer: last armed phase per chunk-group barrier of each stage
+  int armed_kv[2][kCg] = {{-1, -1, -1}, {-1, -1, -1}}, armed_q = -1;
   int unit, t0, t1, slot;
   bool whole;
 
@@ -244,46 +249,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           page = pd.num_pages;
         }
         if (idx >= npages_b) page = pd.num_pages;  // past the context: TMA fills zeros
-        if (gt >= 2) {
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(b_kv_empty + 8 * st, ((gt >> 1) - 1) & 1, tmo, abort_flag));
-          if (!ok) break;
-        }
+        // The chunk groups go out in order, each once the P.V that read its
+        // previous contents is done and each on its own full barrier, so the
+        // first chunk groups of a tile land while the last P.V blocks of the
+        // tile two back still run, and QK^T starts on them early.
         const uint32_t full = b_kv_full + 8 * kCg * st;
-        if (lane == 0) {
-#pragma unroll
-          for (int cg = 0; cg < kCg; ++cg) mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
-          armed_kv[st] = gt;
-        }
-        __syncwarp();
+        const uint32_t empty = b_kv_empty + 8 * kCg * st;
+        // N does not divide 64: lane k*gpp + g (gpp = 8-slot groups per page)
+        // loads group g of page k of the tile, rows r_k + 8 N g + N i (i < 8)
+        // of the (64 dims, row in page, chunk, page) view with traversal
+        // stride N along the rows, so rows past the page's end are out of
+        // the view and fill zeros.  One box is one 8-slot group of a chunk
+        // group (3072 bytes).
+        int r0 = 0, pgk = 0;
         if (kLocal == 2) {
-          // N does not divide 64: lane k*gpp + g (gpp = 8-slot groups per
-          // page) loads group g of page k of the tile, rows r_k + 8 N g +
-          // N i (i < 8) of the (64 dims, row in page, chunk, page) view with
-          // traversal stride N along the rows, so rows past the page's end
-          // are out of the view and fill zeros.  One box is one 8-slot group
-          // of a chunk group (3072 bytes).
           const int gpp_log2 = pd.spp_log2 - 3;
           const int k = lane >> gpp_log2, g = lane & ((1 << gpp_log2) - 1);
-          const int pgk = __shfl_sync(0xffffffffu, page, k & 31);
-          if (lane < 8) {
-            const int r0 = shard_row0(x.s, first_slot + k, pd.num_shards) + 8 * pd.num_shards * g;
-#pragma unroll
-            for (int cg = 0; cg < kCg; ++cg)
+          pgk = __shfl_sync(0xffffffffu, page, k & 31);
+          r0 = shard_row0(x.s, first_slot + k, pd.num_shards) + 8 * pd.num_shards * g;
+        }
+#pragma unroll 1
+        for (int cg = 0; cg < kCg; ++cg) {
+          if (gt >= 2) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(empty + 8 * cg, ((gt >> 1) - 1) & 1, tmo, abort_flag));
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
+            armed_kv[st][cg] = gt;
+          }
+          __syncwarp();
+          if (kLocal == 2) {
+            if (lane < 8)
               tma_load_4d(sKV + st * kTileBytes + cg * kCgBytes + lane * kGroupBytes, &tm_kv,
                           full + 8 * cg, 0, r0, kCgChunks * cg, pgk);
-          }
-        } else if (lane < nv) {
-          // cache row page*64 + res of the (row-in-group, chunk, group, row)
-          // view; a page of num_pages is out of range and fills zeros.  The
-          // chunk groups go out in order, each on its own barrier, so QK^T
-          // can start on the first while the others are still in flight.
-#pragma unroll
-          for (int cg = 0; cg < kCg; ++cg)
+          } else if (lane < nv) {
+            // cache row page*64 + res of the (row-in-group, chunk, group,
+            // row) view; a page of num_pages is out of range and fills zeros
             tma_load_5d(sKV + st * kTileBytes + cg * kCgBytes + lane * box_bytes, &tm_kv,
                         full + 8 * cg, 0, 0, kCgChunks * cg, 0, page * kPage + res);
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
         if (ok && j == t0) {
           // query rows of this unit: reuse of the buffer waits for the last
           // QK^T of the previous piece
@@ -362,13 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++pc;
     }
     if (!ok && lane == 0) set_error(p, misc, kErrTimeout);
-  } else if (warp >= 7 && warp <= 10) {
-    const int pmi = warp - 7;   // the latent block this warp issues
+  } else if (warp == 7) {
     // ------------------------------------------------------------ P.V issue
-    // V^T of latent block pmi: chunks 2 pmi and 2 pmi + 1, the two 64-dim
-    // swizzle atoms of M, lie chunk_off(2 pmi + 1) - chunk_off(2 pmi) apart
-    const uint64_t dv0 = sw128_desc(sKV + chunk_off(2 * pmi),
-                                    chunk_off(2 * pmi + 1) - chunk_off(2 * pmi), kGroupBytes);
+    // One thread issues the four latent blocks of O^T += V^T P^T in order and
+    // frees each chunk group of the stage as soon as the blocks reading it
+    // are done: chunks 0-2 after block 1, chunks 3-5 after block 2, chunks
+    // 6-8 (the probabilities in the rope slot included) after block 3.
+    // V^T of latent block b: chunks 2b and 2b + 1, the two 64-dim swizzle
+    // atoms of M, lie chunk_off(2b + 1) - chunk_off(2b) apart.
     const uint64_t dp0 = sw128_desc(sKV + kGroupRope, 16, kGroupBytes);
     int gbase = 0, pc = 0;
     bool ok = true;
@@ -386,12 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = g & 1;
           const uint32_t st_off = (uint32_t)(st * kTileBytes) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = dv0 + st_off + (uint32_t)((kk * 2 * kGroupBytes) >> 4);
-            const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
-            mma_bf16_ss(tmem + kColO + 64 * pmi, a, bd, id_pv, (j == t0 && kk == 0) ? 0u : 1u);
+          for (int blk = 0; blk < 4; ++blk) {
+            const uint64_t dv0 = sw128_desc(sKV + chunk_off(2 * blk),
+                                            chunk_off(2 * blk + 1) - chunk_off(2 * blk), kGroupBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = dv0 + st_off + (uint32_t)((kk * 2 * kGroupBytes) >> 4);
+              const uint64_t bd = dp0 + st_off + (uint32_t)((32 * kk) >> 4);
+              mma_bf16_ss(tmem + kColO + 64 * blk, a, bd, id_pv, (j == t0 && kk == 0) ? 0u : 1u);
+            }
+            if (blk >= 1) mma_commit(b_kv_empty + 8 * (kCg * st + blk - 1));
           }
-          mma_commit(b_kv_empty + 8 * st);
           mma_commit(b_pv_done + 8 * st);
         }
         __syncwarp();
@@ -615,14 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM is freed and the CTA exits.  A commit tracks every earlier MMA of
     // its thread, so one commit per issuing thread drains them all.
     int never = 0;
-    if (lane == 0 && (warp == 1 || warp == 6 || (warp >= 7 && warp <= 10))) {
+    if (lane == 0 && (warp == 1 || warp == 6 || warp == 7)) {
       mma_commit(smem_u32(&misc->drain));
       mbar_wait(smem_u32(&misc->drain), 0, kDrainNs, &never);
     }
     if (warp == 0 && lane == 0) {
       for (int st = 0; st < 2; ++st)
-        for (int cg = 0; cg < kCg && armed_kv[st] >= 0; ++cg)
-          mbar_wait(b_kv_full + 8 * (kCg * st + cg), (armed_kv[st] >> 1) & 1, kDrainNs, &never);
+        for (int cg = 0; cg < kCg; ++cg)
+          if (armed_kv[st][cg] >= 0)
+            mbar_wait(b_kv_full + 8 * (kCg * st + cg), (armed_kv[st][cg] >> 1) & 1, kDrainNs, &never);
       if (armed_q >= 0) mbar_wait(b_q_full, armed_q & 1, kDrainNs, &never);
     }
     tc_fence_before();
