@@ -673,17 +673,29 @@ def run_dcp(args, world, rank, dist, device, workload=None, partial_fn=None, com
         elapsed = time.perf_counter() - c0
     if clocks is not None:
         clk = clocks.stop()
-    # the rank's partial kernel alone, from an untimed profiled step
+    # the rank's partial kernels alone, from an untimed profiled step: one
+    # event pair around each request group's launch, summed
     kernel_ms = None
     if cuda and partial_fn is None:
         import sequence_sharded_mla_gb300 as mla
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        mla.mla_set_profile_events(e0, e1)
-        step()
-        mla.mla_set_profile_events(None, None)
+        pairs = []
+
+        def timed_partial(*a, **k):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            mla.mla_set_profile_events(e0, e1)
+            try:
+                return dcp._cuda_partial(*a, **k)
+            finally:
+                mla.mla_set_profile_events(None, None)
+                pairs.append((e0, e1))
+
+        dcp.dcp_decode_step(inp["q_local"], inp["kv"], inp["block_table"], inp["seq_lens"],
+                            layout=w.layout, kv_scale=inp["kv_scale"], causal=w.causal,
+                            softmax_scale=w.softmax_scale, w_uv_local=inp["w_uv_local"],
+                            partial_fn=timed_partial, chunks=args.dcp_chunks)
         barrier()
-        kernel_ms = e0.elapsed_time(e1)
+        kernel_ms = sum(e0.elapsed_time(e1) for e0, e1 in pairs)
     local_kv = inp["local_tokens"] * (1152 if w.kv_dtype == "bf16" else 580)
     (elapsed, kms), _ = reduce_over_ranks(dist, [elapsed, kernel_ms or 0.0], 0,
                                           device if cuda else torch.device("cpu"))
@@ -713,8 +725,10 @@ def run_dcp(args, world, rank, dist, device, workload=None, partial_fn=None, com
     }
     if kernel_ms is not None:
         achieved = local_kv / (kms / 1e3) / 1e9
-        line["roofline"] = {"kernel": "mla_partial_kernel<true>" if w.kv_dtype == "bf16"
-                            else "mla_partial_fp8_kernel<true>", "bound": "hbm",
+        line["roofline"] = {"kernel": "mla_partial_kernel<1, true> (local cache, DCP I/O)"
+                            if w.kv_dtype == "bf16" else
+                            "mla_partial_fp8_kernel<1, true> (local cache, DCP I/O)",
+                            "launches": args.dcp_chunks, "bound": "hbm",
                             "achieved": achieved, "peak": peak, "unit": "GB/s",
                             "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                             "traffic": None}

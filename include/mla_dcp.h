@@ -162,6 +162,39 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The per-rank call of a multi-GPU DCP step with the exchanges' own layouts
+ * ("Decode Context Parallelism", section 4.1: AllGather Q -> Compute -> a
+ * combine of the partials; "Kimi K3 Performance Optimizations in vLLM",
+ * section "Decode context parallelism": the partial outputs and LSEs travel
+ * by an all-to-all).  Computes what mla_decode_partial computes for shard
+ * `rank` of `num_ranks` (shard_id = rank, num_shards = num_ranks) with no copy
+ * around it:
+ *   q_gathered: bf16 [num_ranks, batch_total, q_len, H/num_ranks, 576], the
+ *     all-gather of every rank's query heads as it lands (rank k's block
+ *     holds heads k*H/num_ranks ..); this call computes requests
+ *     batch_first .. batch_first + shape->batch - 1 of it.
+ *   block_table, seq_lens (and shape->q_lens): those requests' rows.
+ *   out_send: fp32 [num_ranks, shape->batch, q_len, H/num_ranks, 512];
+ *   lse_send: fp32 [num_ranks, shape->batch, q_len, H/num_ranks]: slice k
+ *     holds this shard's partial of heads k*H/num_ranks .., i.e. the send
+ *     buffers of an all-to-all after which rank k holds every shard's
+ *     partial of its own heads, shard-major, as mla_shard_combine takes
+ *     them.
+ * layout: MLA_LAYOUT_INTERLEAVED_LOCAL or MLA_LAYOUT_CONTIGUOUS_LOCAL (the
+ * rank's own slice of the cache; else MLA_ERR_INVALID).  H must be a multiple
+ * of num_ranks with H/num_ranks a multiple of 8 that divides 64 or is a
+ * multiple of 64 (else MLA_ERR_UNSUPPORTED).  Other
+ * arguments, the workspace (mla_workspace_size(shape, num_ranks, rank)) and
+ * errors as for mla_decode_partial.
+ */
+mla_status mla_decode_partial_dcp(const void* q_gathered, int batch_total, int batch_first,
+                                  const mla_kv_pages* kv, const int32_t* block_table,
+                                  int max_pages_per_req, const int32_t* seq_lens,
+                                  const mla_shape* shape, int rank, int num_ranks,
+                                  mla_layout layout, float* out_send, float* lse_send,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_partial without a workspace argument, for callers that cannot
  * allocate device memory (for example code running while a serving engine's
  * pool already owns the whole GPU, allocator or out-of-memory callbacks, or

@@ -56,7 +56,8 @@ class gqa_kv_pages(ctypes.Structure):
 
 
 _LIB = None
-EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_shard_combine",
+EXPORTS = ("mla_decode_partial", "mla_decode_partial_noalloc", "mla_decode_partial_dcp",
+           "mla_shard_combine",
            "mla_decode_step", "mla_decode_step_workspace_size",
            "mla_workspace_size", "mla_get_device_error", "mla_get_device_error_noalloc",
            "mla_set_wait_budget_ns", "mla_set_withhold_query", "mla_set_profile_events",
@@ -75,6 +76,10 @@ def lib():
                                          ctypes.POINTER(mla_shape), i32, i32, i32, vp, vp, vp,
                                          sz, vp]
         L.mla_decode_partial.restype = i32
+        L.mla_decode_partial_dcp.argtypes = [vp, i32, i32, ctypes.POINTER(mla_kv_pages), vp, i32,
+                                             vp, ctypes.POINTER(mla_shape), i32, i32, i32, vp, vp,
+                                             vp, sz, vp]
+        L.mla_decode_partial_dcp.restype = i32
         L.mla_decode_partial_noalloc.argtypes = [vp, ctypes.POINTER(mla_kv_pages), vp, i32, vp,
                                                  ctypes.POINTER(mla_shape), i32, i32, i32, vp,
                                                  vp, vp]
@@ -150,6 +155,24 @@ def mla_workspace_size(batch, q_len, num_heads, num_shards, shard_id=ALL_SHARDS,
     return int(lib().mla_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
 
 
+def _kv_pages(kv, kv_scale, dev):
+    """The mla_kv_pages descriptor of a bf16 or e4m3 cache (checked)."""
+    if kv.dtype == torch.bfloat16:
+        kv_dtype = KV_BF16
+        if kv_scale is not None:
+            raise ValueError("kv_scale is only for fp8 caches")
+    elif kv.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        kv_dtype = KV_FP8
+        if kv_scale is None:
+            raise ValueError("fp8 caches need kv_scale")
+        _check(kv_scale, "kv_scale", (torch.float32,), 2, dev)
+    else:
+        raise TypeError(f"kv dtype {kv.dtype} unsupported")
+    _check(kv, "kv", (kv.dtype,), 3, dev)
+    return mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
+                        kv_dtype, kv.shape[0], kv.shape[1])
+
+
 def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interleaved",
                        shard_id=ALL_SHARDS, kv_scale=None, causal=False,
                        softmax_scale=DEFAULT_SCALE, out_partial=None, lse_partial=None,
@@ -168,18 +191,7 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
     B, q_len, H, d = q.shape
     if d != D_QK:
         raise ValueError("q must be [B, q_len, H, 576]")
-    if kv.dtype == torch.bfloat16:
-        kv_dtype = KV_BF16
-        if kv_scale is not None:
-            raise ValueError("kv_scale is only for fp8 caches")
-    elif kv.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
-        kv_dtype = KV_FP8
-        if kv_scale is None:
-            raise ValueError("fp8 caches need kv_scale")
-        _check(kv_scale, "kv_scale", (torch.float32,), 2, dev)
-    else:
-        raise TypeError(f"kv dtype {kv.dtype} unsupported")
-    _check(kv, "kv", (kv.dtype,), 3, dev)
+    pages = _kv_pages(kv, kv_scale, dev)
     _check(block_table, "block_table", (torch.int32,), 2, dev)
     _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
     n_out = num_shards if shard_id == ALL_SHARDS else 1
@@ -195,8 +207,6 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
     need = int(lib().mla_workspace_size(ctypes.byref(sh), int(num_shards), int(shard_id)))
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
-    pages = mla_kv_pages(kv.data_ptr(), None if kv_scale is None else kv_scale.data_ptr(),
-                         kv_dtype, kv.shape[0], kv.shape[1])
     st = lib().mla_decode_partial(_ptr(q), ctypes.byref(pages), _ptr(block_table),
                                   block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
                                   int(shard_id), int(num_shards), LAYOUTS[layout],
@@ -205,6 +215,55 @@ def mla_decode_partial(q, kv, block_table, seq_lens, num_shards, layout="interle
     if st != 0:
         raise MLAError(st, "mla_decode_partial")
     return out_partial, lse_partial, workspace
+
+
+def mla_decode_partial_dcp(q_gathered, kv, block_table, seq_lens, rank,
+                           layout="interleaved_local", batch_first=0, kv_scale=None,
+                           causal=False, softmax_scale=DEFAULT_SCALE, out_send=None,
+                           lse_send=None, workspace=None, stream=None, q_lens=None):
+    """The per-rank call of a DCP step in the exchanges' own layouts; returns
+    (out_send, lse_send, workspace).
+
+    q_gathered: bf16 [N, B_total, q_len, H/N, 576], the all-gather of the N
+    ranks' query heads; this call computes requests batch_first ..
+    batch_first + len(seq_lens) - 1 of it over shard `rank` of N of this
+    rank's cache (block_table, seq_lens, q_lens: those requests' rows).
+    out_send: fp32 [N, B, q_len, H/N, 512], lse_send: fp32 [N, B, q_len, H/N]:
+    slice k is this shard's partial of rank k's heads -- the all-to-all's send
+    buffers.
+    """
+    _check(q_gathered, "q_gathered", (torch.bfloat16,), 5)
+    dev = q_gathered.device
+    N, B_total, q_len, Hl, d = q_gathered.shape
+    if d != D_QK:
+        raise ValueError("q_gathered must be [N, B_total, q_len, H/N, 576]")
+    pages = _kv_pages(kv, kv_scale, dev)
+    _check(block_table, "block_table", (torch.int32,), 2, dev)
+    _check(seq_lens, "seq_lens", (torch.int32,), 1, dev)
+    B = seq_lens.shape[0]
+    if block_table.shape[0] != B:
+        raise ValueError("block_table and seq_lens disagree on the number of requests")
+    if out_send is None:
+        out_send = torch.empty((N, B, q_len, Hl, D_V), dtype=torch.float32, device=dev)
+    if lse_send is None:
+        lse_send = torch.empty((N, B, q_len, Hl), dtype=torch.float32, device=dev)
+    _check(out_send, "out_send", (torch.float32,), 5, dev)
+    _check(lse_send, "lse_send", (torch.float32,), 4, dev)
+    if q_lens is not None:
+        _check(q_lens, "q_lens", (torch.int32,), 1, dev)
+    sh = _shape(B, q_len, N * Hl, causal, softmax_scale, q_lens)
+    need = int(lib().mla_workspace_size(ctypes.byref(sh), int(N), int(rank)))
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    st = lib().mla_decode_partial_dcp(_ptr(q_gathered), int(B_total), int(batch_first),
+                                      ctypes.byref(pages), _ptr(block_table),
+                                      block_table.shape[1], _ptr(seq_lens), ctypes.byref(sh),
+                                      int(rank), int(N), LAYOUTS[layout], _ptr(out_send),
+                                      _ptr(lse_send), _ptr(workspace), workspace.numel(),
+                                      _stream_ptr(stream))
+    if st != 0:
+        raise MLAError(st, "mla_decode_partial_dcp")
+    return out_send, lse_send, workspace
 
 
 def mla_decode_step_workspace_size(batch, q_len, num_heads, num_shards) -> int:

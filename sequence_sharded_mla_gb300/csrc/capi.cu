@@ -135,11 +135,19 @@ struct Launched {
 // and partial-attention kernels.  Units that one CTA computes whole are
 // written to out_partial / lse_partial; pieces of split units to the
 // workspace slots described by *L.
+// The DCP rank-major I/O of mla_decode_partial_dcp (rank_heads = 0: none).
+struct RankIo {
+  int rank_heads;   // H / ranks
+  int ranks;
+  int batch_total;  // requests in the gathered query buffer
+  int batch_first;  // first of them computed by this call
+};
+
 mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* block_table,
                           int max_pages_per_req, const int32_t* seq_lens, const mla_shape* shape,
                           int shard_id, int num_shards, mla_layout layout, float* out_partial,
                           float* lse_partial, void* workspace, size_t workspace_bytes,
-                          void* stream, Launched* L) {
+                          void* stream, Launched* L, RankIo rio = RankIo{0, 1, 0, 0}) {
   if (!q || !kv || !block_table || !seq_lens || !out_partial || !lse_partial) return MLA_ERR_INVALID;
   if (!shape_ok(shape)) return MLA_ERR_INVALID;
   if (num_shards < 1 || num_shards > kMaxShards) return MLA_ERR_INVALID;
@@ -192,6 +200,9 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
   pd.ppt = 1;
   pd.spp_log2 = 6;
   pd.pad = 0;
+  pd.rank_heads = rio.rank_heads;
+  pd.q_batch_total = rio.rank_heads ? rio.batch_total : pd.B;
+  pd.q_batch_first = rio.rank_heads ? rio.batch_first : 0;
   if (layout == MLA_LAYOUT_INTERLEAVED) {
     if (kPage % num_shards == 0) {
       pd.ppt = num_shards;
@@ -215,7 +226,22 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
   // [chunk][row][64] shared-memory layout; fallback: one box per chunk.
   CUtensorMap tm_q, tm_kv, tm_kv_pf;
   int q_one_box = 1;
-  {
+  // rank-major gathered query [ranks, batch_total, q_len, rank_heads, 576]:
+  // rows of one rank's heads of one query position are consecutive, so the
+  // kernels load a 64-row group as runs of min(rank_heads, 64) rows
+  const cuuint64_t q_rows_rm = (cuuint64_t)rio.ranks * rio.batch_total * shape->q_len * rio.rank_heads;
+  const cuuint32_t q_run = (cuuint32_t)std::min(rio.rank_heads, kRows);
+  if (rio.rank_heads != 0) {
+    q_one_box = 0;
+    cuuint64_t d2[2] = {(cuuint64_t)kDqk, q_rows_rm};
+    cuuint64_t s2[1] = {(cuuint64_t)kDqk * 2};
+    cuuint32_t b2[2] = {64, q_run};
+    cuuint32_t es[2] = {1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), d2, s2, b2, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  } else {
     cuuint64_t dims[3] = {64, (cuuint64_t)pd.B * pd.R, (cuuint64_t)kChunks};
     cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, 128};
     cuuint32_t box[3] = {64, (cuuint32_t)kRows, (cuuint32_t)kChunks};
@@ -248,9 +274,10 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
     // query rows for the fp8 kernel, by 8-row groups: view (64 dims, row in
     // group, chunk, row group) with strides (-, 1152, 128, 9216); a box lands
     // a 64-row group as [row group][chunk][row][64], 9216 bytes per row group
-    cuuint64_t qd[4] = {64, 8, (cuuint64_t)kChunks, (cuuint64_t)pd.B * pd.R / 8};
+    cuuint64_t qd[4] = {64, 8, (cuuint64_t)kChunks,
+                        rio.rank_heads ? q_rows_rm / 8 : (cuuint64_t)pd.B * pd.R / 8};
     cuuint64_t qs[3] = {(cuuint64_t)kDqk * 2, 128, (cuuint64_t)kDqk * 2 * 8};
-    cuuint32_t qb[4] = {64, 8, (cuuint32_t)kChunks, (cuuint32_t)(kRows / 8)};
+    cuuint32_t qb[4] = {64, 8, (cuuint32_t)kChunks, rio.rank_heads ? q_run / 8 : (cuuint32_t)(kRows / 8)};
     cuuint32_t qe[4] = {1, 1, 1, 1};
     if (encode(&tm_q8, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), qd, qs, qb, qe,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -396,6 +423,38 @@ mla_status mla_decode_partial(const void* q, const mla_kv_pages* kv, const int32
   if (st != MLA_OK) return st;
   if (launch_merge(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, out_partial, lse_partial,
                    L.num_units, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status mla_decode_partial_dcp(const void* q_gathered, int batch_total, int batch_first,
+                                  const mla_kv_pages* kv, const int32_t* block_table,
+                                  int max_pages_per_req, const int32_t* seq_lens,
+                                  const mla_shape* shape, int rank, int num_ranks,
+                                  mla_layout layout, float* out_send, float* lse_send,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!shape_ok(shape) || num_ranks < 1 || num_ranks > kMaxShards || rank < 0 ||
+      rank >= num_ranks)
+    return MLA_ERR_INVALID;
+  if (batch_first < 0 || batch_total < shape->batch ||
+      batch_first > batch_total - shape->batch)
+    return MLA_ERR_INVALID;
+  if (shape->num_heads % num_ranks != 0) return MLA_ERR_INVALID;
+  // a rank holds its own slice of the cache
+  if (layout != MLA_LAYOUT_INTERLEAVED_LOCAL && layout != MLA_LAYOUT_CONTIGUOUS_LOCAL)
+    return MLA_ERR_INVALID;
+  const int hl = shape->num_heads / num_ranks;
+  // runs of one rank's heads are whole 8-row groups, and a 64-row query
+  // group is a whole number of runs (or lies inside one)
+  if (hl % 8 != 0 || (kRows % hl != 0 && hl % kRows != 0)) return MLA_ERR_UNSUPPORTED;
+  Launched L;
+  const mla_status st = partial_launch(q_gathered, kv, block_table, max_pages_per_req, seq_lens,
+                                       shape, rank, num_ranks, layout, out_send, lse_send,
+                                       workspace, workspace_bytes, stream, &L,
+                                       RankIo{hl, num_ranks, batch_total, batch_first});
+  if (st != MLA_OK) return st;
+  if (launch_merge(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, out_send, lse_send, L.num_units,
+                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -75,6 +75,15 @@ struct ProblemDesc {
   int ppt;
   int spp_log2;
   int pad;
+  // DCP rank-major I/O (rank_heads = H / ranks > 0): the query rows are read
+  // from the all-gathered buffer [ranks, q_batch_total, q_len, rank_heads,
+  // 576] (requests q_batch_first..+B of it), and the outputs are written as
+  // head slices [ranks, B, q_len, rank_heads, 512] (and [.., rank_heads]),
+  // slice k holding heads k*rank_heads.. -- the all-to-all's send layout.
+  // 0: both row-major [B, q_len, H, ...].
+  int rank_heads;
+  int q_batch_total;
+  int q_batch_first;
   float scale_log2;    // softmax scale * log2(e)
   const int32_t* block_table;  // [B, max_pages]
   const int32_t* seq_lens;     // [B]
@@ -265,6 +274,29 @@ __device__ __forceinline__ Unit make_unit(const ProblemDesc& pd, int u) {
     }
   }
   return x;
+}
+
+// Row of out_partial / lse_partial that holds row `row` (0..63) of unit x's
+// query group.
+__device__ __forceinline__ size_t out_row(const ProblemDesc& pd, const Unit& x, int row) {
+  const int rr = x.g * kRows + row;            // i * H + h within the request
+  if (pd.rank_heads == 0) return ((size_t)x.so * pd.B + x.b) * pd.R + rr;
+  const int i = rr / pd.H, h = rr - i * pd.H;
+  const int k = h / pd.rank_heads, hl = h - k * pd.rank_heads;
+  return (((size_t)k * pd.B + x.b) * pd.q_len + i) * pd.rank_heads + hl;
+}
+
+// Query rows per TMA box in the rank-major mode: a run of one rank's heads
+// of one query position (rank_heads is a multiple of 8 that divides 64 or is
+// a multiple of 64), and the gathered-buffer row of row `row` of x's group.
+__device__ __forceinline__ int q_run_rows(const ProblemDesc& pd) {
+  return pd.rank_heads < kRows ? pd.rank_heads : kRows;
+}
+__device__ __forceinline__ int q_src_row(const ProblemDesc& pd, const Unit& x, int row) {
+  const int rr = x.g * kRows + row;
+  const int i = rr / pd.H, h = rr - i * pd.H;
+  const int k = h / pd.rank_heads, hl = h - k * pd.rank_heads;
+  return ((k * pd.q_batch_total + pd.q_batch_first + x.b) * pd.q_len + i) * pd.rank_heads + hl;
 }
 
 // Global token position of slot a (0..63) of tile j of unit x.  Interleaved

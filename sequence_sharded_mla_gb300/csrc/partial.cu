@@ -83,6 +83,7 @@ struct Misc {
   int abort;
   float alpha[2][kRows];  // by tile parity: a warp may be one tile ahead of another
   alignas(16) float inv_l[kRows];
+  uint32_t orow[kRows];   // epilogue: destination row of each of the group's rows
 };
 
 constexpr int kSmemQ = 0;
@@ -120,7 +121,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-template <int kLocal>
+template <int kLocal, bool kRankIo>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv,
@@ -300,9 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(b_q_empty, (pc - 1) & 1, tmo, abort_flag));
             if (!ok) break;
           }
-          if (lane == 0 && !(p.withhold_query && pc == 0)) {
+          const bool load_q = !(p.withhold_query && pc == 0);
+          if (lane == 0 && load_q) {
             mbar_arrive_expect_tx(b_q_full, kTileBytes);
             armed_q = pc;
+          }
+          __syncwarp();
+          if (kRankIo && load_q) {
+            // rank-major gathered query: lane k loads run k (one rank's heads
+            // of one query position), chunk by chunk
+            const int run = q_run_rows(pd);
+            if (lane < kRows / run) {
+              const int src = q_src_row(pd, x, lane * run);
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c)
+                tma_load_2d(sQ + c * kChunkBytes + lane * run * 128, &tm_q, b_q_full, c * 64, src);
+            }
+          } else if (lane == 0 && load_q) {
             const int row0 = x.b * pd.R + x.g * kRows;
             if (p.q_one_box) {
               tma_load_3d(sQ, &tm_q, b_q_full, 0, row0, 0);
@@ -553,31 +568,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        abort_flag));
       if (named_bar_or(kBarSoftmax, kSoftmaxThreads, !ok_e)) { ok = false; break; }
       tc_fence_after();
-      float* dst_o;
-      float* dst_lse;
-      if (whole) {
-        size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
-        dst_o = p.out_partial + row0 * kDv;
-        dst_lse = p.lse_partial + row0;
-      } else {
-        size_t sl = 2 * (size_t)blockIdx.x + slot;
-        dst_o = p.ws_o + sl * kRows * kDv;
-        dst_lse = p.ws_lse + sl * kRows;
-      }
+      // destination rows: a whole unit's rows of out_partial (out_row:
+      // row-major, or the DCP head slices), or this CTA's workspace slot for a
+      // piece of a split unit; the store loop reads them from a table
+      float* const obase = whole ? p.out_partial : p.ws_o;
+      float* const lbase = whole ? p.lse_partial : p.ws_lse;
+      const size_t sl = 2 * (size_t)blockIdx.x + slot;
+      // whole units: row-major rows (out_row), or in the DCP head slices
+      // scattered rows (kRankIo), whose destinations the store loop reads
+      // from a table
+      const size_t row0 = whole ? ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows
+                                : sl * kRows;
+      auto dst_row = [&](int row) -> size_t {
+        return (kRankIo && whole) ? out_row(pd, x, row) : row0 + row;
+      };
+      if (kRankIo && tid < kRows) misc->orow[tid] = (uint32_t)dst_row(tid);
       const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
       if (owner && half == 0) {
         float lse = (l_tot > 0.0f) ? (m_run + __log2f(l_tot)) * 0.69314718055994530942f
                                    : -CUDART_INF_F;
         misc->inv_l[r] = (l_tot > 0.0f) ? 1.0f / l_tot : 0.0f;
-        dst_lse[r] = lse;
+        lbase[dst_row(r)] = lse;
       }
       if (whole) {
         // padding rows of a request with fewer query tokens: o = 0, lse = -inf
         // (pieces of a split unit leave them to the merge kernel)
         for (int e = tid; e < (x.rows_out - x.rows) * (kDv / 4); e += kSoftmaxThreads)
-          reinterpret_cast<float4*>(dst_o + (size_t)x.rows * kDv)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          reinterpret_cast<float4*>(obase + dst_row(x.rows + e / (kDv / 4)) * kDv)[e % (kDv / 4)] =
+              make_float4(0.f, 0.f, 0.f, 0.f);
         for (int rr = x.rows + tid; rr < x.rows_out; rr += kSoftmaxThreads)
-          dst_lse[rr] = -CUDART_INF_F;
+          lbase[dst_row(rr)] = -CUDART_INF_F;
       }
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       // O^T block k/2, rows 32*(k%2).. of this thread's latent dim, two TMEM
@@ -599,7 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int row = 32 * (k & 1) + c;
-            if (row < x.rows) dst_o[(size_t)row * kDv + dim] = __uint_as_float(v[c]) * il[c];
+            if (row < x.rows) {
+              if (kRankIo) obase[(size_t)misc->orow[row] * kDv + dim] = __uint_as_float(v[c]) * il[c];
+              else obase[(row0 + row) * kDv + dim] = __uint_as_float(v[c]) * il[c];
+            }
           }
         };
         uint32_t va[32], vb[32];
@@ -652,12 +675,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-template <int kLocal>
+template <int kLocal, bool kRankIo = false>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                   cudaStream_t stream) {
   const cudaError_t e =
-      host::ensure_dynamic_smem(reinterpret_cast<const void*>(&mla_partial_kernel<kLocal>), kSmemBytes);
+      host::ensure_dynamic_smem(reinterpret_cast<const void*>(&mla_partial_kernel<kLocal, kRankIo>), kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -667,7 +690,7 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal>, tm_q, tm_kv, tm_kv_pf, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal, kRankIo>, tm_q, tm_kv, tm_kv_pf, p);
 }
 
 // The cache kind (whole requests, a local slice, or whole requests with
@@ -676,6 +699,8 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                 cudaStream_t stream) {
+  // the DCP rank-major I/O (local caches only) is an instantiation of its own
+  if (p.pd.rank_heads != 0) return launch_partial<1, true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
   return p.pd.local ? launch_partial<1>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
          : p.pd.pad   ? launch_partial<2>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
                       : launch_partial<0>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);

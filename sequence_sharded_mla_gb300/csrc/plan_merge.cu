@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   if (r >= x.rows_out) return;
   const int ps = prefix[u], ue = prefix[u + 1];
   const int us = unit_tile_start(prefix, u, hdr->unit_cost);
-  const size_t row0 = ((size_t)x.so * pd.B + x.b) * pd.R + (size_t)x.g * kRows;
-  float4* dst = reinterpret_cast<float4*>(out_partial + (row0 + r) * kDv);
+  const size_t orow = out_row(pd, x, r);
+  float4* dst = reinterpret_cast<float4*>(out_partial + orow * kDv);
   const int per = hdr->per_cta;
   const bool split = us < ue && us / per != (ue - 1) / per;
   // rows with no token to see: the shard holds none of the request's
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
   // (a whole unit's padding rows are written by the partial kernel)
   if (us == ue || (split && r >= x.rows)) {
     for (int v = lane; v < kDv / 4; v += 32) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) lse_partial[row0 + r] = -CUDART_INF_F;
+    if (lane == 0) lse_partial[orow] = -CUDART_INF_F;
     return;
   }
   const int c0 = us / per, c1 = (ue - 1) / per;
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     dst[lane + 32 * i] = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
-  if (lane == 0) lse_partial[row0 + r] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
+  if (lane == 0) lse_partial[orow] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
 }
 
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,

@@ -48,17 +48,17 @@ def _worker(rank, world, port, out):
         Hl = H // world
         calls = {"partial": 0, "outs": []}
 
-        def partial_fn(q_full, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
+        def partial_fn(q_g, b0, b1, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
                        q_lens=None):
             calls["partial"] += 1
             assert N == world and shard_id == rank and lay == "interleaved"
-            b0 = sl_.storage_offset()
-            b1 = b0 + sl_.shape[0]
-            q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)[b0:b1]
-            assert torch.equal(q_full, q)             # the all-gathered query
+            assert sl_.storage_offset() == b0 and sl_.shape[0] == b1 - b0
+            q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16)
+            # the all-gathered query, rank-major: block k holds rank k's heads
+            assert torch.equal(q_g, q.reshape(B, q_len, N, Hl, 576).permute(2, 0, 1, 3, 4))
             o, l = oracle.attend(w, shard=shard_id, num_shards=N, layout=lay)
-            o = o.reshape(B, q_len, H, 512)[b0:b1]
-            l = l.reshape(B, q_len, H)[b0:b1]
+            o = np.moveaxis(o.reshape(B, q_len, N, Hl, 512)[b0:b1], 2, 0)
+            l = np.moveaxis(l.reshape(B, q_len, N, Hl)[b0:b1], 2, 0)
             return (torch.from_numpy(np.ascontiguousarray(o, dtype=np.float32)),
                     torch.from_numpy(np.ascontiguousarray(l, dtype=np.float32)))
 

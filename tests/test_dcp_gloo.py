@@ -54,20 +54,21 @@ def _worker(rank, world, port, layout, causal, wuv, chunks, out):
             w_uv_local = torch.from_numpy(w.w_uv.view(np.int16)).view(torch.bfloat16)[
                 rank * Hl:(rank + 1) * Hl].contiguous()
 
-        seen = {"q": []}
+        seen = {"q_ok": [], "groups": []}
+        # the all-gathered query, rank-major: block k holds rank k's heads
+        q_gathered = q.reshape(B, q_len, world, Hl, 576).permute(2, 0, 1, 3, 4)
 
-        def partial_fn(q_full, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
+        def partial_fn(q_g, b0, b1, kv_, bt_, sl_, N, lay, shard_id, kv_scale, causal_, scale,
                        q_lens=None):
-            # the request group [b0, b1) is a view into the full batch
-            b0 = sl_.storage_offset()
-            b1 = b0 + sl_.shape[0]
-            seen["q"].append(q_full)
+            seen["q_ok"].append(torch.equal(q_g, q_gathered))
+            seen["groups"].append((b0, b1))
             assert N == world and shard_id == rank and lay == layout and causal_ == causal
             assert kv_ is kv and bt_.storage_offset() == b0 * bt.shape[1]
             assert torch.equal(bt_, bt[b0:b1]) and torch.equal(sl_, sl[b0:b1])
             o, l = oracle.attend(w, shard=shard_id, num_shards=N, layout=lay)
-            o = o.reshape(B, q_len, H, 512)[b0:b1]
-            l = l.reshape(B, q_len, H)[b0:b1]
+            # head slices [N, b1 - b0, q_len, H/N, ...], slice k for rank k
+            o = np.moveaxis(o.reshape(B, q_len, N, Hl, 512)[b0:b1], 2, 0)
+            l = np.moveaxis(l.reshape(B, q_len, N, Hl)[b0:b1], 2, 0)
             return (torch.from_numpy(np.ascontiguousarray(o, dtype=np.float32)),
                     torch.from_numpy(np.ascontiguousarray(l, dtype=np.float32)))
 
@@ -85,8 +86,11 @@ def _worker(rank, world, port, layout, causal, wuv, chunks, out):
         res, lse = dcp.dcp_decode_step(q_local, kv, bt, sl, layout=layout, causal=causal,
                                        w_uv_local=w_uv_local, partial_fn=partial_fn,
                                        combine_fn=combine_fn, chunks=chunks)
-        assert len(seen["q"]) == min(chunks, B)
-        out[rank] = (torch.equal(torch.cat(seen["q"], 0), q), res.numpy(), lse.numpy())
+        groups = seen["groups"]
+        assert len(groups) == min(chunks, B)
+        assert groups[0][0] == 0 and groups[-1][1] == B
+        assert all(a[1] == b[0] for a, b in zip(groups, groups[1:]))
+        out[rank] = (all(seen["q_ok"]), res.numpy(), lse.numpy())
     finally:
         dist.destroy_process_group()
 
@@ -122,10 +126,13 @@ def test_dcp_exchange_gives_each_rank_its_heads_of_unsharded_attention(world, la
 
 
 def test_head_slices_route_to_their_ranks_single_process():
-    """Without a process group the exchange is the identity reshuffle."""
+    """Without a process group the exchange hands the one head slice back, and
+    the query all-gather is the rank's own heads as a block of one."""
     from sequence_sharded_mla_gb300 import dcp
-    o = torch.arange(2 * 1 * 32 * 512, dtype=torch.float32).reshape(2, 1, 32, 512)
-    lse = torch.arange(2 * 1 * 32, dtype=torch.float32).reshape(2, 1, 32)
+    o = torch.arange(1 * 2 * 1 * 32 * 512, dtype=torch.float32).reshape(1, 2, 1, 32, 512)
+    lse = torch.arange(1 * 2 * 1 * 32, dtype=torch.float32).reshape(1, 2, 1, 32)
     po, pl = dcp.exchange_head_slices(o, lse)
-    assert po.shape == (1, 2, 1, 32, 512) and torch.equal(po[0], o)
-    assert torch.equal(pl[0], lse)
+    assert po.shape == (1, 2, 1, 32, 512) and torch.equal(po, o) and torch.equal(pl, lse)
+    q = torch.randn(2, 1, 32, 576).to(torch.bfloat16)
+    g = dcp.gather_query_heads(q)
+    assert g.shape == (1, 2, 1, 32, 576) and torch.equal(g[0], q)
