@@ -433,7 +433,7 @@ def gqa_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
 
     outputs = [(out, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)),
                (lse, torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True))]
-    config = {"workload": mi.GQA_CONFIG_NAME, "batch": B, "heads": H,
+    config = {"workload": name, "batch": B, "heads": H,
               "kv_heads": w.num_kv_heads, "head_dim": D, "q_len": q_len, "num_shards": N,
               "layout": w.layout, "kv_dtype": "bf16", "causal": bool(w.causal),
               "total_tokens_per_gpu": w.total_tokens}
