@@ -158,7 +158,7 @@ def dist_setup(args, backend="nccl"):
     return world, rank, local, pg
 
 
-def rank_workload_params(config, rank, requests=0):
+def rank_workload_params(config, rank, requests=0, wuv=False):
     """Arguments of the batch rank ``rank`` decodes: rank 0 the configuration
     itself, every other rank an independently seeded batch of the same shape
     (weak scaling: ranks share nothing on the data path).  ``requests`` > 0
@@ -173,20 +173,23 @@ def rank_workload_params(config, rank, requests=0):
         p["name"] += f"-first{requests}"
         p["batch"] = requests
         p["seq_lens"] = list(p["seq_lens"])[:requests]
+    if wuv and not p.get("with_w_uv"):
+        p["name"] += "+wuv"
+        p["with_w_uv"] = True
     return p
 
 
 _WORKLOADS = {}
 
 
-def rank_workload(config, rank, requests=0, pinned=True):
+def rank_workload(config, rank, requests=0, pinned=True, wuv=False):
     """The rank's workload, generated once per process (the shard-count sweep
     runs one cache at several shard counts and layouts)."""
     import mla_inputs as mi
-    key = (config, rank, requests, pinned)
+    key = (config, rank, requests, pinned, wuv)
     if key not in _WORKLOADS:
         _WORKLOADS[key] = mi.build_workload(pinned=pinned,
-                                            **rank_workload_params(config, rank, requests))
+                                            **rank_workload_params(config, rank, requests, wuv))
     return _WORKLOADS[key]
 
 
@@ -333,11 +336,11 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
 
     import mla_inputs as mi
     import sequence_sharded_mla_gb300 as mla
-    w = rank_workload(args.config, rank, args.requests)
+    w = rank_workload(args.config, rank, args.requests, wuv=getattr(args, "wuv", False))
     B, H, q_len = w.batch, w.num_heads, w.q_len
     N = args.num_shards or w.num_shards
     layout = args.layout or w.layout
-    key = ("device", args.config, rank, args.requests)
+    key = ("device", args.config, rank, args.requests, getattr(args, "wuv", False))
     if key not in _WORKLOADS:
         q = _pinned_pair(torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16), dev)
         if w.kv_dtype == "bf16":
@@ -883,6 +886,8 @@ def main():
                          "or 6: the grouped-query batch")
     ap.add_argument("--requests", type=int, default=0,
                     help="profiling only: keep the first K requests of the workload")
+    ap.add_argument("--wuv", action="store_true",
+                    help="attach a W_UV projection to the configuration (fused into the step)")
     ap.add_argument("--num-shards", type=int, default=0,
                     help="override the configuration's logical shard count (1..8)")
     ap.add_argument("--layout", default="", choices=["", "interleaved", "contiguous"],

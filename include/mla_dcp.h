@@ -262,7 +262,11 @@ mla_status mla_shard_combine(const float* partials, const float* lses, int num_s
  * A shard's unit that the work split divides between several CTAs leaves one
  * partial per CTA; these pieces are merged together with the other shards'
  * partials in the combine itself (the LSE merge is associative), so no merged
- * per-shard partial is written.
+ * per-shard partial is written.  With w_uv and B * q_len >= 64 query rows per
+ * head, the combine writes the output o in bf16 into the workspace and the
+ * W_UV projection runs as one tensor-core GEMM per head (o rounded to bf16
+ * before the product, as when projecting the unfused bf16 output); with
+ * fewer rows the combine projects on the fly.
  *
  * Arguments as for mla_decode_partial and mla_shard_combine; layout must be
  * MLA_LAYOUT_INTERLEAVED or MLA_LAYOUT_CONTIGUOUS.  out: bf16

@@ -30,6 +30,9 @@ cudaError_t launch_combine(const float* partials, const float* lses, int num_sha
 cudaError_t launch_combine_wuv(const float* partials, const float* lses, int num_shards,
                                int rows_per_head_group, int H, const uint16_t* w_uv, uint16_t* y,
                                float* lse_out, cudaStream_t stream);
+cudaError_t launch_wuv_gemm(const uint16_t* o, const uint16_t* w_uv, uint16_t* y,
+                            int rows_per_head, int H, unsigned* err,
+                            unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t launch_step_combine(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
                                 const float* ws_o, const float* ws_lse, const float* part,
                                 const float* part_lse, const uint16_t* w_uv, uint16_t* out,
@@ -390,22 +393,30 @@ mla_status partial_launch(const void* q, const mla_kv_pages* kv, const int32_t* 
   return MLA_OK;
 }
 
-// Workspace of a whole decode step: the partial-attention workspace, then
-// the shard partials [N, B, R, 512] and their LSEs [N, B, R].
+// Workspace of a whole decode step: the partial-attention workspace, the
+// shard partials [N, B, R, 512] and their LSEs [N, B, R], then the combined
+// output [B, R, 512] in bf16 that the tensor-core W_UV projection reads.
 struct StepLayout {
-  size_t partial_ws, part, part_lse, total;
+  size_t partial_ws, part, part_lse, obf, total;
 };
 
 StepLayout step_layout(const mla_shape* shape, int num_shards) {
   auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
   StepLayout s;
   s.partial_ws = up(mla_workspace_size(shape, num_shards, MLA_ALL_SHARDS));
-  const size_t rows = (size_t)num_shards * shape->batch * shape->q_len * shape->num_heads;
+  const size_t rows1 = (size_t)shape->batch * shape->q_len * shape->num_heads;
+  const size_t rows = (size_t)num_shards * rows1;
   s.part = s.partial_ws;
   s.part_lse = s.part + up(rows * kDv * sizeof(float));
-  s.total = s.part_lse + up(rows * sizeof(float));
+  s.obf = s.part_lse + up(rows * sizeof(float));
+  s.total = s.obf + up(rows1 * kDv * sizeof(uint16_t));
   return s;
 }
+
+// Rows per head from which the fused W_UV projection runs as a tensor-core
+// GEMM per head (after a combine that writes O) instead of on the CUDA cores
+// inside the combine.
+constexpr int kWuvGemmMinRows = 64;
 
 }  // namespace
 
@@ -487,9 +498,23 @@ mla_status mla_decode_step(const void* q, const mla_kv_pages* kv, const int32_t*
                                        MLA_ALL_SHARDS, num_shards, layout, part, part_lse,
                                        workspace, sl.partial_ws, stream, &L);
   if (st != MLA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int rows_per_head = shape->batch * shape->q_len;
+  if (w_uv != nullptr && rows_per_head >= kWuvGemmMinRows) {
+    // many rows per head: the combine writes O (bf16) into the workspace and
+    // one tcgen05 GEMM per head projects it
+    uint16_t* obf = reinterpret_cast<uint16_t*>(ws + sl.obf);
+    if (launch_step_combine(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, part, part_lse, nullptr,
+                            obf, lse_out, cs) != cudaSuccess ||
+        launch_wuv_gemm(obf, static_cast<const uint16_t*>(w_uv), static_cast<uint16_t*>(out),
+                        rows_per_head, shape->num_heads, &L.hdr->err,
+                        host::wait_budget_ns(kTimeoutNs), cs) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    return MLA_OK;
+  }
   if (launch_step_combine(L.pd, L.hdr, L.prefix, L.ws_o, L.ws_lse, part, part_lse,
                           static_cast<const uint16_t*>(w_uv), static_cast<uint16_t*>(out),
-                          lse_out, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                          lse_out, cs) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -131,9 +131,15 @@ def test_config2_bimodal_agentic(dev):
     check_sampled(w, res, rows, w.num_shards, w.layout)
 
 
-@pytest.mark.parametrize("cfg", [2, 4, 5])
+@pytest.mark.parametrize("cfg", [2, 4, 5, "4+wuv"])
 def test_decode_step_full_size(dev, cfg):
-    w = mi.config_workload(cfg)
+    """cfg "4+wuv": the q_len-9 batch with a W_UV projection, 144 query rows
+    per head, which runs on the tensor cores after the combine."""
+    if cfg == "4+wuv":
+        w = mi.config_workload(4, with_w_uv=True)
+        cfg = 4
+    else:
+        w = mi.config_workload(cfg)
     n = check_step(w, dev, sample_rows(w, n_random=6, seed=20 + cfg))
     assert n >= 8
 

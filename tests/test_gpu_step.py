@@ -71,6 +71,22 @@ def test_step_wuv_many_rows_per_head(dev):
     check_step(w, dev, with_wuv=True)
 
 
+@pytest.mark.parametrize("kv_dtype,B,q_len,q_lens", [
+    ("bf16", 8, 9, None),                                   # 72 rows per head: one ragged block
+    ("fp8", 16, 9, None),                                   # 144: a full block and a ragged one
+    ("bf16", 16, 5, [5, 1, 3, 5, 2, 5, 4, 1, 5, 5, 3, 2, 1, 5, 4, 5]),   # padding rows
+])
+def test_step_wuv_tensor_core_projection(dev, kv_dtype, B, q_len, q_lens):
+    """64 or more query rows per head: the combine writes o in bf16 and the
+    W_UV projection runs as one tcgen05 GEMM per head in blocks of 128 rows."""
+    lens = [37 + 911 * b % 3000 for b in range(B)]
+    w = mi.build_workload("step-wuv-tc", B, q_len, 32, lens, 2, "interleaved", kv_dtype, True,
+                          seed=1020 + B + q_len, with_w_uv=True, poison=True, q_lens=q_lens,
+                          kv_sigma=1.0 if kv_dtype == "fp8" else 0.5)
+    assert B * q_len >= 64
+    check_step(w, dev, with_wuv=True)
+
+
 def test_step_causal_and_padded_query_counts(dev):
     lens = [8000, 20, 3, 4100]
     w = mi.build_workload("step-q", len(lens), 9, 64, lens, 2, "interleaved", "bf16", True,
