@@ -211,28 +211,29 @@ __device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, 
   merge_pieces_ctx<kVec, kB>(src, ctx, lane, q0, acc, M, wsum, 0, ctx.count);
 }
 
-// Two warps per query row, one per 256-wide half of the 512 latent dims (a
-// lane owns two float4 of its half, so each load instruction of a warp reads
-// 512 contiguous bytes), eight pieces in flight per batch; a block of 256
-// threads handles four rows.
-template <class Src>
-__global__ void __launch_bounds__(256, 2) mla_combine_kernel(Src src, int rows,
-                                                             uint16_t* __restrict__ out,
-                                                             float* __restrict__ lse_out) {
+// Warp w handles part w % (4 / kVec) of row w / (4 / kVec) of its block: a
+// lane owns kVec float4 of the part's 128 kVec latent dims, so each load
+// instruction of a warp reads 512 contiguous bytes; kB pieces are in flight
+// per batch; at least kMinB blocks of 256 threads run per SM.
+template <class Src, int kMinB, int kVec, int kB>
+__global__ void __launch_bounds__(256, kMinB) mla_combine_kernel(Src src, int rows,
+                                                                 uint16_t* __restrict__ out,
+                                                                 float* __restrict__ lse_out) {
+  constexpr int kWarpsPerRow = 4 / kVec, kRowsPerBlock = 8 / kWarpsPerRow;
   griddep_wait();                // the partials
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + (warp >> 1), half = warp & 1;
+  const int row = blockIdx.x * kRowsPerBlock + warp / kWarpsPerRow, part = warp % kWarpsPerRow;
   if (row >= rows) return;
-  float4 acc[2];
+  float4 acc[kVec];
   float M, wsum;
-  merge_pieces<2, 8>(src, row, lane, 64 * half, acc, M, wsum);
+  merge_pieces<kVec, kB>(src, row, lane, 32 * kVec * part, acc, M, wsum);
   const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
   uint2* dst = reinterpret_cast<uint2*>(out + (size_t)row * kDv);
 #pragma unroll
-  for (int v = 0; v < 2; ++v)
-    dst[64 * half + lane + 32 * v] = make_uint2(pack2(acc[v].x * inv, acc[v].y * inv),
-                                                pack2(acc[v].z * inv, acc[v].w * inv));
-  if (lse_out != nullptr && half == 0 && lane == 0)
+  for (int v = 0; v < kVec; ++v)
+    dst[32 * kVec * part + lane + 32 * v] = make_uint2(pack2(acc[v].x * inv, acc[v].y * inv),
+                                                     pack2(acc[v].z * inv, acc[v].w * inv));
+  if (lse_out != nullptr && part == 0 && lane == 0)
     lse_out[row] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
 }
 
@@ -375,17 +376,26 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
   cluster.sync();                // peers' shared memory stays alive until read
 }
 
+// The combine is latency-bound.  Many rows (with few pieces each, e.g. a
+// verify batch of 9,216 rows) want many blocks per SM; fewer rows, where long
+// requests bring dozens of pieces per row, want more pieces in flight per warp
+// (measured: 31.1 -> 22.4 us on the q_len-9 batch, 21.0 -> 19.5 us on the
+// bimodal batch against one shape for both).
+constexpr int kManyRows = 4096;
+
 template <class Src>
 cudaError_t launch_combine_impl(const Src& src, int rows, uint16_t* out, float* lse_out,
                                 cudaStream_t stream) {
+  const bool many = rows >= kManyRows;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ceil_div(rows, 4));
+  cfg.gridDim = dim3(ceil_div(rows, many ? 4 : 2));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src>, src, rows, out, lse_out);
+  if (many) return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src, 4, 2, 2>, src, rows, out, lse_out);
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src, 4, 1, 4>, src, rows, out, lse_out);
 }
 
 template <class Src>
