@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole page
     const int nv = (pd.layout == kInterleaved && kLocal != 1) ? pd.ppt : 1;
     const int box_bytes = kCgBytes / nv;     // one chunk group of one page's slots
+    // Every wait on a chunk group's release costs the producer a wake-up
+    // before its boxes go out.  With four or more boxes per chunk group
+    // (interleaved shards of a global cache) chunk groups 1 and 2 go out
+    // together after one wait; with fewer, each waits for its own release.
+    const bool join12 = (kLocal == 2 ? 8 : nv) >= 4;
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -269,18 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pgk = __shfl_sync(0xffffffffu, page, k & 31);
           r0 = shard_row0(x.s, first_slot + k, pd.num_shards) + 8 * pd.num_shards * g;
         }
-#pragma unroll 1
-        for (int cg = 0; cg < kCg; ++cg) {
-          if (gt >= 2) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(empty + 8 * cg, ((gt >> 1) - 1) & 1, tmo, abort_flag));
-            if (!ok) break;
-          }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
-            armed_kv[st][cg] = gt;
-          }
-          __syncwarp();
+        auto issue_cg = [&](int cg) {
           if (kLocal == 2) {
             if (lane < 8)
               tma_load_4d(sKV + st * kTileBytes + cg * kCgBytes + lane * kGroupBytes, &tm_kv,
@@ -291,8 +285,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_5d(sKV + st * kTileBytes + cg * kCgBytes + lane * box_bytes, &tm_kv,
                         full + 8 * cg, 0, 0, kCgChunks * cg, 0, page * kPage + res);
           }
-          __syncwarp();
+          armed_kv[st][cg] = gt;   // the teardown drains issued copies only
+        };
+        auto wait_free = [&](int cg) {
+          return gt < 2 || __all_sync(0xffffffffu, mbar_wait(empty + 8 * cg, ((gt >> 1) - 1) & 1,
+                                                             tmo, abort_flag));
+        };
+        ok = wait_free(0);
+        if (!ok) break;
+        // chunk group 0's release implies that tile gt - 2 landed whole (its
+        // QK^T is done), so all three full barriers can be armed now
+        if (lane == 0) {
+#pragma unroll
+          for (int cg = 0; cg < kCg; ++cg) mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
         }
+        __syncwarp();
+        issue_cg(0);
+        if (join12) {
+          // chunk group 2's release implies chunk group 1's: one thread
+          // issues the P.V blocks and their commits in order
+          ok = wait_free(2);
+          if (ok) {
+            issue_cg(1);
+            issue_cg(2);
+          }
+        } else {
+          ok = wait_free(1);
+          if (ok) issue_cg(1);
+          ok = ok && wait_free(2);
+          if (ok) issue_cg(2);
+        }
+        __syncwarp();
         if (!ok) break;
         if (ok && j == t0) {
           // query rows of this unit: reuse of the buffer waits for the last
