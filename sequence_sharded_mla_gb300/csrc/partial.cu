@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 }  // namespace
 
-template <int kLocal, bool kRankIo>
+template <int kLocal, bool kRankIo, bool kJoin12>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_partial_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_kv,
@@ -205,11 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whole page
     const int nv = (pd.layout == kInterleaved && kLocal != 1) ? pd.ppt : 1;
     const int box_bytes = kCgBytes / nv;     // one chunk group of one page's slots
-    // Every wait on a chunk group's release costs the producer a wake-up
-    // before its boxes go out.  With four or more boxes per chunk group
-    // (interleaved shards of a global cache) chunk groups 1 and 2 go out
-    // together after one wait; with fewer, each waits for its own release.
-    const bool join12 = (kLocal == 2 ? 8 : nv) >= 4;
     int gt = 0, pc = 0;
     bool ok = true;
     while (ok && it.next(unit, t0, t1, whole, slot)) {
@@ -285,37 +280,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_5d(sKV + st * kTileBytes + cg * kCgBytes + lane * box_bytes, &tm_kv,
                         full + 8 * cg, 0, 0, kCgChunks * cg, 0, page * kPage + res);
           }
-          armed_kv[st][cg] = gt;   // the teardown drains issued copies only
         };
         auto wait_free = [&](int cg) {
           return gt < 2 || __all_sync(0xffffffffu, mbar_wait(empty + 8 * cg, ((gt >> 1) - 1) & 1,
                                                              tmo, abort_flag));
         };
-        ok = wait_free(0);
-        if (!ok) break;
-        // chunk group 0's release implies that tile gt - 2 landed whole (its
-        // QK^T is done), so all three full barriers can be armed now
-        if (lane == 0) {
+        if (kJoin12) {
+          // Every wait costs the producer a wake-up before its boxes go out;
+          // with four or more boxes per chunk group, chunk groups 1 and 2 go
+          // out together after one wait.  Chunk group 0's release implies
+          // that tile gt - 2 landed whole (its QK^T is done), so all three
+          // full barriers are armed at once.
+          ok = wait_free(0);
+          if (!ok) break;
+          if (lane == 0) {
 #pragma unroll
-          for (int cg = 0; cg < kCg; ++cg) mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
-        }
-        __syncwarp();
-        issue_cg(0);
-        if (join12) {
+            for (int cg = 0; cg < kCg; ++cg) mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
+          }
+          __syncwarp();
+          issue_cg(0);
+          if (lane == 0) armed_kv[st][0] = gt;   // the teardown drains issued copies only
           // chunk group 2's release implies chunk group 1's: one thread
           // issues the P.V blocks and their commits in order
           ok = wait_free(2);
           if (ok) {
             issue_cg(1);
             issue_cg(2);
+            if (lane == 0) armed_kv[st][1] = armed_kv[st][2] = gt;
           }
+          __syncwarp();
         } else {
-          ok = wait_free(1);
-          if (ok) issue_cg(1);
-          ok = ok && wait_free(2);
-          if (ok) issue_cg(2);
+#pragma unroll 1
+          for (int cg = 0; cg < kCg; ++cg) {
+            ok = wait_free(cg);
+            if (!ok) break;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full + 8 * cg, kCgBytes);
+              armed_kv[st][cg] = gt;
+            }
+            __syncwarp();
+            issue_cg(cg);
+            __syncwarp();
+          }
         }
-        __syncwarp();
         if (!ok) break;
         if (ok && j == t0) {
           // query rows of this unit: reuse of the buffer waits for the last
@@ -698,12 +705,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int partial_smem_bytes() { return kSmemBytes; }
 
-template <int kLocal, bool kRankIo = false>
+template <int kLocal, bool kRankIo, bool kJoin12>
 static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                   const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                   cudaStream_t stream) {
   const cudaError_t e =
-      host::ensure_dynamic_smem(reinterpret_cast<const void*>(&mla_partial_kernel<kLocal, kRankIo>), kSmemBytes);
+      host::ensure_dynamic_smem(
+          reinterpret_cast<const void*>(&mla_partial_kernel<kLocal, kRankIo, kJoin12>), kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -713,20 +721,27 @@ static cudaError_t launch_partial(const CUtensorMap& tm_q, const CUtensorMap& tm
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal, kRankIo>, tm_q, tm_kv, tm_kv_pf, p);
+  return cudaLaunchKernelEx(&cfg, mla_partial_kernel<kLocal, kRankIo, kJoin12>, tm_q, tm_kv, tm_kv_pf,
+                            p);
 }
 
 // The cache kind (whole requests, a local slice, or whole requests with
 // interleaved shards whose count does not divide the page) is a template
 // parameter: branching on it at run time cost about 2% on the bimodal batch.
+// So is the producer's wait policy, set by the TMA boxes per chunk group: a
+// whole-cache tile of N interleaved shards (N | 64) has N boxes per chunk
+// group, one N ∤ 64 has eight, a contiguous or local tile one.
 cudaError_t launch_partial_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
                                 const CUtensorMap& tm_kv_pf, const PartialParams& p, int grid,
                                 cudaStream_t stream) {
   // the DCP rank-major I/O (local caches only) is an instantiation of its own
-  if (p.pd.rank_heads != 0) return launch_partial<1, true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
-  return p.pd.local ? launch_partial<1>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
-         : p.pd.pad   ? launch_partial<2>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
-                      : launch_partial<0>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
+  if (p.pd.rank_heads != 0)
+    return launch_partial<1, true, false>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
+  if (p.pd.local) return launch_partial<1, false, false>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
+  if (p.pd.pad) return launch_partial<2, false, true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
+  const int boxes = p.pd.layout == kInterleaved ? p.pd.ppt : 1;
+  return boxes >= 4 ? launch_partial<0, false, true>(tm_q, tm_kv, tm_kv_pf, p, grid, stream)
+                    : launch_partial<0, false, false>(tm_q, tm_kv, tm_kv_pf, p, grid, stream);
 }
 
 }  // namespace mla
