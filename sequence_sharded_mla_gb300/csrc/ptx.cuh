@@ -184,6 +184,21 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared, cached in L2 only; both
+// addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Until every committed cp.async copy of this thread has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // Arrive on `bar` once all of this thread's earlier cp.async copies are done
 // (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
