@@ -350,58 +350,18 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
   }
   cp_async_wait_all();           // this thread's W_UV copies
   __syncthreads();
-  // the merge's per-warp sums are consumed: their space holds the projection
-  // of each quarter of the CTA's latent dims
-  float (*ypart)[kWuvRows][kDuv] = reinterpret_cast<float (*)[kWuvRows][kDuv]>(&sm.red[0][0][0]);
   {
-    // thread (g, p): output columns 2p and 2p + 1 over dims [32 g, 32 g + 32)
-    // of every row, so that each W_UV pair is read and widened once
-    const int p = tid & (kDuv / 2 - 1), g = tid >> 6;
-    float acc[kWuvRows][2];
+    // thread (rh, c): output column c, rows 4 rh .. 4 rh + 3
+    const int c = tid & (kDuv - 1), rh = tid >> 7;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int d = 0; d < kWuvDims; ++d) {
+      const float w = __uint_as_float(((uint32_t)sm.wsm[d][c]) << 16);
 #pragma unroll
-    for (int r = 0; r < kWuvRows; ++r) acc[r][0] = acc[r][1] = 0.f;
-#pragma unroll
-    for (int d0 = 0; d0 < kWuvDims / 4; d0 += 4) {
-      const int d = (kWuvDims / 4) * g + d0;
-      float w0[4], w1[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t wv = *reinterpret_cast<const uint32_t*>(&sm.wsm[d + e][2 * p]);
-        w0[e] = __uint_as_float(wv << 16);
-        w1[e] = __uint_as_float(wv & 0xffff0000u);
-      }
-#pragma unroll
-      for (int r = 0; r < kWuvRows; ++r) {
-        if (r < nr) {
-          const float4 s4 = *reinterpret_cast<const float4*>(&sm.so[r][d]);
-          acc[r][0] = fmaf(s4.x, w0[0], acc[r][0]);
-          acc[r][1] = fmaf(s4.x, w1[0], acc[r][1]);
-          acc[r][0] = fmaf(s4.y, w0[1], acc[r][0]);
-          acc[r][1] = fmaf(s4.y, w1[1], acc[r][1]);
-          acc[r][0] = fmaf(s4.z, w0[2], acc[r][0]);
-          acc[r][1] = fmaf(s4.z, w1[2], acc[r][1]);
-          acc[r][0] = fmaf(s4.w, w0[3], acc[r][0]);
-          acc[r][1] = fmaf(s4.w, w1[3], acc[r][1]);
-        }
-      }
+      for (int r = 0; r < 4; ++r) a[r] = fmaf(sm.so[4 * rh + r][d], w, a[r]);
     }
 #pragma unroll
-    for (int r = 0; r < kWuvRows; ++r)
-      if (r < nr) *reinterpret_cast<float2*>(&ypart[g][r][2 * p]) = make_float2(acc[r][0], acc[r][1]);
-  }
-  __syncthreads();
-  {
-    // row r: the four quarters' sums, in quarter order
-    const int r = warp;
-    if (r < nr) {
-      float4 v = *reinterpret_cast<const float4*>(&ypart[0][r][4 * lane]);
-#pragma unroll
-      for (int g = 1; g < 4; ++g) {
-        const float4 a = *reinterpret_cast<const float4*>(&ypart[g][r][4 * lane]);
-        v = make_float4(v.x + a.x, v.y + a.y, v.z + a.z, v.w + a.w);
-      }
-      *reinterpret_cast<float4*>(&sm.yp[r][4 * lane]) = v;
-    }
+    for (int r = 0; r < 4; ++r) sm.yp[4 * rh + r][c] = a[r];
   }
   cluster.sync();                // every CTA's partial projection is complete
   {
