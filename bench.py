@@ -384,7 +384,15 @@ def mla_case(args, rank, dev, stream, ev_p, ev_k, ev_c):
               "causal": bool(w.causal), "fused_w_uv": d_wuv is not None,
               "total_tokens_per_gpu": w.total_tokens}
     fp8 = w.kv_dtype == "fp8"
-    kernel = "mla_partial_fp8_kernel<false>" if fp8 else "mla_partial_kernel<false>"
+    # the template instance the library launches: cache kind (0 whole
+    # requests, 2 interleaved shards that do not divide the page), and for
+    # bf16 whether the producer waits once for chunk groups 1 and 2 (four or
+    # more boxes per chunk group)
+    pad = layout == "interleaved" and 64 % N != 0
+    kind = 2 if pad else 0
+    boxes = 8 if pad else (N if layout == "interleaved" else 1)
+    kernel = (f"mla_partial_fp8_kernel<{kind}, false>" if fp8 else
+              f"mla_partial_kernel<{kind}, false, {'true' if boxes >= 4 else 'false'}>")
     rows = B * q_len * H
     flops = 2.0 * H * (576 + 512) * visible_pairs(w.seq_lens, q_len, w.causal)
     comb = N * rows * (512 * 4 + 4) + rows * ((128 if d_wuv is not None else 512) * 2 + 4)
@@ -728,7 +736,7 @@ def run_dcp(args, world, rank, dist, device, workload=None, partial_fn=None, com
     }
     if kernel_ms is not None:
         achieved = local_kv / (kms / 1e3) / 1e9
-        line["roofline"] = {"kernel": "mla_partial_kernel<1, true> (local cache, DCP I/O)"
+        line["roofline"] = {"kernel": "mla_partial_kernel<1, true, false> (local cache, DCP I/O)"
                             if w.kv_dtype == "bf16" else
                             "mla_partial_fp8_kernel<1, true> (local cache, DCP I/O)",
                             "launches": args.dcp_chunks, "bound": "hbm",
