@@ -205,11 +205,73 @@ __device__ __forceinline__ void merge_pieces_ctx(const Src& src, const typename 
   wsum = ws;
 }
 
+// The same merge with each batch staged in shared memory by cp.async: a
+// lane copies its kVec float4 of each of the batch's kB pieces into `stage`
+// (this warp's [kB][kVec * 32] float4) and reads back only what it copied, so
+// the batch's bytes in flight hold no registers and kB can be several times
+// what the register file allows.
 template <int kVec, int kB, class Src>
-__device__ __forceinline__ void merge_pieces(const Src& src, int row, int lane, int q0,
-                                             float4 (&acc)[kVec], float& M, float& wsum) {
-  const typename Src::Ctx ctx = src.prepare(row, lane);
-  merge_pieces_ctx<kVec, kB>(src, ctx, lane, q0, acc, M, wsum, 0, ctx.count);
+__device__ __forceinline__ void merge_pieces_staged(const Src& src, const typename Src::Ctx& ctx,
+                                                    int lane, int q0, float4* stage,
+                                                    float4 (&acc)[kVec], float& M, float& wsum) {
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  M = -CUDART_INF_F;
+  float ws = 0.f;
+  const int kend = ctx.count;
+  for (int k0 = 0; k0 < kend; k0 += 32) {
+    const float* p;
+    float l;
+    src.piece(ctx, min(k0 + lane, kend - 1), p, l);
+    if (k0 + lane >= kend) l = -CUDART_INF_F;
+    const unsigned long long pa = reinterpret_cast<unsigned long long>(p);
+    const int n = min(32, kend - k0);
+    for (int j = 0; j < n; j += kB) {
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj) {
+        const float4* s4 = reinterpret_cast<const float4*>(__shfl_sync(0xffffffffu, pa, j + jj));
+        if (j + jj < n) {
+#pragma unroll
+          for (int v = 0; v < kVec; ++v)
+            cp_async_16(smem_u32(stage + jj * (32 * kVec) + lane + 32 * v), s4 + q0 + lane + 32 * v);
+        }
+      }
+      cp_async_commit();
+      float mb = (lane >= j && lane < j + kB) ? l : -CUDART_INF_F;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+      cp_async_wait_all();
+      if (mb > M) {
+        const float sc = M == -CUDART_INF_F ? 0.f : __expf(M - mb);
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+          acc[v].x *= sc;
+          acc[v].y *= sc;
+          acc[v].z *= sc;
+          acc[v].w *= sc;
+        }
+        ws *= sc;
+        M = mb;
+      }
+      if (M == -CUDART_INF_F) continue;   // nothing seen yet: every lse so far is -inf
+#pragma unroll
+      for (int jj = 0; jj < kB; ++jj) {
+        const float w = __expf(__shfl_sync(0xffffffffu, l, j + jj) - M);
+        if (j + jj < n) {
+          ws += w;
+#pragma unroll
+          for (int v = 0; v < kVec; ++v) {
+            const float4 o = stage[jj * (32 * kVec) + lane + 32 * v];
+            acc[v].x = fmaf(w, o.x, acc[v].x);
+            acc[v].y = fmaf(w, o.y, acc[v].y);
+            acc[v].z = fmaf(w, o.z, acc[v].z);
+            acc[v].w = fmaf(w, o.w, acc[v].w);
+          }
+        }
+      }
+    }
+  }
+  wsum = ws;
 }
 
 // Warp w handles part w % (4 / kVec) of row w / (4 / kVec) of its block: a
@@ -221,13 +283,16 @@ __global__ void __launch_bounds__(256, kMinB) mla_combine_kernel(Src src, int ro
                                                                  uint16_t* __restrict__ out,
                                                                  float* __restrict__ lse_out) {
   constexpr int kWarpsPerRow = 4 / kVec, kRowsPerBlock = 8 / kWarpsPerRow;
+  extern __shared__ __align__(16) float4 combine_stage[];   // [8 warps][kB][kVec * 32]
   griddep_wait();                // the partials
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + warp / kWarpsPerRow, part = warp % kWarpsPerRow;
   if (row >= rows) return;
   float4 acc[kVec];
   float M, wsum;
-  merge_pieces<kVec, kB>(src, row, lane, 32 * kVec * part, acc, M, wsum);
+  const typename Src::Ctx ctx = src.prepare(row, lane);
+  merge_pieces_staged<kVec, kB>(src, ctx, lane, 32 * kVec * part,
+                                combine_stage + warp * (kB * 32 * kVec), acc, M, wsum);
   const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
   uint2* dst = reinterpret_cast<uint2*>(out + (size_t)row * kDv);
 #pragma unroll
@@ -387,20 +452,34 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
 // (measured: 31.1 -> 22.4 us on the q_len-9 batch, 21.0 -> 19.5 us on the
 // bimodal batch against one shape for both).
 constexpr int kManyRows = 4096;
+// pieces per staged batch: 8 warps x kB x 512 B (one float4 per lane) or
+// x 1 KB (two) is 48 KB of shared memory per block, four blocks per SM
+constexpr int kFewB = 12, kManyB = 6;
 
-template <class Src>
-cudaError_t launch_combine_impl(const Src& src, int rows, uint16_t* out, float* lse_out,
-                                cudaStream_t stream) {
-  const bool many = rows >= kManyRows;
+template <class Src, int kMinB, int kVec, int kB>
+cudaError_t launch_combine_shape(const Src& src, int rows, uint16_t* out, float* lse_out,
+                                 cudaStream_t stream) {
+  constexpr int kRowsPerBlock = 2 * kVec;
+  constexpr int smem = 8 * kB * 32 * kVec * (int)sizeof(float4);
+  const cudaError_t e = host::ensure_dynamic_smem(
+      reinterpret_cast<const void*>(&mla_combine_kernel<Src, kMinB, kVec, kB>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ceil_div(rows, many ? 4 : 2));
+  cfg.gridDim = dim3(ceil_div(rows, kRowsPerBlock));
   cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  if (many) return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src, 4, 2, 2>, src, rows, out, lse_out);
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src, 4, 1, 4>, src, rows, out, lse_out);
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel<Src, kMinB, kVec, kB>, src, rows, out, lse_out);
+}
+
+template <class Src>
+cudaError_t launch_combine_impl(const Src& src, int rows, uint16_t* out, float* lse_out,
+                                cudaStream_t stream) {
+  if (rows >= kManyRows) return launch_combine_shape<Src, 4, 2, kManyB>(src, rows, out, lse_out, stream);
+  return launch_combine_shape<Src, 4, 1, kFewB>(src, rows, out, lse_out, stream);
 }
 
 template <class Src>
