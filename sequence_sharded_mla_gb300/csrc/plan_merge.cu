@@ -14,6 +14,8 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "host_util.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace mla {
@@ -33,99 +35,67 @@ __global__ void __launch_bounds__(1024) mla_plan_kernel(ProblemDesc pd, WsHeader
              grid, min_tiles, unit_cost, bad_qlen);
 }
 
-// Block (u, y) handles query rows [4y, 4y + 4) of unit u, one warp per row:
-// the warp forms the row's piece weights once (in shared memory), then each
-// lane accumulates 16 of the 512 latent dims over the pieces.
-constexpr int kMergeRowsPerBlock = 4;
-constexpr int kMaxPieces = 512;    // pieces of one unit <= persistent CTAs
+// The pieces of a split unit: CTA c0 + k's piece of the unit, in the
+// workspace slot it wrote (a CTA writes its first piece to slot 0 and its
+// last to slot 1; the unit's first CTA had an earlier piece iff its range
+// starts before the unit's positions).
+struct UnitPieces {
+  const float* ws_o;
+  const float* ws_lse;
+  struct Ctx {
+    int c0, count, r, first_in_slot1;
+  };
+  __device__ void piece(const Ctx& c, int k, const float*& src, float& lse) const {
+    const size_t cc = (size_t)(c.c0 + k);
+    const size_t slot = (k == 0 && c.first_in_slot1) ? 2 * cc + 1 : 2 * cc;
+    src = ws_o + (slot * kRows + c.r) * kDv;
+    lse = ws_lse[slot * kRows + c.r];
+  }
+};
 
-__global__ void __launch_bounds__(32 * kMergeRowsPerBlock) mla_merge_kernel(
+// Block (u, y) handles query rows 2y and 2y + 1 of unit u with four warps
+// per row, each merging 128 of the 512 latent dims over the unit's pieces
+// (kMergeBatch pieces in flight per warp).
+constexpr int kMergeRowsPerBlock = 2;
+constexpr int kMergeBatch = 12;
+constexpr int kMergeSmem = 8 * kMergeBatch * 32 * (int)sizeof(float4);
+
+__global__ void __launch_bounds__(256, 4) mla_merge_kernel(
     ProblemDesc pd, const WsHeader* hdr, const int* prefix, const float* ws_o,
     const float* ws_lse, float* out_partial, float* lse_partial) {
-  __shared__ float wts[kMergeRowsPerBlock][kMaxPieces];
+  extern __shared__ __align__(16) float4 merge_stage[];   // [8 warps][kMergeBatch][32]
   griddep_wait();                // the partial kernel's pieces and outputs
   griddep_launch_dependents();
   const int u = blockIdx.x;
   const Unit x = make_unit(pd, u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * kMergeRowsPerBlock + warp;
+  const int r = blockIdx.y * kMergeRowsPerBlock + (warp >> 2), part = warp & 3;
   if (r >= x.rows_out) return;
   const int ps = prefix[u], ue = prefix[u + 1];
   const int us = unit_tile_start(prefix, u, hdr->unit_cost);
   const size_t orow = out_row(pd, x, r);
-  float4* dst = reinterpret_cast<float4*>(out_partial + orow * kDv);
+  float4* dst = reinterpret_cast<float4*>(out_partial + orow * kDv) + 32 * part;
   const int per = hdr->per_cta;
   const bool split = us < ue && us / per != (ue - 1) / per;
   // rows with no token to see: the shard holds none of the request's
   // positions, or the row is padding of a request with fewer query tokens
   // (a whole unit's padding rows are written by the partial kernel)
   if (us == ue || (split && r >= x.rows)) {
-    for (int v = lane; v < kDv / 4; v += 32) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) lse_partial[orow] = -CUDART_INF_F;
+    dst[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (part == 0 && lane == 0) lse_partial[orow] = -CUDART_INF_F;
     return;
   }
   const int c0 = us / per, c1 = (ue - 1) / per;
   if (c0 == c1) return;  // written directly by the partial kernel
-  const int np = c1 - c0 + 1;
-  // a CTA writes its first piece to slot 0 and its last to slot 1; the first
-  // CTA of the unit had an earlier piece iff its range starts before the
-  // unit's positions (the position before them is another unit's tile)
-  auto slot_of = [&](int c) -> size_t {
-    return (c == c0 && c0 * per < ps) ? 2 * (size_t)c + 1 : 2 * (size_t)c;
-  };
-  // the first two pieces' rows are loaded before the weights are known, so
-  // their latency overlaps the LSE reduction (most split units have two)
-  float4 o0[4], o1[4];
-  {
-    const float4* s0 = reinterpret_cast<const float4*>(ws_o + (slot_of(c0) * kRows + r) * kDv);
-    const float4* s1 = reinterpret_cast<const float4*>(ws_o + (slot_of(c0 + 1) * kRows + r) * kDv);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o0[i] = s0[lane + 32 * i];
-      o1[i] = s1[lane + 32 * i];
-    }
-  }
-  float M = -CUDART_INF_F;
-  for (int k = lane; k < np; k += 32) M = fmaxf(M, ws_lse[slot_of(c0 + k) * kRows + r]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float wsum = 0.f;
-  for (int k = lane; k < np; k += 32) {
-    const float w = M > -CUDART_INF_F ? __expf(ws_lse[slot_of(c0 + k) * kRows + r] - M) : 0.f;
-    wts[warp][k] = w;
-    wsum += w;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-  __syncwarp();
-  float4 acc[4];
-  {
-    const float w0 = wts[warp][0], w1 = wts[warp][1];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[i].x = w0 * o0[i].x + w1 * o1[i].x;
-      acc[i].y = w0 * o0[i].y + w1 * o1[i].y;
-      acc[i].z = w0 * o0[i].z + w1 * o1[i].z;
-      acc[i].w = w0 * o0[i].w + w1 * o1[i].w;
-    }
-  }
-  for (int k = 2; k < np; ++k) {
-    const float w = wts[warp][k];
-    const float4* src = reinterpret_cast<const float4*>(ws_o + (slot_of(c0 + k) * kRows + r) * kDv);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 o = src[lane + 32 * i];
-      acc[i].x += w * o.x;
-      acc[i].y += w * o.y;
-      acc[i].z += w * o.z;
-      acc[i].w += w * o.w;
-    }
-  }
+  const UnitPieces src{ws_o, ws_lse};
+  const UnitPieces::Ctx ctx{c0, c1 - c0 + 1, r, c0 * per < ps ? 1 : 0};
+  float4 acc[1];
+  float M, wsum;
+  merge_pieces_staged<1, kMergeBatch>(src, ctx, lane, 32 * part,
+                                      merge_stage + warp * (kMergeBatch * 32), acc, M, wsum);
   const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    dst[lane + 32 * i] = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
-  if (lane == 0) lse_partial[orow] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
+  dst[lane] = make_float4(acc[0].x * inv, acc[0].y * inv, acc[0].z * inv, acc[0].w * inv);
+  if (part == 0 && lane == 0) lse_partial[orow] = wsum > 0.f ? M + __logf(wsum) : -CUDART_INF_F;
 }
 
 cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int grid,
@@ -137,9 +107,13 @@ cudaError_t launch_plan(const ProblemDesc& pd, WsHeader* hdr, int* prefix, int g
 cudaError_t launch_merge(const ProblemDesc& pd, const WsHeader* hdr, const int* prefix,
                          const float* ws_o, const float* ws_lse, float* out_partial,
                          float* lse_partial, int num_units, cudaStream_t stream) {
+  const cudaError_t e =
+      host::ensure_dynamic_smem(reinterpret_cast<const void*>(&mla_merge_kernel), kMergeSmem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_units, kRows / kMergeRowsPerBlock);
-  cfg.blockDim = dim3(32 * kMergeRowsPerBlock);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = kMergeSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr = pdl_attribute();
   cfg.attrs = &attr;
