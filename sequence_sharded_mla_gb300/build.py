@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libmla_dcp.so")
 SOURCES = ["partial.cu", "partial_fp8.cu", "wuv_gemm.cu", "plan_merge.cu", "combine.cu", "capi.cu", "noalloc.cu", "gqa.cu"]
-HEADERS = ["common.cuh", "ptx.cuh", "host_util.h"]
+HEADERS = ["common.cuh", "merge.cuh", "ptx.cuh", "host_util.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
