@@ -727,8 +727,9 @@ def run_dcp(args, world, rank, dist, device, workload=None, partial_fn=None, com
                          "inputs not flushed from L2",
                    "parallelism": f"dcp{world}: one sequence shard per GPU, query all-gather, "
                                   "head-sliced all-to-all of the partials, combine per head "
-                                  f"slice; {args.dcp_chunks} request group(s) whose exchange "
-                                  "overlaps the next group's partial"},
+                                  f"slice; {args.dcp_chunks} request group(s)"
+                                  + (", each group's exchange overlapping the next group's "
+                                     "partial" if args.dcp_chunks > 1 else "")},
         "exchange": dict(dcp_exchange_bytes(w, world), chunks=args.dcp_chunks,
                          step_ms=ms, partial_kernel_ms_max=kms if kernel_ms is not None else None,
                          outside_partial_kernel_ms=(ms - kms) if kernel_ms is not None else None),
@@ -905,9 +906,10 @@ def main():
                          "the DCP step over one global batch")
     ap.add_argument("--dcp", action="store_true",
                     help="run the DCP step also at --gpus 1 (an exchange-free check of its path)")
-    ap.add_argument("--dcp-chunks", type=int, default=2,
+    ap.add_argument("--dcp-chunks", type=int, default=1,
                     help="DCP step: request groups whose exchange overlaps the next group's "
-                         "partial attention")
+                         "partial attention (each group is a launch of its own, with its own "
+                         "start and tail: more than one pays only when the exchange is long)")
     ap.add_argument("--sweep", action="store_true",
                     help="with --config 3: the shard-count sweep, N = 1, 2, 4, 8 in both "
                          "layouts over one seeded cache (one JSON line with a table)")
