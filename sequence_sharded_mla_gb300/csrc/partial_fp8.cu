@@ -816,13 +816,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             il[4 * c4 + 2] = t.z;
             il[4 * c4 + 3] = t.w;
           }
+          // DCP I/O: each aligned group of 8 rows has 8 consecutive
+          // destination rows (a rank's heads are a multiple of 8), so the 32
+          // rows take 4 base addresses from the table and every store an
+          // immediate offset from one of them: a lookup per store sits on
+          // the softmax warps' critical path (one warp per scheduler)
+          float* b8[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            b8[q4] = kRankIo ? obase + (size_t)misc->orow[32 * (k & 1) + 8 * q4] * kDv + dim
+                             : obase + (row0 + 32 * (k & 1) + 8 * q4) * kDv + dim;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int row = 32 * (k & 1) + c;
-            if (row < x.rows) {
-              if (kRankIo) obase[(size_t)misc->orow[row] * kDv + dim] = __uint_as_float(v[c]) * il[c];
-              else obase[(row0 + row) * kDv + dim] = __uint_as_float(v[c]) * il[c];
-            }
+            if (row < x.rows) b8[c >> 3][(c & 7) * kDv] = __uint_as_float(v[c]) * il[c];
           }
         };
         uint32_t va[32], vb[32];
