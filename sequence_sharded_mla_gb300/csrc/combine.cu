@@ -385,9 +385,12 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
 // (measured: 31.1 -> 22.4 us on the q_len-9 batch, 21.0 -> 19.5 us on the
 // bimodal batch against one shape for both).
 constexpr int kManyRows = 4096;
-// pieces per staged batch: 8 warps x kB x 512 B (one float4 per lane) or
-// x 1 KB (two) is 48 KB of shared memory per block, four blocks per SM
-constexpr int kFewB = 12, kManyB = 6;
+// Pieces per staged batch.  Fewer rows: four warps per row (one float4 per
+// lane), 12 pieces in flight per warp, 8 x 12 x 512 B = 48 KB per block.
+// Many rows: one warp per row (four float4 per lane, all 512 dims), 3 pieces
+// in flight, 8 x 3 x 2 KB = 48 KB: eight rows per block, half the blocks of
+// two warps per row.  Four blocks per SM either way.
+constexpr int kFewB = 12, kManyB = 3;
 
 template <class Src, int kMinB, int kVec, int kB>
 cudaError_t launch_combine_shape(const Src& src, int rows, uint16_t* out, float* lse_out,
@@ -411,7 +414,7 @@ cudaError_t launch_combine_shape(const Src& src, int rows, uint16_t* out, float*
 template <class Src>
 cudaError_t launch_combine_impl(const Src& src, int rows, uint16_t* out, float* lse_out,
                                 cudaStream_t stream) {
-  if (rows >= kManyRows) return launch_combine_shape<Src, 4, 2, kManyB>(src, rows, out, lse_out, stream);
+  if (rows >= kManyRows) return launch_combine_shape<Src, 4, 4, kManyB>(src, rows, out, lse_out, stream);
   return launch_combine_shape<Src, 4, 1, kFewB>(src, rows, out, lse_out, stream);
 }
 
