@@ -208,9 +208,10 @@ __device__ __forceinline__ void merge_pieces_ctx(const Src& src, const typename 
 
 
 // Warp w handles part w % (4 / kVec) of row w / (4 / kVec) of its block: a
-// lane owns kVec float4 of the part's 128 kVec latent dims, so each load
-// instruction of a warp reads 512 contiguous bytes; kB pieces are in flight
-// per batch; at least kMinB blocks of 256 threads run per SM.
+// lane owns kVec float4 of the part's 128 kVec latent dims, so each copy
+// instruction of a warp moves 512 contiguous bytes; kB pieces per batch are
+// in flight, staged in the warp's slice of dynamic shared memory; at least
+// kMinB blocks of 256 threads run per SM.
 template <class Src, int kMinB, int kVec, int kB>
 __global__ void __launch_bounds__(256, kMinB) mla_combine_kernel(Src src, int rows,
                                                                  uint16_t* __restrict__ out,
@@ -380,10 +381,9 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
 }
 
 // The combine is latency-bound.  Many rows (with few pieces each, e.g. a
-// verify batch of 9,216 rows) want many blocks per SM; fewer rows, where long
-// requests bring dozens of pieces per row, want more pieces in flight per warp
-// (measured: 31.1 -> 22.4 us on the q_len-9 batch, 21.0 -> 19.5 us on the
-// bimodal batch against one shape for both).
+// verify batch of 9,216 rows) want many rows in flight per SM; fewer rows,
+// where long requests bring dozens of pieces per row, want many pieces of
+// one row in flight.
 constexpr int kManyRows = 4096;
 // Pieces per staged batch.  Fewer rows: four warps per row (one float4 per
 // lane), 12 pieces in flight per warp, 8 x 12 x 512 B = 48 KB per block.
