@@ -386,11 +386,11 @@ __global__ void __cluster_dims__(kWuvSplit, 1, 1) __launch_bounds__(256, 2)
 // one row in flight.
 constexpr int kManyRows = 4096;
 // Pieces per staged batch.  Fewer rows: four warps per row (one float4 per
-// lane), 12 pieces in flight per warp, 8 x 12 x 512 B = 48 KB per block.
-// Many rows: one warp per row (four float4 per lane, all 512 dims), 3 pieces
-// in flight, 8 x 3 x 2 KB = 48 KB: eight rows per block, half the blocks of
-// two warps per row.  Four blocks per SM either way.
-constexpr int kFewB = 12, kManyB = 3;
+// lane), 16 pieces in flight per warp, 8 x 16 x 512 B = 64 KB per block,
+// three blocks per SM.  Many rows: one warp per row (four float4 per lane,
+// all 512 dims), 3 pieces in flight, 8 x 3 x 2 KB = 48 KB: eight rows per
+// block, half the blocks of two warps per row, four blocks per SM.
+constexpr int kFewB = 16, kManyB = 3;
 
 template <class Src, int kMinB, int kVec, int kB>
 cudaError_t launch_combine_shape(const Src& src, int rows, uint16_t* out, float* lse_out,
