@@ -29,7 +29,9 @@ With chunks = k > 1 the requests are cut into k groups: the all-to-all of a
 group's partials is started asynchronously (on NCCL's own stream on GPUs)
 and the next group's partial attention runs meanwhile, so the exchange
 overlaps compute; the combines follow once each exchange has landed, each
-into its requests' rows of the output.
+into its requests' rows of the output.  Every group is a launch of its own,
+with its own start and tail (tens of microseconds on a GB300), so more than
+one group pays only when the exchange takes longer than that.
 """
 from __future__ import annotations
 
@@ -128,7 +130,8 @@ def dcp_decode_step(q_local: torch.Tensor, kv: torch.Tensor, block_table: torch.
     mla_layout's *_LOCAL layouts).  seq_lens: the global lengths [B].
     w_uv_local: bf16 [H/N, 512, 128], W_UV of this rank's heads, or None.
     q_lens: optional int32 [B] query tokens per request of a padded batch.
-    chunks: request groups whose exchange overlaps the next group's compute.
+    chunks: request groups whose exchange overlaps the next group's compute
+    (1, the default: one launch over the whole batch).
     Returns (out [B, q_len, H/N, 512 | 128] bf16, lse [B, q_len, H/N] fp32).
 
     partial_fn / combine_fn replace the library's CUDA calls; the library's
